@@ -1,0 +1,418 @@
+"""Benchmark of the SplitZip GB300 codec: one step = encode + decode of the
+32-layer BF16 KV cache (32 x 2 x 32768 x 8 x 128 = 2,147,483,648 elements,
+4.29 GB), inputs resident in HBM.
+
+Prints one JSON line.  `value` is the round-trip throughput in GB/s of
+uncompressed bytes (bytes of the tensor / (encode + decode time)); encode and
+decode throughputs, the compression ratio, the escape rate and the derived
+link-transfer model are reported beside it.  `--impl reference` times the CPU
+oracle on a bounded sample of the same workload instead.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+Under torchrun each rank encodes/decodes its own copy of the workload (chunks
+are independent, no data exchange): weak scaling, max time over ranks.
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+METRIC = "encode/decode GB/s (uncompressed) on 1 GB300, % HBM roofline, ratio"
+WORKLOAD = "kv_cache_32x2x32768x8x128_bf16"
+CHUNK = 65536
+LINKS_GBS = (50.0, 100.0)
+
+
+def parse_args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=300)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--e2e-steps", type=int, default=5)
+    p.add_argument("--cpu-seconds", type=float, default=10.0, help="oracle time budget for cpu_baseline")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
+    return p.parse_args()
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world, device):
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(x, world, device):
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f), "measured"
+    except (OSError, ValueError):
+        return {"hbm_gbs": 6800.0}, "fallback"
+
+
+# ----------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu_index), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+        time.sleep(0.15)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def stop(self, t0, t1):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        time.sleep(0.12)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        sm, smax, reasons, n = [], [], set(), 0
+        window = [(t, l) for t, l in self.lines if t0 <= t <= t1 + 0.06]
+        if not window:  # timed region shorter than the sampling period
+            window = self.lines[-3:]
+        for _, line in window:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            n += 1
+            for name, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": n}
+
+
+# ------------------------------------------------------------ workload
+
+def generate(seed, device):
+    from lossless_kv_cache_gb300 import workloads as W
+    n_layers, layer = W.layers_of(WORKLOAD)
+    parts = [layer(seed, l, device) for l in range(n_layers)]
+    return torch.cat(parts)
+
+
+def config_dict(world):
+    return {"workload": WORKLOAD, "shape": [32, 2, 32768, 8, 128], "elements": 2147483648,
+            "element_dtype": "bf16", "chunk_elems": CHUNK, "codebook": "Top-16 from layer 0 of seed 1",
+            "l2": "inputs 4.29 GB > 129 MB L2 (no flush needed)",
+            "parallelism": "replicas of the workload per GPU, no collective" if world > 1 else "single GPU"}
+
+
+def escape_rate_of(blob_hdr_bytes, n):
+    E = int(np.frombuffer(blob_hdr_bytes[24:32], dtype=np.uint64)[0])
+    return E, E / n
+
+
+# --------------------------------------------------------- CPU oracle
+
+def oracle_throughput(x_host_bits, cb_exps, seconds, max_chunks):
+    """Encode + decode successive 64-chunk blocks with the scalar oracle until
+    `seconds` of CPU time are spent; returns (GB/s uncompressed, elements, s)."""
+    import oracle
+    block = 64 * CHUNK
+    done, t_total = 0, 0.0
+    cb = np.asarray(cb_exps, dtype=np.uint8)
+    while t_total < seconds and done + block <= min(x_host_bits.size, max_chunks * CHUNK):
+        xs = x_host_bits[done: done + block]
+        t0 = time.perf_counter()
+        blob = oracle.encode(xs, 0, cb, CHUNK)
+        y = oracle.decode(blob, xs.size, 0)
+        t_total += time.perf_counter() - t0
+        if not np.array_equal(y, xs):
+            raise RuntimeError("oracle round trip failed")
+        done += block
+    return 2.0 * done / t_total / 1e9, done, t_total
+
+
+# ---------------------------------------------------------------- arms
+
+def run_reference(args, world, rank):
+    """The CPU oracle on a bounded sample of the workload, per step."""
+    if rank != 0:
+        return None
+    from lossless_kv_cache_gb300 import workloads as W
+    _, layer = W.layers_of(WORKLOAD)
+    x = layer(0, 0, "cpu").numpy().view(np.uint16)  # layer 0 of seed 0
+    cal = layer(1, 0, "cpu").numpy().view(np.uint16)
+    import oracle
+    cb = oracle.calibrate(oracle.histogram(cal, 0), 0)
+    per_step = 16 * CHUNK  # elements per step (a bounded sample)
+    times = []
+    for s in range(args.warmup + args.steps):
+        off = (s * per_step) % (x.size - per_step + 1)
+        xs = x[off: off + per_step]
+        t0 = time.perf_counter()
+        blob = oracle.encode(xs, 0, cb, CHUNK)
+        y = oracle.decode(blob, xs.size, 0)
+        dt = time.perf_counter() - t0
+        if not np.array_equal(y, xs):
+            raise RuntimeError("oracle round trip failed")
+        if s >= args.warmup:
+            times.append(dt)
+    total = sum(times)
+    value = 2.0 * per_step * len(times) / total / 1e9
+    sample = "%d elements (%d chunks of 65536) of layer 0 per step, scalar C oracle, 1 thread" % (
+        per_step, per_step // CHUNK)
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * total / len(times), 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u16",
+        "data": "synthetic (seeded torch CPU generator)", "config": config_dict(world),
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def run_ours(args, world, rank, local):
+    import lossless_kv_cache_gb300 as sz
+
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    sz.lib()  # fails loudly when the CUDA library is missing
+    n = 32 * 2 * 32768 * 1024
+    raw_bytes = 2 * n
+
+    x = generate(rank, device)  # weak scaling: every rank has its own workload
+    from lossless_kv_cache_gb300 import workloads as W
+    _, layer = W.layers_of(WORKLOAD)
+    cal = layer(1, 0, device)
+    cb, _ = sz.calibrate(cal, sz.BF16)
+    del cal
+
+    bufs = sz.EncodeBuffers(n, sz.BF16, CHUNK, device=device)
+    out = torch.empty(n, dtype=torch.int16, device=device)
+    dstatus = torch.zeros(4, dtype=torch.int32, device=device)
+    stream = torch.cuda.current_stream()
+    h = stream.cuda_stream
+    xp, op, wp, ws = x.data_ptr(), bufs.out.data_ptr(), bufs.ws.data_ptr(), bufs.ws_bytes
+    cap = bufs.capacity
+
+    def check(st, what):
+        if st != sz.OK:
+            raise sz.SplitZipError(st, what)
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        check(sz.splitzip_encode_streams(xp, n, sz.BF16, cb, CHUNK, op, cap, wp, ws, h), "encode_streams")
+        if ev is not None:
+            ev[1].record(stream)
+        check(sz.splitzip_encode_escapes(n, sz.BF16, CHUNK, op, cap, wp, ws, bufs.size.data_ptr(),
+                                         bufs.status.data_ptr(), h), "encode_escapes")
+        if ev is not None:
+            ev[2].record(stream)
+        size_now = bufs.capacity  # decode bound: the buffer; the header carries the real size
+        check(sz.splitzip_decode(op, size_now, out.data_ptr(), n, sz.BF16, dstatus.data_ptr(), h), "decode")
+        if ev is not None:
+            ev[3].record(stream)
+
+    for _ in range(max(args.warmup, 1)):
+        step()
+    torch.cuda.synchronize()
+    assert int(bufs.status[0]) == sz.OK and int(dstatus[0]) == sz.OK
+    verified = bool(torch.equal(out, x))
+    blob_size = int(bufs.size[0])
+    E, esc_rate = escape_rate_of(bufs.out[:64].cpu().numpy().tobytes(), n)
+
+    # ---- timed region: K steps, events around every kernel launch group ----
+    K = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    clocks = ClockSampler(local)
+    clocks.start()
+    barrier(world)
+    torch.cuda.synchronize()
+    t_wall0 = time.time()
+    for k in range(K):
+        step(evs[k])
+    torch.cuda.synchronize()
+    t_wall1 = time.time()
+    barrier(world)
+    clk = clocks.stop(t_wall0, t_wall1)
+    total_ms = evs[0][0].elapsed_time(evs[-1][3])
+    total_ms = max_over_ranks(total_ms, world, device)
+    dense_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
+    esc_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
+    dec_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in evs)
+    enc_ms = dense_ms + esc_ms
+    ms_per_step = total_ms / K
+    all_bytes = sum_over_ranks(raw_bytes * K, world, device)
+    value = all_bytes / (total_ms * 1e-3) / 1e9
+
+    # ---- roofline of the dominant kernel (algorithmic bytes / event time) ----
+    peaks, peak_kind = measured_peaks()
+    hbm = float(peaks["hbm_gbs"])
+    C = n // CHUNK
+    alg_dense = 2 * n + n // 2 + n                 # read BF16, write nibbles + sign|mantissa
+    alg_decode = n // 2 + n + 3 * E + 12 * C + 2 * n  # read streams + escapes + index, write BF16
+    if dense_ms >= dec_ms:
+        name, alg, ms = "encode_streams_kernel<bf16>", alg_dense, dense_ms
+    else:
+        name, alg, ms = "decode_kernel<bf16>", alg_decode, dec_ms
+    achieved = alg / (ms * 1e-3) / 1e9
+    roofline = {"bound": "hbm", "kernel": name, "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
+                "frac": round(achieved / hbm, 4), "peak_source": "%s hbm_gbs (copy)" % peak_kind,
+                "algorithmic_bytes_per_launch": alg, "traffic": None}
+    per_kernel = {
+        "encode_streams": {"ms": round(dense_ms, 4), "alg_bytes": alg_dense,
+                           "gbs": round(alg_dense / (dense_ms * 1e-3) / 1e9, 1)},
+        "encode_escapes": {"ms": round(esc_ms, 4), "alg_bytes": 3 * E + 12 * C,
+                           "gbs": round((3 * E + 12 * C) / (esc_ms * 1e-3) / 1e9, 1)},
+        "decode": {"ms": round(dec_ms, 4), "alg_bytes": alg_decode,
+                   "gbs": round(alg_decode / (dec_ms * 1e-3) / 1e9, 1)},
+    }
+    enc_gbs = raw_bytes / (enc_ms * 1e-3) / 1e9
+    dec_gbs = raw_bytes / (dec_ms * 1e-3) / 1e9
+    enc_alg = alg_dense + 3 * E + 12 * C
+    link = {}
+    for L in LINKS_GBS:
+        t_plain = raw_bytes / (L * 1e9)
+        t_zip = (enc_ms + dec_ms) * 1e-3 + blob_size / (L * 1e9)
+        link["%d_GBps" % int(L)] = {"t_uncompressed_ms": round(1e3 * t_plain, 3),
+                                    "t_splitzip_ms": round(1e3 * t_zip, 3),
+                                    "speedup": round(t_plain / t_zip, 4)}
+
+    # ---- e2e: host pinned input -> H2D -> encode -> decode -> D2H ----
+    e2e = None
+    if not args.no_e2e:
+        x_host = torch.empty(n, dtype=torch.int16, pin_memory=True)
+        x_host.copy_(x)
+        y_host = torch.empty(n, dtype=torch.int16, pin_memory=True)
+        xin = torch.empty_like(x)
+        xin_p = xin.data_ptr()
+
+        def e2e_step():
+            xin.copy_(x_host, non_blocking=True)
+            check(sz.splitzip_encode(xin_p, n, sz.BF16, cb, CHUNK, op, cap, wp, ws, bufs.size.data_ptr(),
+                                     bufs.status.data_ptr(), h), "encode")
+            check(sz.splitzip_decode(op, cap, out.data_ptr(), n, sz.BF16, dstatus.data_ptr(), h), "decode")
+            y_host.copy_(out, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize()
+        barrier(world)
+        ea, eb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ea.record(stream)
+        for _ in range(args.e2e_steps):
+            e2e_step()
+        eb.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = max_over_ranks(ea.elapsed_time(eb), world, device)
+        e2e_ok = bool(torch.equal(y_host, x_host))
+        e2e_bytes = sum_over_ranks(raw_bytes * args.e2e_steps, world, device)
+        e2e = {"value": round(e2e_bytes / (e2e_ms * 1e-3) / 1e9, 3), "unit": "GB/s",
+               "h2d_bytes_per_step": raw_bytes, "d2h_bytes_per_step": raw_bytes,
+               "ms_per_step": round(e2e_ms / args.e2e_steps, 3), "verified": e2e_ok}
+        del x_host, y_host, xin
+
+    # ---- CPU oracle on a bounded sample (rank 0 only) ----
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        xh = x[: 512 * CHUNK].cpu().numpy().view(np.uint16)
+        gbs, elems, secs = oracle_throughput(xh, cb.values(), args.cpu_seconds, 512)
+        cpu = {"value": round(gbs, 5), "unit": "GB/s", "cores": 1, "kind": "oracle",
+               "sample": "%d elements (first %d chunks of the workload), encode+decode, %.1f s, scalar C "
+                         "oracle, 1 thread" % (elems, elems // CHUNK, secs)}
+
+    if rank != 0:
+        return None
+    return {
+        "metric": METRIC, "value": round(value, 3), "unit": "GB/s", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "u16",
+        "data": "synthetic (seeded torch CUDA generator; recipe of the workload module)",
+        "config": config_dict(world),
+        "encode_gbs": round(enc_gbs, 2), "decode_gbs": round(dec_gbs, 2),
+        "encode_hbm_frac": round(enc_alg / (enc_ms * 1e-3) / 1e9 / hbm, 4),
+        "decode_hbm_frac": round(alg_decode / (dec_ms * 1e-3) / 1e9 / hbm, 4),
+        "ratio": round(raw_bytes / blob_size, 5), "compressed_bytes": blob_size, "escapes": E,
+        "escape_rate": round(esc_rate, 6), "verified_bit_exact": verified,
+        "per_kernel": per_kernel, "link_model": link,
+        "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clk,
+        "gpu_launches": 4 * K,
+    }
+
+
+def main():
+    args = parse_args()
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        res = run_reference(args, world, rank)
+    else:
+        res = run_ours(args, world, rank, local)
+    if rank == 0 and res is not None:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,185 @@
+/*
+ * splitzip.h — C ABI of the GB300 (sm_103a) SplitZip lossless KV-cache codec.
+ *
+ * Method: "SplitZip: Ultra Fast Lossless KV Compression for Disaggregated LLM
+ * Serving" (gist.science summary page), section "Method: SplitZip".  A BF16 or
+ * FP8-E5M2 tensor is split into
+ *   - a 4-bit code per element: the exponent mapped through an offline
+ *     calibrated Top-16 codebook, two codes per byte ("Encoding strategy:
+ *     Fixed-length coding");
+ *   - the sign and mantissa bits, stored raw ("Sign/mantissa preservation";
+ *     FP8-E5M2 per Contributions 4);
+ *   - a sparse escape stream of (16-bit in-chunk position, 8-bit exponent)
+ *     for exponents outside the codebook ("Escape stream").
+ * Decoding maps every code back through a 16-entry table and then overwrites
+ * the escaped exponents ("Decoding strategy: Parallelism, Correction"), so the
+ * output is bit-identical to the input.
+ *
+ * Conventions for every entry point:
+ *   - The caller owns every buffer.  d_ pointers are CUDA device pointers on
+ *     the current device, h_ pointers are host pointers.  The library keeps no
+ *     reference to any buffer after the call returns.
+ *   - Device work is enqueued on `stream` and is asynchronous: the return value
+ *     reports only errors detectable on the host before launch (bad arguments,
+ *     too-small buffers, CUDA launch failures).  Data-dependent errors found by
+ *     the GPU are written to *d_status (a device int) in stream order.
+ *   - Device pointers must be 16-byte aligned (SPLITZIP_ERR_INVALID_ARG
+ *     otherwise).
+ *   - Elements are raw bits: BF16 as 16-bit little-endian words, FP8-E5M2 as
+ *     bytes.  No value is special: NaN, inf, signed zeros and subnormals round
+ *     trip bit for bit.
+ *   - On any error the contents of output buffers are unspecified, but no
+ *     access is made outside the buffers at the sizes passed in.
+ *
+ * Container format v1 (little-endian; every section starts on a 16-byte
+ * boundary; all padding bytes are zero).  The page gives no byte format; this
+ * layout is this library's own:
+ *   off 0   u32 magic 0x50495A53 ("SZIP")   off 4  u16 version = 1
+ *   off 6   u8  dtype (splitzip_dtype_t)     off 7  u8  reserved = 0
+ *   off 8   u64 n (elements)                 off 16 u32 chunk_elems
+ *   off 20  u32 n_chunks C = ceil(n / chunk_elems)
+ *   off 24  u64 E = total escapes            off 32 u8  codebook[16]
+ *   off 48  16 reserved bytes = 0
+ *   off 64  u64 esc_offset[C]: exclusive prefix sum of esc_count
+ *           u32 esc_count[C]:  escapes in chunk c
+ *   A16     nibble stream, ceil(n/2) bytes: element 2k in the low nibble of
+ *           byte k, element 2k+1 in the high nibble; an escaped element's
+ *           nibble is 0
+ *   A16     sign|mantissa stream: BF16 one byte per element,
+ *           (sign << 7) | mantissa7; FP8-E5M2 3 bits per element,
+ *           (sign << 2) | mantissa2, LSB-first bitstream, element i at bits
+ *           [3i, 3i+3), padded with zero bits to 3*ceil(n/8) bytes
+ *   A16     esc_pos u16[E]: in-chunk positions, chunk by chunk, ascending
+ *   A16     esc_exp u8[E]: the original exponents, same order (E5M2: the
+ *           5-bit exponent zero-extended); the container ends here.
+ * Size = A16(64 + 12C) + A16(ceil(n/2)) + A16(S) + A16(2E) + E, A16 = round
+ * up to 16, S = n (BF16) or 3*ceil(n/8) (FP8-E5M2).
+ * chunk_elems is a power of two in [64, 65536] (the 16-bit position field of
+ * the escape records bounds it; the page uses 65,536-element chunks).
+ */
+#ifndef SPLITZIP_H
+#define SPLITZIP_H
+
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    SPLITZIP_BF16 = 0,      /* bfloat16: 1 sign, 8 exponent, 7 mantissa bits */
+    SPLITZIP_FP8_E5M2 = 1   /* FP8-E5M2: 1 sign, 5 exponent, 2 mantissa bits */
+} splitzip_dtype_t;
+
+typedef enum {
+    SPLITZIP_OK = 0,
+    SPLITZIP_ERR_INVALID_ARG = 1, /* null/misaligned pointer, bad dtype, chunk size, codebook */
+    SPLITZIP_ERR_CAPACITY = 2,    /* output or workspace smaller than required */
+    SPLITZIP_ERR_CORRUPT = 3,     /* container inconsistent (header, index, escapes, size) */
+    SPLITZIP_ERR_CUDA = 4,        /* a CUDA runtime call or launch failed */
+    SPLITZIP_ERR_TIMEOUT = 5,     /* reserved: a bounded device wait gave up */
+    SPLITZIP_ERR_UNSUPPORTED = 6  /* no sm_103a device, or a size beyond the limits */
+} splitzip_status_t;
+
+#define SPLITZIP_DEFAULT_CHUNK_ELEMS 65536u
+#define SPLITZIP_HEADER_BYTES 64u
+
+/* Top-16 codebook: code i stands for exponent exps[i].  The 16 values must be
+ * distinct and below 256 (BF16) or 32 (FP8-E5M2). */
+typedef struct {
+    uint8_t dtype;    /* splitzip_dtype_t */
+    uint8_t exps[16];
+} splitzip_codebook_t;
+
+/* Parsed header plus the derived section offsets (bytes from blob start). */
+typedef struct {
+    uint64_t n_elems;
+    uint64_t total_escapes;
+    uint64_t size;          /* total container bytes */
+    uint64_t index_off, counts_off, nibble_off, signmant_off, escpos_off, escexp_off;
+    uint32_t chunk_elems;
+    uint32_t n_chunks;
+    uint8_t dtype;
+    uint8_t codebook[16];
+} splitzip_header_t;
+
+/* Human-readable name of a splitzip_status_t value (static storage). */
+const char* splitzip_status_string(int status);
+
+/* Exponent histogram of n elements (Results, "Ablations: Calibration": the
+ * codebook is calibrated offline from exponent statistics).
+ * d_x: n elements of `dtype`; d_hist256: 256 u64 counts, overwritten (bins
+ * 32..255 stay 0 for FP8-E5M2).  Enqueued on `stream`. */
+int splitzip_exponent_histogram(const void* d_x, uint64_t n, int dtype, uint64_t* d_hist256,
+                                cudaStream_t stream);
+
+/* Top-16 codebook from a 256-bin exponent histogram (Method, "Fixed-length
+ * coding": the 16 most frequent exponents get the 4-bit codes).  Ties go to
+ * the smaller exponent; unseen exponents fill the remaining codes in
+ * ascending order; code 0 is the most frequent exponent.
+ * hist256: host array, or device array when hist_is_device != 0 (then the
+ * call copies it to the host and synchronises the current device's default
+ * stream).  FP8-E5M2 histograms with counts in bins >= 32 are rejected. */
+int splitzip_calibrate(const uint64_t* hist256, int hist_is_device, int dtype,
+                       splitzip_codebook_t* out_cb);
+
+/* Container size for n elements with exactly `total_escapes` escapes. */
+int splitzip_compressed_size(uint64_t n, int dtype, uint32_t chunk_elems, uint64_t total_escapes,
+                             uint64_t* out_bytes);
+
+/* Worst-case container size (every element escapes): the capacity that
+ * splitzip_encode requires of d_out. */
+int splitzip_max_compressed_size(uint64_t n, int dtype, uint32_t chunk_elems, uint64_t* out_bytes);
+
+/* Device scratch bytes splitzip_encode needs for n elements (about 4 bytes
+ * per element: the per-tile escape staging area, plus per-tile counts). */
+int splitzip_encode_workspace_size(uint64_t n, int dtype, uint32_t chunk_elems, uint64_t* out_bytes);
+
+/* Encode n elements (Method, "Encoding strategy").
+ * d_in: n elements; cb: host codebook of the same dtype; d_out: container,
+ * out_capacity >= splitzip_max_compressed_size; d_ws: ws_bytes >=
+ * splitzip_encode_workspace_size, contents need not be initialised;
+ * d_out_size: device u64 that receives the container size; d_status: device
+ * int set to SPLITZIP_OK when the container is complete.  n = 0 is valid and
+ * gives a 64-byte container.  Equivalent to splitzip_encode_streams followed
+ * by splitzip_encode_escapes on the same stream. */
+int splitzip_encode(const void* d_in, uint64_t n, int dtype, const splitzip_codebook_t* cb,
+                    uint32_t chunk_elems, void* d_out, uint64_t out_capacity, void* d_ws,
+                    uint64_t ws_bytes, uint64_t* d_out_size, int* d_status, cudaStream_t stream);
+
+/* First encode stage: writes the header (without E), the nibble and the
+ * sign|mantissa streams, and stages each tile's escapes and count in d_ws.
+ * After it completes on `stream` the two dense streams are final, so a caller
+ * can start moving them while the second stage runs. */
+int splitzip_encode_streams(const void* d_in, uint64_t n, int dtype, const splitzip_codebook_t* cb,
+                            uint32_t chunk_elems, void* d_out, uint64_t out_capacity, void* d_ws,
+                            uint64_t ws_bytes, cudaStream_t stream);
+
+/* Second encode stage: per-chunk counts and prefix offsets, E, the escape
+ * stream in ascending position order, all padding, *d_out_size and
+ * *d_status.  Arguments must match the preceding splitzip_encode_streams. */
+int splitzip_encode_escapes(uint64_t n, int dtype, uint32_t chunk_elems, void* d_out,
+                            uint64_t out_capacity, void* d_ws, uint64_t ws_bytes,
+                            uint64_t* d_out_size, int* d_status, cudaStream_t stream);
+
+/* Decode a container into n elements (Method, "Decoding strategy").
+ * d_in: in_bytes bytes of container (in_bytes >= its size); d_out: n
+ * elements.  The GPU checks the header (magic, version, dtype and n equal to
+ * the arguments, chunk size, sizes against in_bytes), the index (offsets are
+ * the prefix of the counts, counts fit their chunks) and every escape
+ * (position inside its chunk and ascending, exponent in range); on a
+ * mismatch it writes SPLITZIP_ERR_CORRUPT to *d_status, else SPLITZIP_OK. */
+int splitzip_decode(const void* d_in, uint64_t in_bytes, void* d_out, uint64_t n, int dtype,
+                    int* d_status, cudaStream_t stream);
+
+/* Parse and check a container header held in host memory (bytes >= 64).
+ * Returns SPLITZIP_ERR_CORRUPT for a malformed header or a size larger than
+ * `bytes`. */
+int splitzip_parse_header(const void* h_blob, uint64_t bytes, splitzip_header_t* out);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPLITZIP_H */

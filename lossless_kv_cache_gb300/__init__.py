@@ -1,0 +1,272 @@
+"""SplitZip lossless KV-cache codec for GB300 (sm_103a).
+
+Thin ctypes binding of the C ABI in include/splitzip.h: the ``splitzip_*``
+functions below take the same arguments as the C entry points (device
+pointers as Python ints, a CUDA stream handle as an int) and return the same
+status codes.  Every step of the codec runs in the CUDA kernels of
+``libsplitzip.so``; this module only marshals arguments.  The torch helpers at
+the end (``calibrate``, ``encode``, ``decode``) allocate device memory with
+torch and call the same entry points.
+
+Method: "SplitZip: Ultra Fast Lossless KV Compression for Disaggregated LLM
+Serving", section "Method: SplitZip".
+"""
+import ctypes
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libsplitzip.so")
+
+BF16 = 0
+FP8_E5M2 = 1
+OK, ERR_INVALID_ARG, ERR_CAPACITY, ERR_CORRUPT, ERR_CUDA, ERR_TIMEOUT, ERR_UNSUPPORTED = range(7)
+DEFAULT_CHUNK_ELEMS = 65536
+HEADER_BYTES = 64
+
+
+class SplitZipError(RuntimeError):
+    def __init__(self, status, where=""):
+        self.status = status
+        super().__init__("%s: %s (status %d)" % (where, splitzip_status_string(status), status))
+
+
+class Codebook(ctypes.Structure):
+    """splitzip_codebook_t: code i stands for exponent exps[i]."""
+    _fields_ = [("dtype", ctypes.c_uint8), ("exps", ctypes.c_uint8 * 16)]
+
+    def values(self):
+        return list(self.exps)
+
+    @classmethod
+    def make(cls, dtype, exps):
+        cb = cls()
+        cb.dtype = dtype
+        for i, e in enumerate(exps):
+            cb.exps[i] = int(e)
+        return cb
+
+
+class Header(ctypes.Structure):
+    """splitzip_header_t."""
+    _fields_ = [
+        ("n_elems", ctypes.c_uint64),
+        ("total_escapes", ctypes.c_uint64),
+        ("size", ctypes.c_uint64),
+        ("index_off", ctypes.c_uint64),
+        ("counts_off", ctypes.c_uint64),
+        ("nibble_off", ctypes.c_uint64),
+        ("signmant_off", ctypes.c_uint64),
+        ("escpos_off", ctypes.c_uint64),
+        ("escexp_off", ctypes.c_uint64),
+        ("chunk_elems", ctypes.c_uint32),
+        ("n_chunks", ctypes.c_uint32),
+        ("dtype", ctypes.c_uint8),
+        ("codebook", ctypes.c_uint8 * 16),
+    ]
+
+
+_u64, _u32, _int, _vp = ctypes.c_uint64, ctypes.c_uint32, ctypes.c_int, ctypes.c_void_p
+_P_u64 = ctypes.POINTER(ctypes.c_uint64)
+
+# name -> (restype, argtypes); mirrors include/splitzip.h
+SIGNATURES = {
+    "splitzip_status_string": (ctypes.c_char_p, [_int]),
+    "splitzip_exponent_histogram": (_int, [_vp, _u64, _int, _vp, _vp]),
+    "splitzip_calibrate": (_int, [_vp, _int, _int, ctypes.POINTER(Codebook)]),
+    "splitzip_compressed_size": (_int, [_u64, _int, _u32, _u64, _P_u64]),
+    "splitzip_max_compressed_size": (_int, [_u64, _int, _u32, _P_u64]),
+    "splitzip_encode_workspace_size": (_int, [_u64, _int, _u32, _P_u64]),
+    "splitzip_encode": (_int, [_vp, _u64, _int, ctypes.POINTER(Codebook), _u32, _vp, _u64, _vp, _u64, _vp,
+                               _vp, _vp]),
+    "splitzip_encode_streams": (_int, [_vp, _u64, _int, ctypes.POINTER(Codebook), _u32, _vp, _u64, _vp,
+                                       _u64, _vp]),
+    "splitzip_encode_escapes": (_int, [_u64, _int, _u32, _vp, _u64, _vp, _u64, _vp, _vp, _vp]),
+    "splitzip_decode": (_int, [_vp, _u64, _vp, _u64, _int, _vp, _vp]),
+    "splitzip_parse_header": (_int, [_vp, _u64, ctypes.POINTER(Header)]),
+}
+
+_lib = None
+
+
+def lib():
+    """The loaded libsplitzip.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError("libsplitzip.so is missing: build it with "
+                               "`python -c 'import __graft_entry__ as g; g.build()'`")
+        L = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in SIGNATURES.items():
+            f = getattr(L, name)
+            f.restype = res
+            f.argtypes = args
+        _lib = L
+    return _lib
+
+
+# ---------------------------------------------------------------- C entry points
+
+def splitzip_status_string(status):
+    return lib().splitzip_status_string(status).decode()
+
+
+def splitzip_exponent_histogram(d_x, n, dtype, d_hist256, stream):
+    return lib().splitzip_exponent_histogram(d_x, n, dtype, d_hist256, stream)
+
+
+def splitzip_calibrate(hist256, hist_is_device, dtype, out_cb):
+    return lib().splitzip_calibrate(hist256, hist_is_device, dtype, ctypes.byref(out_cb))
+
+
+def splitzip_compressed_size(n, dtype, chunk_elems, total_escapes, out_bytes):
+    return lib().splitzip_compressed_size(n, dtype, chunk_elems, total_escapes, ctypes.byref(out_bytes))
+
+
+def splitzip_max_compressed_size(n, dtype, chunk_elems, out_bytes):
+    return lib().splitzip_max_compressed_size(n, dtype, chunk_elems, ctypes.byref(out_bytes))
+
+
+def splitzip_encode_workspace_size(n, dtype, chunk_elems, out_bytes):
+    return lib().splitzip_encode_workspace_size(n, dtype, chunk_elems, ctypes.byref(out_bytes))
+
+
+def splitzip_encode(d_in, n, dtype, cb, chunk_elems, d_out, out_capacity, d_ws, ws_bytes, d_out_size,
+                    d_status, stream):
+    return lib().splitzip_encode(d_in, n, dtype, ctypes.byref(cb), chunk_elems, d_out, out_capacity, d_ws,
+                                 ws_bytes, d_out_size, d_status, stream)
+
+
+def splitzip_encode_streams(d_in, n, dtype, cb, chunk_elems, d_out, out_capacity, d_ws, ws_bytes, stream):
+    return lib().splitzip_encode_streams(d_in, n, dtype, ctypes.byref(cb), chunk_elems, d_out, out_capacity,
+                                         d_ws, ws_bytes, stream)
+
+
+def splitzip_encode_escapes(n, dtype, chunk_elems, d_out, out_capacity, d_ws, ws_bytes, d_out_size, d_status,
+                            stream):
+    return lib().splitzip_encode_escapes(n, dtype, chunk_elems, d_out, out_capacity, d_ws, ws_bytes,
+                                         d_out_size, d_status, stream)
+
+
+def splitzip_decode(d_in, in_bytes, d_out, n, dtype, d_status, stream):
+    return lib().splitzip_decode(d_in, in_bytes, d_out, n, dtype, d_status, stream)
+
+
+def splitzip_parse_header(h_blob, nbytes, out):
+    return lib().splitzip_parse_header(h_blob, nbytes, ctypes.byref(out))
+
+
+# ------------------------------------------------------------ size helpers
+
+def _size_call(fn, *args):
+    out = ctypes.c_uint64(0)
+    st = fn(*args, out)
+    if st != OK:
+        raise SplitZipError(st, fn.__name__)
+    return out.value
+
+
+def max_compressed_size(n, dtype, chunk_elems=DEFAULT_CHUNK_ELEMS):
+    return _size_call(splitzip_max_compressed_size, n, dtype, chunk_elems)
+
+
+def compressed_size(n, dtype, chunk_elems, total_escapes):
+    return _size_call(splitzip_compressed_size, n, dtype, chunk_elems, total_escapes)
+
+
+def workspace_size(n, dtype, chunk_elems=DEFAULT_CHUNK_ELEMS):
+    return _size_call(splitzip_encode_workspace_size, n, dtype, chunk_elems)
+
+
+def parse_header(blob_bytes):
+    """Header of a container held in host memory (bytes / numpy / torch CPU)."""
+    import numpy as np
+    buf = np.ascontiguousarray(np.frombuffer(bytes(blob_bytes), dtype=np.uint8)) \
+        if isinstance(blob_bytes, (bytes, bytearray)) else np.ascontiguousarray(blob_bytes).view(np.uint8)
+    h = Header()
+    st = splitzip_parse_header(buf.ctypes.data, buf.size, h)
+    if st != OK:
+        raise SplitZipError(st, "splitzip_parse_header")
+    return h
+
+
+# ------------------------------------------------------------ torch helpers
+
+def _torch():
+    import torch
+    return torch
+
+
+def _stream_handle(stream):
+    torch = _torch()
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def _bits_dtype(dtype):
+    torch = _torch()
+    return torch.int16 if dtype == BF16 else torch.uint8
+
+
+def _check(st, where):
+    if st != OK:
+        raise SplitZipError(st, where)
+
+
+def calibrate(x, dtype, stream=None):
+    """Exponent histogram of the device tensor ``x`` (raw bits) on the GPU,
+    then the Top-16 codebook.  Synchronises."""
+    torch = _torch()
+    hist = torch.empty(256, dtype=torch.int64, device=x.device)
+    _check(splitzip_exponent_histogram(x.data_ptr(), x.numel(), dtype, hist.data_ptr(), _stream_handle(stream)),
+           "splitzip_exponent_histogram")
+    torch.cuda.current_stream().synchronize() if stream is None else stream.synchronize()
+    h = hist.cpu()
+    cb = Codebook()
+    _check(splitzip_calibrate(h.data_ptr(), 0, dtype, cb), "splitzip_calibrate")
+    return cb, h
+
+
+class EncodeBuffers:
+    """Device buffers for one encode of n elements (capacity-sized)."""
+
+    def __init__(self, n, dtype, chunk_elems=DEFAULT_CHUNK_ELEMS, device="cuda"):
+        torch = _torch()
+        self.n, self.dtype, self.chunk_elems = n, dtype, chunk_elems
+        self.capacity = max_compressed_size(n, dtype, chunk_elems)
+        self.ws_bytes = workspace_size(n, dtype, chunk_elems)
+        self.out = torch.empty(self.capacity, dtype=torch.uint8, device=device)
+        self.ws = torch.empty(max(self.ws_bytes, 16), dtype=torch.uint8, device=device)
+        self.size = torch.zeros(2, dtype=torch.int64, device=device)   # [0] = container bytes
+        self.status = torch.zeros(4, dtype=torch.int32, device=device)  # [0] = status
+
+
+def encode_into(x, cb, bufs, stream=None):
+    """Enqueue the encode of device tensor ``x`` into ``bufs`` (asynchronous)."""
+    _check(splitzip_encode(x.data_ptr(), x.numel(), bufs.dtype, cb, bufs.chunk_elems, bufs.out.data_ptr(),
+                           bufs.capacity, bufs.ws.data_ptr(), bufs.ws_bytes, bufs.size.data_ptr(),
+                           bufs.status.data_ptr(), _stream_handle(stream)), "splitzip_encode")
+
+
+def encode(x, cb, dtype, chunk_elems=DEFAULT_CHUNK_ELEMS, stream=None):
+    """Encode device tensor ``x``; returns the container as a uint8 device
+    tensor of its exact size.  Synchronises to read the size."""
+    bufs = EncodeBuffers(x.numel(), dtype, chunk_elems, device=x.device)
+    encode_into(x, cb, bufs, stream)
+    size, status = int(bufs.size[0].item()), int(bufs.status[0].item())
+    _check(status, "splitzip_encode (device)")
+    return bufs.out[:size]
+
+
+def decode_into(blob, in_bytes, out, n, dtype, status, stream=None):
+    _check(splitzip_decode(blob.data_ptr(), in_bytes, out.data_ptr() if n else 0, n, dtype, status.data_ptr(),
+                           _stream_handle(stream)), "splitzip_decode")
+
+
+def decode(blob, n, dtype, stream=None):
+    """Decode a device container into a new device tensor of raw bits."""
+    torch = _torch()
+    out = torch.empty(max(n, 1), dtype=_bits_dtype(dtype), device=blob.device)
+    status = torch.zeros(4, dtype=torch.int32, device=blob.device)
+    decode_into(blob, blob.numel(), out, n, dtype, status, stream)
+    _check(int(status[0].item()), "splitzip_decode (device)")
+    return out[:n]

@@ -1,0 +1,322 @@
+// Host side of the SplitZip C ABI declared in include/splitzip.h: argument
+// checks, container geometry, codebook calibration, and the stream-ordered
+// launch sequence of the encode / decode / histogram kernels.
+#include <algorithm>
+#include <cstring>
+#include <mutex>
+
+#include "splitzip_internal.cuh"
+
+using namespace splitzip;
+
+namespace {
+
+constexpr uint64_t kMaxElems = uint64_t(1) << 48;  // keeps every size below 2^52
+constexpr int kMaxDevices = 64;
+
+struct DeviceState {
+    bool ready;
+    int status;
+    int sms;
+    int encode_bpsm[2], decode_bpsm[2], hist_bpsm[2], gather_bpsm;
+};
+
+std::mutex g_mutex;
+DeviceState g_devices[kMaxDevices];
+
+// Per-device facts, computed once: SM count and resident CTAs per SM of
+// every kernel (grids are sized as a multiple of the SM count).
+int device_state(DeviceState* out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return SPLITZIP_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return SPLITZIP_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    DeviceState& d = g_devices[dev];
+    if (!d.ready) {
+        int major = 0, minor = 0;
+        d.status = SPLITZIP_OK;
+        if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
+            cudaGetLastError();
+            return SPLITZIP_ERR_CUDA;
+        }
+        if (major != 10 || minor != 3) {
+            d.status = SPLITZIP_ERR_UNSUPPORTED;  // the kernels are built for sm_103a only
+        } else {
+            for (int t = 0; t < 2; ++t) {
+                if (occupancy_encode(&d.encode_bpsm[t], t) != cudaSuccess ||
+                    occupancy_decode(&d.decode_bpsm[t], t) != cudaSuccess ||
+                    occupancy_histogram(&d.hist_bpsm[t], t) != cudaSuccess) {
+                    cudaGetLastError();
+                    return SPLITZIP_ERR_CUDA;
+                }
+            }
+            if (occupancy_gather(&d.gather_bpsm) != cudaSuccess) {
+                cudaGetLastError();
+                return SPLITZIP_ERR_CUDA;
+            }
+        }
+        d.ready = true;
+    }
+    *out = d;
+    return d.status;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+bool valid_dtype(int dtype) { return dtype == SPLITZIP_BF16 || dtype == SPLITZIP_FP8_E5M2; }
+bool valid_chunk(uint32_t c) { return c >= kMinChunk && c <= kMaxChunk && (c & (c - 1u)) == 0u; }
+uint32_t exponent_bins(int dtype) { return dtype == SPLITZIP_BF16 ? 256u : 32u; }
+
+int check_geometry(uint64_t n, int dtype, uint32_t chunk) {
+    if (!valid_dtype(dtype) || !valid_chunk(chunk)) return SPLITZIP_ERR_INVALID_ARG;
+    if (n > kMaxElems || (n + chunk - 1u) / chunk > 0xFFFFFFFFull) return SPLITZIP_ERR_UNSUPPORTED;
+    return SPLITZIP_OK;
+}
+
+int check_codebook(const splitzip_codebook_t* cb, int dtype) {
+    if (!cb || cb->dtype != dtype) return SPLITZIP_ERR_INVALID_ARG;
+    bool seen[256] = {false};
+    for (int i = 0; i < 16; ++i) {
+        const uint8_t e = cb->exps[i];
+        if (e >= exponent_bins(dtype) || seen[e]) return SPLITZIP_ERR_INVALID_ARG;
+        seen[e] = true;
+    }
+    return SPLITZIP_OK;
+}
+
+int grid_for(uint64_t work_items, int sms, int blocks_per_sm) {
+    const uint64_t cap = uint64_t(sms) * uint64_t(blocks_per_sm > 0 ? blocks_per_sm : 1);
+    return int(std::max<uint64_t>(1, std::min<uint64_t>(work_items, cap)));
+}
+
+// Shared checks of the two encode stages; fills the kernel arguments.
+int prepare_encode(const void* d_in, uint64_t n, int dtype, const splitzip_codebook_t* cb, bool need_input,
+                   uint32_t chunk, void* d_out, uint64_t out_capacity, void* d_ws, uint64_t ws_bytes,
+                   EncodeArgs* a) {
+    int st = check_geometry(n, dtype, chunk);
+    if (st != SPLITZIP_OK) return st;
+    if (need_input) {
+        if ((st = check_codebook(cb, dtype)) != SPLITZIP_OK) return st;
+        if (n > 0 && (!d_in || !aligned(d_in, 16))) return SPLITZIP_ERR_INVALID_ARG;
+    }
+    if (!d_out || !aligned(d_out, 16)) return SPLITZIP_ERR_INVALID_ARG;
+    const Layout worst = layout_for(n, dtype, chunk, n);
+    if (out_capacity < worst.size) return SPLITZIP_ERR_CAPACITY;
+    const Workspace W = workspace_for(n, chunk);
+    if (ws_bytes < W.bytes) return SPLITZIP_ERR_CAPACITY;
+    if (W.bytes > 0 && (!d_ws || !aligned(d_ws, 16))) return SPLITZIP_ERR_INVALID_ARG;
+
+    const Layout L = layout_for(n, dtype, chunk, 0);
+    uint8_t* out = static_cast<uint8_t*>(d_out);
+    uint8_t* ws = static_cast<uint8_t*>(d_ws);
+    a->in = d_in;
+    a->n = n;
+    a->out = out;
+    a->nibbles = out + L.nibble_off;
+    a->signmant = out + L.signmant_off;
+    a->tile_counts = reinterpret_cast<uint32_t*>(ws + W.counts_off);
+    a->staging = reinterpret_cast<uint32_t*>(ws + W.staging_off);
+    a->n_tiles = W.n_tiles;
+    a->tile_elems = W.tile_elems;
+    a->chunk_elems = chunk;
+    a->n_chunks = L.n_chunks;
+    a->dtype = dtype;
+    if (cb) std::memcpy(a->codebook, cb->exps, 16);
+    else std::memset(a->codebook, 0, 16);
+    return SPLITZIP_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* splitzip_status_string(int status) {
+    switch (status) {
+        case SPLITZIP_OK: return "ok";
+        case SPLITZIP_ERR_INVALID_ARG: return "invalid argument";
+        case SPLITZIP_ERR_CAPACITY: return "buffer too small";
+        case SPLITZIP_ERR_CORRUPT: return "corrupt container";
+        case SPLITZIP_ERR_CUDA: return "CUDA error";
+        case SPLITZIP_ERR_TIMEOUT: return "device wait timed out";
+        case SPLITZIP_ERR_UNSUPPORTED: return "unsupported device or size";
+        default: return "unknown status";
+    }
+}
+
+int splitzip_compressed_size(uint64_t n, int dtype, uint32_t chunk_elems, uint64_t total_escapes,
+                             uint64_t* out_bytes) {
+    int st = check_geometry(n, dtype, chunk_elems);
+    if (st != SPLITZIP_OK) return st;
+    if (!out_bytes || total_escapes > n) return SPLITZIP_ERR_INVALID_ARG;
+    *out_bytes = layout_for(n, dtype, chunk_elems, total_escapes).size;
+    return SPLITZIP_OK;
+}
+
+int splitzip_max_compressed_size(uint64_t n, int dtype, uint32_t chunk_elems, uint64_t* out_bytes) {
+    return splitzip_compressed_size(n, dtype, chunk_elems, n, out_bytes);
+}
+
+int splitzip_encode_workspace_size(uint64_t n, int dtype, uint32_t chunk_elems, uint64_t* out_bytes) {
+    int st = check_geometry(n, dtype, chunk_elems);
+    if (st != SPLITZIP_OK) return st;
+    if (!out_bytes) return SPLITZIP_ERR_INVALID_ARG;
+    *out_bytes = workspace_for(n, chunk_elems).bytes;
+    return SPLITZIP_OK;
+}
+
+int splitzip_calibrate(const uint64_t* hist256, int hist_is_device, int dtype, splitzip_codebook_t* out_cb) {
+    if (!hist256 || !out_cb || !valid_dtype(dtype)) return SPLITZIP_ERR_INVALID_ARG;
+    uint64_t h[256];
+    if (hist_is_device) {
+        if (cudaMemcpy(h, hist256, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess) {
+            cudaGetLastError();
+            return SPLITZIP_ERR_CUDA;
+        }
+    } else {
+        std::memcpy(h, hist256, sizeof(h));
+    }
+    const uint32_t bins = exponent_bins(dtype);
+    for (uint32_t b = bins; b < 256; ++b)
+        if (h[b] != 0) return SPLITZIP_ERR_INVALID_ARG;
+    // Most frequent first; the stable sort keeps ascending exponent order on ties.
+    uint16_t order[256];
+    for (uint32_t b = 0; b < bins; ++b) order[b] = uint16_t(b);
+    std::stable_sort(order, order + bins, [&](uint16_t x, uint16_t y) { return h[x] > h[y]; });
+    out_cb->dtype = uint8_t(dtype);
+    for (int i = 0; i < 16; ++i) out_cb->exps[i] = uint8_t(order[i]);
+    return SPLITZIP_OK;
+}
+
+int splitzip_exponent_histogram(const void* d_x, uint64_t n, int dtype, uint64_t* d_hist256,
+                                cudaStream_t stream) {
+    if (!valid_dtype(dtype) || !d_hist256 || !aligned(d_hist256, 16)) return SPLITZIP_ERR_INVALID_ARG;
+    if (n > 0 && (!d_x || !aligned(d_x, 16))) return SPLITZIP_ERR_INVALID_ARG;
+    if (n > kMaxElems) return SPLITZIP_ERR_UNSUPPORTED;
+    DeviceState d;
+    int st = device_state(&d);
+    if (st != SPLITZIP_OK) return st;
+    if (cudaMemsetAsync(d_hist256, 0, 256 * sizeof(uint64_t), stream) != cudaSuccess) {
+        cudaGetLastError();
+        return SPLITZIP_ERR_CUDA;
+    }
+    if (n == 0) return SPLITZIP_OK;
+    const uint64_t vec_per_block = uint64_t(kHistThreads);
+    const uint64_t vecs = n * (dtype == SPLITZIP_BF16 ? 2 : 1) / 16;
+    const int grid = grid_for((vecs + vec_per_block - 1) / vec_per_block, d.sms, d.hist_bpsm[dtype]);
+    return launch_histogram(d_x, n, dtype, reinterpret_cast<unsigned long long*>(d_hist256), grid, stream) ==
+                   cudaSuccess
+               ? SPLITZIP_OK
+               : SPLITZIP_ERR_CUDA;
+}
+
+int splitzip_encode_streams(const void* d_in, uint64_t n, int dtype, const splitzip_codebook_t* cb,
+                            uint32_t chunk_elems, void* d_out, uint64_t out_capacity, void* d_ws,
+                            uint64_t ws_bytes, cudaStream_t stream) {
+    EncodeArgs a;
+    int st = prepare_encode(d_in, n, dtype, cb, true, chunk_elems, d_out, out_capacity, d_ws, ws_bytes, &a);
+    if (st != SPLITZIP_OK) return st;
+    DeviceState d;
+    if ((st = device_state(&d)) != SPLITZIP_OK) return st;
+    EncodeLut lut;
+    std::memset(lut.code, kEscapeFlag, sizeof(lut.code));
+    for (int k = 0; k < 16; ++k) lut.code[cb->exps[k]] = uint8_t(k);
+    const int grid = grid_for(a.n_tiles, d.sms, d.encode_bpsm[dtype]);
+    return launch_encode_streams(a, lut, grid, stream) == cudaSuccess ? SPLITZIP_OK : SPLITZIP_ERR_CUDA;
+}
+
+int splitzip_encode_escapes(uint64_t n, int dtype, uint32_t chunk_elems, void* d_out, uint64_t out_capacity,
+                            void* d_ws, uint64_t ws_bytes, uint64_t* d_out_size, int* d_status,
+                            cudaStream_t stream) {
+    if (!d_out_size || !aligned(d_out_size, 8) || !d_status || !aligned(d_status, 4))
+        return SPLITZIP_ERR_INVALID_ARG;
+    EncodeArgs a;
+    int st = prepare_encode(nullptr, n, dtype, nullptr, false, chunk_elems, d_out, out_capacity, d_ws, ws_bytes,
+                            &a);
+    if (st != SPLITZIP_OK) return st;
+    DeviceState d;
+    if ((st = device_state(&d)) != SPLITZIP_OK) return st;
+    const int warps_per_block = kGatherThreads / 32;
+    const int grid = grid_for((a.n_tiles + warps_per_block - 1) / warps_per_block, d.sms, d.gather_bpsm);
+    return launch_encode_escapes(a, d_out_size, d_status, grid, stream) == cudaSuccess ? SPLITZIP_OK
+                                                                                      : SPLITZIP_ERR_CUDA;
+}
+
+int splitzip_encode(const void* d_in, uint64_t n, int dtype, const splitzip_codebook_t* cb, uint32_t chunk_elems,
+                    void* d_out, uint64_t out_capacity, void* d_ws, uint64_t ws_bytes, uint64_t* d_out_size,
+                    int* d_status, cudaStream_t stream) {
+    if (!d_out_size || !aligned(d_out_size, 8) || !d_status || !aligned(d_status, 4))
+        return SPLITZIP_ERR_INVALID_ARG;
+    int st = splitzip_encode_streams(d_in, n, dtype, cb, chunk_elems, d_out, out_capacity, d_ws, ws_bytes, stream);
+    if (st != SPLITZIP_OK) return st;
+    return splitzip_encode_escapes(n, dtype, chunk_elems, d_out, out_capacity, d_ws, ws_bytes, d_out_size,
+                                   d_status, stream);
+}
+
+int splitzip_decode(const void* d_in, uint64_t in_bytes, void* d_out, uint64_t n, int dtype, int* d_status,
+                    cudaStream_t stream) {
+    if (!valid_dtype(dtype) || !d_in || !aligned(d_in, 16) || !d_status || !aligned(d_status, 4))
+        return SPLITZIP_ERR_INVALID_ARG;
+    if (n > 0 && (!d_out || !aligned(d_out, 16))) return SPLITZIP_ERR_INVALID_ARG;
+    if (n > kMaxElems) return SPLITZIP_ERR_UNSUPPORTED;
+    if (in_bytes < kHeaderBytes) return SPLITZIP_ERR_CORRUPT;
+    DeviceState d;
+    int st = device_state(&d);
+    if (st != SPLITZIP_OK) return st;
+    if (cudaMemsetAsync(d_status, 0, sizeof(int), stream) != cudaSuccess) {
+        cudaGetLastError();
+        return SPLITZIP_ERR_CUDA;
+    }
+    DecodeArgs a;
+    a.in = static_cast<const uint8_t*>(d_in);
+    a.in_bytes = in_bytes;
+    a.out = d_out;
+    a.n = n;
+    a.dtype = dtype;
+    a.status = d_status;
+    const int grid = grid_for((n + kMinChunk - 1) / kMinChunk, d.sms, d.decode_bpsm[dtype]);
+    return launch_decode(a, grid, stream) == cudaSuccess ? SPLITZIP_OK : SPLITZIP_ERR_CUDA;
+}
+
+int splitzip_parse_header(const void* h_blob, uint64_t bytes, splitzip_header_t* out) {
+    if (!h_blob || !out) return SPLITZIP_ERR_INVALID_ARG;
+    if (bytes < kHeaderBytes) return SPLITZIP_ERR_CORRUPT;
+    const uint8_t* b = static_cast<const uint8_t*>(h_blob);
+    auto u16 = [&](int o) { return uint16_t(b[o] | (b[o + 1] << 8)); };
+    auto u32 = [&](int o) {
+        uint32_t v = 0;
+        for (int i = 3; i >= 0; --i) v = (v << 8) | b[o + i];
+        return v;
+    };
+    auto u64 = [&](int o) { return uint64_t(u32(o)) | (uint64_t(u32(o + 4)) << 32); };
+    if (u32(0) != kMagic || u16(4) != kVersion || !valid_dtype(b[6]) || b[7] != 0) return SPLITZIP_ERR_CORRUPT;
+    for (int i = 48; i < 64; ++i)
+        if (b[i] != 0) return SPLITZIP_ERR_CORRUPT;
+    splitzip_header_t h;
+    h.dtype = b[6];
+    h.n_elems = u64(8);
+    h.chunk_elems = u32(16);
+    h.n_chunks = u32(20);
+    h.total_escapes = u64(24);
+    std::memcpy(h.codebook, b + 32, 16);
+    if (!valid_chunk(h.chunk_elems) || h.n_elems > kMaxElems) return SPLITZIP_ERR_CORRUPT;
+    if ((h.n_elems + h.chunk_elems - 1u) / h.chunk_elems != h.n_chunks) return SPLITZIP_ERR_CORRUPT;
+    if (h.total_escapes > h.n_elems) return SPLITZIP_ERR_CORRUPT;
+    splitzip_codebook_t cb;
+    cb.dtype = h.dtype;
+    std::memcpy(cb.exps, h.codebook, 16);
+    if (check_codebook(&cb, h.dtype) != SPLITZIP_OK) return SPLITZIP_ERR_CORRUPT;
+    const Layout L = layout_for(h.n_elems, h.dtype, h.chunk_elems, h.total_escapes);
+    if (L.size > bytes) return SPLITZIP_ERR_CORRUPT;
+    h.size = L.size;
+    h.index_off = L.index_off;
+    h.counts_off = L.counts_off;
+    h.nibble_off = L.nibble_off;
+    h.signmant_off = L.signmant_off;
+    h.escpos_off = L.escpos_off;
+    h.escexp_off = L.escexp_off;
+    *out = h;
+    return SPLITZIP_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,128 @@
+// Internal definitions shared by the SplitZip GB300 kernels and the C ABI.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "splitzip.h"
+
+namespace splitzip {
+
+constexpr uint32_t kMagic = 0x50495A53u;  // "SZIP" little-endian
+constexpr uint16_t kVersion = 1;
+constexpr uint64_t kHeaderBytes = 64;
+constexpr uint32_t kMinChunk = 64;
+constexpr uint32_t kMaxChunk = 65536;
+
+// Work decomposition.  A tile is the unit one CTA processes per loop trip:
+// 256 threads x 32 elements.  A tile never straddles a chunk (chunk sizes are
+// powers of two >= 64, so tile_elems = min(kTileElems, chunk_elems) divides
+// chunk_elems).
+constexpr int kEncodeThreads = 256;
+constexpr uint32_t kTileElems = 8192;
+constexpr int kDecodeThreads = 512;
+constexpr int kHistThreads = 256;
+constexpr int kIndexThreads = 1024;
+constexpr int kGatherThreads = 256;
+
+// Encoder table entry: low 4 bits = code, bit 4 = escape flag.
+constexpr uint8_t kEscapeFlag = 0x10;
+
+__host__ __device__ inline uint64_t align16(uint64_t x) { return (x + 15u) & ~uint64_t(15); }
+
+__host__ __device__ inline uint64_t signmant_bytes(int dtype, uint64_t n) {
+    return dtype == SPLITZIP_BF16 ? n : 3u * ((n + 7u) / 8u);
+}
+
+// Byte offsets of every section of a container (format v1, see splitzip.h).
+struct Layout {
+    uint64_t n_chunks;
+    uint64_t index_off, counts_off, index_end, nibble_off, signmant_off, escpos_off, escexp_off, size;
+};
+
+__host__ __device__ inline Layout layout_for(uint64_t n, int dtype, uint32_t chunk, uint64_t E) {
+    Layout L;
+    L.n_chunks = (n + chunk - 1u) / chunk;
+    L.index_off = kHeaderBytes;
+    L.counts_off = L.index_off + 8u * L.n_chunks;
+    L.index_end = L.counts_off + 4u * L.n_chunks;
+    L.nibble_off = align16(L.index_end);
+    L.signmant_off = L.nibble_off + align16((n + 1u) / 2u);
+    L.escpos_off = L.signmant_off + align16(signmant_bytes(dtype, n));
+    L.escexp_off = L.escpos_off + align16(2u * E);
+    L.size = L.escexp_off + E;
+    return L;
+}
+
+__host__ __device__ inline uint32_t tile_elems_for(uint32_t chunk) {
+    return chunk < kTileElems ? chunk : kTileElems;
+}
+
+// Encoder workspace: per-tile escape counts, then per-tile staging slots of
+// tile_elems records each.  A record is (in-chunk position << 8) | exponent.
+struct Workspace {
+    uint64_t n_tiles;
+    uint32_t tile_elems;
+    uint64_t counts_off, staging_off, bytes;
+};
+
+__host__ __device__ inline Workspace workspace_for(uint64_t n, uint32_t chunk) {
+    Workspace W;
+    W.tile_elems = tile_elems_for(chunk);
+    W.n_tiles = (n + W.tile_elems - 1u) / W.tile_elems;
+    W.counts_off = 0;
+    W.staging_off = align16(4u * W.n_tiles);
+    W.bytes = W.staging_off + 4u * W.n_tiles * W.tile_elems;
+    return W;
+}
+
+struct EncodeLut {
+    uint8_t code[256];  // exponent -> code | kEscapeFlag
+};
+
+struct EncodeArgs {
+    const void* in;
+    uint64_t n;
+    uint8_t* out;           // container base
+    uint8_t* nibbles;       // out + nibble_off
+    uint8_t* signmant;      // out + signmant_off
+    uint32_t* tile_counts;  // workspace
+    uint32_t* staging;      // workspace
+    uint64_t n_tiles;
+    uint32_t tile_elems;
+    uint32_t chunk_elems;
+    uint64_t n_chunks;
+    int dtype;
+    uint8_t codebook[16];
+};
+
+struct DecodeArgs {
+    const uint8_t* in;
+    uint64_t in_bytes;
+    void* out;
+    uint64_t n;
+    int dtype;
+    int* status;
+};
+
+// Launchers (encode.cu, decode.cu, histogram.cu).  Each returns the result of
+// cudaGetLastError() after its launches.
+cudaError_t launch_encode_streams(const EncodeArgs& a, const EncodeLut& lut, int grid, cudaStream_t s);
+cudaError_t launch_encode_escapes(const EncodeArgs& a, uint64_t* d_out_size, int* d_status, int grid,
+                                  cudaStream_t s);
+cudaError_t launch_decode(const DecodeArgs& a, int grid, cudaStream_t s);
+cudaError_t launch_histogram(const void* x, uint64_t n, int dtype, unsigned long long* hist, int grid,
+                             cudaStream_t s);
+
+// Resident-CTA counts per SM for each kernel (filled once per device).
+struct DeviceInfo {
+    int sm_count;
+    int cc_major, cc_minor;
+    int encode_blocks_per_sm, decode_blocks_per_sm, gather_blocks_per_sm, hist_blocks_per_sm;
+};
+cudaError_t occupancy_encode(int* blocks_per_sm, int dtype);
+cudaError_t occupancy_decode(int* blocks_per_sm, int dtype);
+cudaError_t occupancy_gather(int* blocks_per_sm);
+cudaError_t occupancy_histogram(int* blocks_per_sm, int dtype);
+
+}  // namespace splitzip

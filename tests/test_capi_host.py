@@ -1,0 +1,159 @@
+"""C ABI checks that need no GPU: the library loads and exports every entry
+point include/splitzip.h declares, and the host-side logic (sizes, argument
+checks, codebook calibration, header parsing) agrees with the CPU oracle."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import lossless_kv_cache_gb300 as sz
+from lossless_kv_cache_gb300 import workloads as W
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "splitzip.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(splitzip_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for required in ("splitzip_calibrate", "splitzip_max_compressed_size", "splitzip_encode", "splitzip_decode",
+                     "splitzip_exponent_histogram", "splitzip_parse_header"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(splitzip_lib):
+    for name in declared_functions():
+        assert hasattr(splitzip_lib, name), name
+    # the binding mirrors the C names
+    assert set(sz.SIGNATURES) == set(declared_functions())
+    for name in declared_functions():
+        assert callable(getattr(sz, name))
+
+
+def test_status_strings(splitzip_lib):
+    assert sz.splitzip_status_string(sz.OK) == "ok"
+    assert "corrupt" in sz.splitzip_status_string(sz.ERR_CORRUPT)
+    assert sz.splitzip_status_string(99) == "unknown status"
+
+
+@pytest.mark.parametrize("dtype", [sz.BF16, sz.FP8_E5M2])
+@pytest.mark.parametrize("chunk", [64, 256, 8192, 65536])
+def test_sizes_match_oracle(splitzip_lib, dtype, chunk):
+    for n in (0, 1, 2, 7, 31, 64, 65, 1000, 65537, 2**31 + 3, 2**32):
+        for E in {0, 1, n // 3, n}:
+            if E > n:
+                continue
+            assert sz.compressed_size(n, dtype, chunk, E) == oracle.container_size(n, dtype, chunk, E)
+        assert sz.max_compressed_size(n, dtype, chunk) == oracle.max_container_size(n, dtype, chunk)
+
+
+def test_workspace_size(splitzip_lib):
+    # per-tile counts + 4 bytes of staging per element slot
+    n = 5 * 8192 + 3
+    tiles = 6
+    assert sz.workspace_size(n, sz.BF16, 65536) == -(-4 * tiles // 16) * 16 + 4 * tiles * 8192
+    assert sz.workspace_size(0, sz.BF16, 65536) == 0
+
+
+def test_size_argument_errors(splitzip_lib):
+    out = ctypes.c_uint64(0)
+    assert sz.splitzip_max_compressed_size(10, 2, 65536, out) == sz.ERR_INVALID_ARG      # dtype
+    assert sz.splitzip_max_compressed_size(10, 0, 100, out) == sz.ERR_INVALID_ARG        # not pow2
+    assert sz.splitzip_max_compressed_size(10, 0, 32, out) == sz.ERR_INVALID_ARG         # < 64
+    assert sz.splitzip_max_compressed_size(10, 0, 131072, out) == sz.ERR_INVALID_ARG     # > 65536
+    assert sz.splitzip_compressed_size(10, 0, 64, 11, out) == sz.ERR_INVALID_ARG         # E > n
+    assert sz.splitzip_max_compressed_size(2**49, 0, 65536, out) == sz.ERR_UNSUPPORTED
+
+
+def _cb(dtype, exps=None):
+    return sz.Codebook.make(dtype, exps if exps is not None else range(16))
+
+
+def test_encode_argument_errors_are_host_side(splitzip_lib):
+    n, chunk = 1000, 64
+    cap = sz.max_compressed_size(n, 0, chunk)
+    ws = sz.workspace_size(n, 0, chunk)
+    A = 1 << 20  # a 16-aligned fake device address: no call below reaches the GPU
+    good = dict(d_in=A, n=n, dtype=0, cb=_cb(0), chunk_elems=chunk, d_out=A, out_capacity=cap, d_ws=A,
+                ws_bytes=ws, d_out_size=A, d_status=A, stream=0)
+
+    def call(**kw):
+        args = dict(good, **kw)
+        return sz.splitzip_encode(**args)
+
+    assert call(dtype=5) == sz.ERR_INVALID_ARG
+    assert call(chunk_elems=96) == sz.ERR_INVALID_ARG
+    assert call(d_in=None) == sz.ERR_INVALID_ARG
+    assert call(d_in=A + 8) == sz.ERR_INVALID_ARG          # misaligned
+    assert call(d_out=None) == sz.ERR_INVALID_ARG
+    assert call(d_out_size=None) == sz.ERR_INVALID_ARG
+    assert call(d_status=None) == sz.ERR_INVALID_ARG
+    assert call(out_capacity=cap - 1) == sz.ERR_CAPACITY
+    assert call(ws_bytes=ws - 1) == sz.ERR_CAPACITY
+    assert call(d_ws=None) == sz.ERR_INVALID_ARG
+    assert call(cb=_cb(1)) == sz.ERR_INVALID_ARG            # codebook of another dtype
+    assert call(cb=_cb(0, [1] * 16)) == sz.ERR_INVALID_ARG  # duplicate exponents
+    assert call(dtype=1, cb=_cb(1, range(20, 36))) == sz.ERR_INVALID_ARG  # E5M2 exponent >= 32
+
+
+def test_decode_argument_errors_are_host_side(splitzip_lib):
+    A = 1 << 20
+    assert sz.splitzip_decode(None, 64, A, 10, 0, A, 0) == sz.ERR_INVALID_ARG
+    assert sz.splitzip_decode(A + 4, 64, A, 10, 0, A, 0) == sz.ERR_INVALID_ARG
+    assert sz.splitzip_decode(A, 64, A, 10, 3, A, 0) == sz.ERR_INVALID_ARG
+    assert sz.splitzip_decode(A, 64, A, 10, 0, None, 0) == sz.ERR_INVALID_ARG
+    assert sz.splitzip_decode(A, 63, A, 10, 0, A, 0) == sz.ERR_CORRUPT
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU error path")
+def test_valid_call_without_gpu_reports_cuda_error(splitzip_lib):
+    A = 1 << 20
+    st = sz.splitzip_decode(A, 1 << 20, A, 10, 0, A, 0)
+    assert st in (sz.ERR_CUDA, sz.ERR_UNSUPPORTED)
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_calibrate_host_histogram_matches_oracle(splitzip_lib, seed):
+    rng = np.random.default_rng(seed)
+    for dtype, bins in ((sz.BF16, 256), (sz.FP8_E5M2, 32)):
+        h = np.zeros(256, dtype=np.uint64)
+        support = rng.choice(bins, size=rng.integers(1, bins + 1), replace=False)
+        h[support] = rng.integers(0, 4, size=support.size) * rng.integers(1, 1 << 40)
+        cb = sz.Codebook()
+        assert sz.splitzip_calibrate(h.ctypes.data, 0, dtype, cb) == sz.OK
+        assert cb.dtype == dtype
+        np.testing.assert_array_equal(np.array(cb.values(), np.uint8), oracle.calibrate(h, dtype))
+
+
+def test_calibrate_rejects_bad_e5m2_histogram(splitzip_lib):
+    h = np.zeros(256, dtype=np.uint64)
+    h[33] = 1
+    assert sz.splitzip_calibrate(h.ctypes.data, 0, sz.FP8_E5M2, sz.Codebook()) == sz.ERR_INVALID_ARG
+
+
+def test_parse_header_matches_oracle(splitzip_lib):
+    x = W.escape_stress(2, chunks=3, chunk_elems=4096).numpy().view(np.uint16)[:10001]
+    cb = oracle.calibrate(oracle.histogram(x, 0), 0)
+    blob = oracle.encode(x, 0, cb, 2048)
+    h = sz.parse_header(blob)
+    st, ref = oracle.parse_header(blob)
+    assert st == oracle.OK
+    assert (h.n_elems, h.total_escapes, h.size, h.chunk_elems, h.n_chunks, h.dtype) == (
+        ref.n, ref.total_escapes, ref.size, ref.chunk_elems, ref.n_chunks, ref.dtype)
+    assert list(h.codebook) == list(ref.codebook)
+    assert h.size == blob.size
+    # header-level corruptions are rejected like the oracle rejects them
+    from tests.test_oracle_pins import corruptions
+    for name, bad in corruptions(blob):
+        o_st, _ = oracle.parse_header(bad)
+        buf = np.ascontiguousarray(bad)
+        st = sz.splitzip_parse_header(buf.ctypes.data, buf.size, sz.Header())
+        assert (st == sz.OK) == (o_st == oracle.OK), name
