@@ -43,6 +43,8 @@ def parse_args():
     p.add_argument("--cpu-seconds", type=float, default=10.0, help="oracle time budget for cpu_baseline")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--layers", type=int, default=32,
+                   help="encode only the first L layers (a smaller case for profiling; not a bench line)")
     return p.parse_args()
 
 
@@ -152,15 +154,16 @@ class ClockSampler:
 
 # ------------------------------------------------------------ workload
 
-def generate(seed, device):
+def generate(seed, device, layers):
     from lossless_kv_cache_gb300 import workloads as W
-    n_layers, layer = W.layers_of(WORKLOAD)
-    parts = [layer(seed, l, device) for l in range(n_layers)]
+    _, layer = W.layers_of(WORKLOAD)
+    parts = [layer(seed, l, device) for l in range(layers)]
     return torch.cat(parts)
 
 
-def config_dict(world):
-    return {"workload": WORKLOAD, "shape": [32, 2, 32768, 8, 128], "elements": 2147483648,
+def config_dict(world, layers=32):
+    name = WORKLOAD if layers == 32 else "%s (first %d layers only: profiling case)" % (WORKLOAD, layers)
+    return {"workload": name, "shape": [layers, 2, 32768, 8, 128], "elements": layers * 2 * 32768 * 1024,
             "element_dtype": "bf16", "chunk_elems": CHUNK, "codebook": "Top-16 from layer 0 of seed 1",
             "l2": "inputs 4.29 GB > 129 MB L2 (no flush needed)",
             "parallelism": "replicas of the workload per GPU, no collective" if world > 1 else "single GPU"}
@@ -173,15 +176,16 @@ def escape_rate_of(blob_hdr_bytes, n):
 
 # --------------------------------------------------------- CPU oracle
 
-def oracle_throughput(x_host_bits, cb_exps, seconds, max_chunks):
-    """Encode + decode successive 64-chunk blocks with the scalar oracle until
-    `seconds` of CPU time are spent; returns (GB/s uncompressed, elements, s)."""
+def oracle_throughput(x_dev, cb_exps, seconds):
+    """Encode + decode successive 64-chunk blocks of the workload with the
+    scalar oracle until `seconds` of CPU time are spent; returns (GB/s
+    uncompressed, elements, seconds)."""
     import oracle
     block = 64 * CHUNK
     done, t_total = 0, 0.0
     cb = np.asarray(cb_exps, dtype=np.uint8)
-    while t_total < seconds and done + block <= min(x_host_bits.size, max_chunks * CHUNK):
-        xs = x_host_bits[done: done + block]
+    while t_total < seconds and done + block <= x_dev.numel():
+        xs = x_dev[done: done + block].cpu().numpy().view(np.uint16)
         t0 = time.perf_counter()
         blob = oracle.encode(xs, 0, cb, CHUNK)
         y = oracle.decode(blob, xs.size, 0)
@@ -237,10 +241,10 @@ def run_ours(args, world, rank, local):
     device = torch.device("cuda", local)
     torch.cuda.set_device(device)
     sz.lib()  # fails loudly when the CUDA library is missing
-    n = 32 * 2 * 32768 * 1024
+    n = args.layers * 2 * 32768 * 1024
     raw_bytes = 2 * n
 
-    x = generate(rank, device)  # weak scaling: every rank has its own workload
+    x = generate(rank, device, args.layers)  # weak scaling: every rank has its own workload
     from lossless_kv_cache_gb300 import workloads as W
     _, layer = W.layers_of(WORKLOAD)
     cal = layer(1, 0, device)
@@ -375,8 +379,7 @@ def run_ours(args, world, rank, local):
     # ---- CPU oracle on a bounded sample (rank 0 only) ----
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
-        xh = x[: 512 * CHUNK].cpu().numpy().view(np.uint16)
-        gbs, elems, secs = oracle_throughput(xh, cb.values(), args.cpu_seconds, 512)
+        gbs, elems, secs = oracle_throughput(x, cb.values(), args.cpu_seconds)
         cpu = {"value": round(gbs, 5), "unit": "GB/s", "cores": 1, "kind": "oracle",
                "sample": "%d elements (first %d chunks of the workload), encode+decode, %.1f s, scalar C "
                          "oracle, 1 thread" % (elems, elems // CHUNK, secs)}
@@ -388,7 +391,7 @@ def run_ours(args, world, rank, local):
         "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "u16",
         "data": "synthetic (seeded torch CUDA generator; recipe of the workload module)",
-        "config": config_dict(world),
+        "config": config_dict(world, args.layers),
         "encode_gbs": round(enc_gbs, 2), "decode_gbs": round(dec_gbs, 2),
         "encode_hbm_frac": round(enc_alg / (enc_ms * 1e-3) / 1e9 / hbm, 4),
         "decode_hbm_frac": round(alg_decode / (dec_ms * 1e-3) / 1e9 / hbm, 4),
