@@ -163,6 +163,31 @@ int splitzip_encode_escapes(uint64_t n, int dtype, uint32_t chunk_elems, void* d
                             uint64_t out_capacity, void* d_ws, uint64_t ws_bytes,
                             uint64_t* d_out_size, int* d_status, cudaStream_t stream);
 
+/* Size of the device array that splitzip_encode_noalloc uses as scratch. */
+#define SPLITZIP_NOALLOC_SCRATCH_BYTES (32ull << 20)
+
+/* splitzip_encode without a caller-provided workspace.  The SplitZip page has
+ * no counterpart to this entry point; it exists for callers that cannot
+ * allocate device memory at encode time: a serving engine whose KV pool and
+ * allocator already own nearly all of the GPU's memory, or a path that must
+ * not call cudaMalloc/cudaFree because they can synchronise the device.
+ * Its scratch is a fixed device array of SPLITZIP_NOALLOC_SCRATCH_BYTES
+ * (32 MiB) held by every GPU that loads this library until the process
+ * exits.  Limits: n must satisfy splitzip_encode_workspace_size(n, dtype,
+ * chunk_elems) <= SPLITZIP_NOALLOC_SCRATCH_BYTES (8,380,416 elements at the
+ * default chunk size); larger n returns SPLITZIP_ERR_CAPACITY before any GPU
+ * work.  The call allocates nothing: the caller still passes input, output,
+ * d_out_size and d_status exactly as for splitzip_encode, and the output is
+ * byte-identical to splitzip_encode's.  The first call on each device looks up
+ * the array's device address (cudaGetSymbolAddress) with that device current;
+ * make that first call before any stream capture.  Every call on a device
+ * shares the array, so calls whose GPU work overlaps (other streams or host
+ * threads) race and must be serialised by the caller; no clearing between
+ * calls is needed, the encoder writes every scratch byte it reads. */
+int splitzip_encode_noalloc(const void* d_in, uint64_t n, int dtype, const splitzip_codebook_t* cb,
+                            uint32_t chunk_elems, void* d_out, uint64_t out_capacity,
+                            uint64_t* d_out_size, int* d_status, cudaStream_t stream);
+
 /* Decode a container into n elements (Method, "Decoding strategy").
  * d_in: in_bytes bytes of container (in_bytes >= its size); d_out: n
  * elements.  The GPU checks the header (magic, version, dtype and n equal to

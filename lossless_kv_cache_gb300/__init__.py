@@ -22,6 +22,7 @@ FP8_E5M2 = 1
 OK, ERR_INVALID_ARG, ERR_CAPACITY, ERR_CORRUPT, ERR_CUDA, ERR_TIMEOUT, ERR_UNSUPPORTED = range(7)
 DEFAULT_CHUNK_ELEMS = 65536
 HEADER_BYTES = 64
+NOALLOC_SCRATCH_BYTES = 32 << 20  # SPLITZIP_NOALLOC_SCRATCH_BYTES
 
 
 class SplitZipError(RuntimeError):
@@ -81,6 +82,8 @@ SIGNATURES = {
     "splitzip_encode_streams": (_int, [_vp, _u64, _int, ctypes.POINTER(Codebook), _u32, _vp, _u64, _vp,
                                        _u64, _vp]),
     "splitzip_encode_escapes": (_int, [_u64, _int, _u32, _vp, _u64, _vp, _u64, _vp, _vp, _vp]),
+    "splitzip_encode_noalloc": (_int, [_vp, _u64, _int, ctypes.POINTER(Codebook), _u32, _vp, _u64, _vp, _vp,
+                                       _vp]),
     "splitzip_decode": (_int, [_vp, _u64, _vp, _u64, _int, _vp, _vp]),
     "splitzip_parse_header": (_int, [_vp, _u64, ctypes.POINTER(Header)]),
 }
@@ -144,6 +147,11 @@ def splitzip_encode_streams(d_in, n, dtype, cb, chunk_elems, d_out, out_capacity
 def splitzip_encode_escapes(n, dtype, chunk_elems, d_out, out_capacity, d_ws, ws_bytes, d_out_size, d_status,
                             stream):
     return lib().splitzip_encode_escapes(n, dtype, chunk_elems, d_out, out_capacity, d_ws, ws_bytes,
+                                         d_out_size, d_status, stream)
+
+
+def splitzip_encode_noalloc(d_in, n, dtype, cb, chunk_elems, d_out, out_capacity, d_out_size, d_status, stream):
+    return lib().splitzip_encode_noalloc(d_in, n, dtype, ctypes.byref(cb), chunk_elems, d_out, out_capacity,
                                          d_out_size, d_status, stream)
 
 
