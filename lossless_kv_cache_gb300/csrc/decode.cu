@@ -11,10 +11,14 @@
 //     barrier), the chunk's escape records overwrite the exponent field of the
 //     escaped elements, making the output bit-exact.
 //
-// Persistent grid: each CTA loops over chunks.  Every CTA validates the header
-// first; each chunk validates its index entry and each escape record, and
-// errors go to the status word without any out-of-bounds access.
+// Persistent grid: each CTA loops over its chunks.  A producer warp streams
+// the chunks' nibble and sign|mantissa bytes into a 4-stage shared-memory ring
+// with bulk copies (TMA); eight consumer warps decode from shared memory and
+// write 16-byte streaming stores.  Every CTA validates the header first; each
+// chunk validates its index entry and each escape record, and errors go to the
+// status word without any out-of-bounds access.
 #include "splitzip_internal.cuh"
+#include "tma_pipeline.cuh"
 
 namespace splitzip {
 namespace {
@@ -31,7 +35,7 @@ __device__ __forceinline__ void report(int* status, int code) { atomicCAS(status
 // Header checks (format v1): magic, version, dtype and n as given, reserved
 // bytes zero, chunk size, chunk count, E <= n, codebook distinct and in range,
 // container size within in_bytes.
-__device__ bool read_header(const DecodeArgs& a, Header& h) {
+__device__ __forceinline__ bool read_header(const DecodeArgs& a, Header& h) {
     if (a.in_bytes < kHeaderBytes) return false;
     const uint4* p = reinterpret_cast<const uint4*>(a.in);
     const uint4 q0 = p[0], q1 = p[1], q2 = p[2], q3 = p[3];
@@ -47,13 +51,22 @@ __device__ bool read_header(const DecodeArgs& a, Header& h) {
     if (h.chunk < kMinChunk || h.chunk > kMaxChunk || (h.chunk & (h.chunk - 1u)) != 0u) return false;
     if ((h.n + h.chunk - 1u) / h.chunk != h.n_chunks) return false;
     if (h.E > h.n) return false;
-    const uint32_t cbw[4] = {q2.x, q2.y, q2.z, q2.w};
     const uint32_t bins = a.dtype == SPLITZIP_BF16 ? 256u : 32u;
-    uint32_t seen[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+    uint64_t seen[4] = {0u, 0u, 0u, 0u};  // set of exponents met so far (constant indices only)
+#pragma unroll
     for (int i = 0; i < 16; ++i) {
-        const uint32_t e = (cbw[i >> 2] >> (8 * (i & 3))) & 0xFFu;
-        if (e >= bins || (seen[e >> 5] >> (e & 31)) & 1u) return false;
-        seen[e >> 5] |= 1u << (e & 31);
+        const uint32_t w = i < 4 ? q2.x : i < 8 ? q2.y : i < 12 ? q2.z : q2.w;
+        const uint32_t e = (w >> (8 * (i & 3))) & 0xFFu;
+        const uint64_t bit = uint64_t(1) << (e & 63u);
+        bool dup = false;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            if ((e >> 6) == uint32_t(q)) {
+                dup = (seen[q] & bit) != 0;
+                seen[q] |= bit;
+            }
+        }
+        if (e >= bins || dup) return false;
         h.codebook[i] = uint8_t(e);
     }
     h.L = layout_for(h.n, a.dtype, h.chunk, h.E);
@@ -100,23 +113,116 @@ __device__ __forceinline__ uint4 decode_unit_e5m2(uint2 nib, uint32_t s3lo, uint
     return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
+// Decode work: each CTA walks its chunks (c = blockIdx.x, +gridDim.x, ...)
+// as a sequence of sub-tiles of up to kSub elements.  Producer and consumers
+// walk the same sequence, so sub-tile i always lives in stage i % kStages.
+constexpr int kConsumerWarps = 8;
+constexpr int kConsumers = kConsumerWarps * 32;
+constexpr int kBlock = kConsumers + 32;  // + one producer warp
+constexpr int kStages = 4;
+constexpr uint32_t kSub = 8192;
+constexpr uint32_t kNibCap = kSub / 2 + 32;  // + room for a 16-byte window shift
+constexpr uint32_t kSmCap = kSub + 32;
+constexpr uint32_t kStageBytes = (kNibCap + kSmCap + 127u) & ~127u;
+constexpr uint32_t kDecodeSmem = kStages * kStageBytes;
+
+struct SubTile {
+    Window nib, sm;
+};
+
 template <int DT>
-__global__ void __launch_bounds__(kDecodeThreads) decode_kernel(const DecodeArgs a) {
-    constexpr int kUnitElems = DT == SPLITZIP_BF16 ? 8 : 16;
-    constexpr int kWarps = kDecodeThreads / 32;
+__device__ __forceinline__ SubTile subtile_windows(const uint8_t* nibbles, const uint8_t* signmant, uint64_t g,
+                                                   uint32_t cnt) {
+    SubTile t;
+    t.nib = window_of(nibbles + g / 2, (cnt + 1u) / 2u);
+    if constexpr (DT == SPLITZIP_BF16)
+        t.sm = window_of(signmant + g, cnt);
+    else
+        t.sm = window_of(signmant + g / 8u * 3u, 3u * ((cnt + 7u) / 8u));
+    return t;
+}
+
+// Dense decode of one sub-tile from shared memory; results go straight to
+// global memory with 16-byte streaming stores.
+template <int DT>
+__device__ __forceinline__ void decode_subtile(const uint8_t* nb, const uint8_t* sb, void* out_base, uint64_t g,
+                                               uint32_t cnt, int tid, const uint16_t* lut2) {
+    if constexpr (DT == SPLITZIP_BF16) {
+        uint16_t* out = static_cast<uint16_t*>(out_base) + g;
+        const uint32_t units = (cnt + 7u) / 8u;
+#pragma unroll 4
+        for (uint32_t u = tid; u < units; u += kConsumers) {
+            const uint32_t e = 8u * u;
+            if (e + 8u <= cnt) {
+                const uint32_t nib = *reinterpret_cast<const uint32_t*>(nb + e / 2);
+                const uint2 sm = *reinterpret_cast<const uint2*>(sb + e);
+                __stcs(reinterpret_cast<uint4*>(out + e), decode_unit_bf16(nib, sm, lut2));
+            } else {
+                const uint32_t valid = cnt - e;
+                uint32_t nib = 0;
+                uint64_t smw = 0;
+                for (uint32_t b = 0; b < (valid + 1u) / 2u; ++b) nib |= uint32_t(nb[e / 2 + b]) << (8u * b);
+                for (uint32_t b = 0; b < valid; ++b) smw |= uint64_t(sb[e + b]) << (8u * b);
+                const uint4 o = decode_unit_bf16(nib, make_uint2(uint32_t(smw), uint32_t(smw >> 32)), lut2);
+                for (uint32_t k = 0; k < valid; ++k) {
+                    const uint32_t q = k >> 1;
+                    const uint32_t w = q == 0 ? o.x : q == 1 ? o.y : q == 2 ? o.z : o.w;
+                    out[e + k] = uint16_t(w >> (16u * (k & 1u)));
+                }
+            }
+        }
+    } else {
+        uint8_t* out = static_cast<uint8_t*>(out_base) + g;
+        const uint32_t units = (cnt + 15u) / 16u;
+#pragma unroll 2
+        for (uint32_t u = tid; u < units; u += kConsumers) {
+            const uint32_t e = 16u * u;
+            // 6 bytes of s3 per unit, 2-byte aligned in the stage
+            const uint16_t* s16 = reinterpret_cast<const uint16_t*>(sb + 6u * u);
+            if (e + 16u <= cnt) {
+                const uint2 nib = *reinterpret_cast<const uint2*>(nb + e / 2);
+                const uint32_t s3lo = uint32_t(s16[0]) | (uint32_t(s16[1]) << 16), s3hi = s16[2];
+                __stcs(reinterpret_cast<uint4*>(out + e), decode_unit_e5m2(nib, s3lo, s3hi, lut2));
+            } else {
+                const uint32_t valid = cnt - e;
+                uint64_t nw = 0, sw = 0;
+                for (uint32_t b = 0; b < (valid + 1u) / 2u; ++b) nw |= uint64_t(nb[e / 2 + b]) << (8u * b);
+                const uint8_t* s8 = sb + 6u * u;
+                for (uint32_t b = 0; b < 3u * ((valid + 7u) / 8u); ++b) sw |= uint64_t(s8[b]) << (8u * b);
+                const uint4 o = decode_unit_e5m2(make_uint2(uint32_t(nw), uint32_t(nw >> 32)), uint32_t(sw),
+                                                 uint32_t(sw >> 32), lut2);
+                for (uint32_t k = 0; k < valid; ++k) {
+                    const uint32_t q = k >> 2;
+                    const uint32_t w = q == 0 ? o.x : q == 1 ? o.y : q == 2 ? o.z : o.w;
+                    out[e + k] = uint8_t(w >> (8u * (k & 3u)));
+                }
+            }
+        }
+    }
+}
+
+template <int DT>
+__global__ void __launch_bounds__(kBlock) decode_kernel(const DecodeArgs a) {
+    extern __shared__ __align__(128) uint8_t stages[];
+    __shared__ __align__(8) uint64_t full_bar[kStages];
+    __shared__ __align__(8) uint64_t empty_bar[kStages];
     __shared__ Header hdr;
     __shared__ int header_ok;
     __shared__ uint16_t lut2[256];  // nibble byte -> (exponent of low code) | (exponent of high code) << 8
-    __shared__ __align__(16) uint8_t s3_stage[kWarps][192];
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     if (tid == 0) {
         header_ok = read_header(a, hdr);
         if (!header_ok) report(a.status, SPLITZIP_ERR_CORRUPT);
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&full_bar[s], 1);
+            mbar_init(&empty_bar[s], kConsumerWarps);
+        }
+        mbar_init_fence();
     }
     __syncthreads();
     if (!header_ok) return;
-    for (int b = tid; b < 256; b += kDecodeThreads)
+    for (int b = tid; b < 256; b += kBlock)
         lut2[b] = uint16_t(hdr.codebook[b & 15]) | uint16_t(hdr.codebook[b >> 4] << 8);
     __syncthreads();
 
@@ -124,102 +230,62 @@ __global__ void __launch_bounds__(kDecodeThreads) decode_kernel(const DecodeArgs
     const Layout L = hdr.L;
     const uint8_t* nibbles = in + L.nibble_off;
     const uint8_t* signmant = in + L.signmant_off;
+    const uint64_t chunk = hdr.chunk, C = hdr.n_chunks, E = hdr.E;
+    const uint32_t sub = uint32_t(min(uint64_t(kSub), chunk));
+
+    if (warp == kConsumerWarps) {
+        // ---- producer: one thread streams the sub-tiles into the stages ----
+        if (lane != 0) return;
+        uint32_t it = 0;
+        for (uint64_t c = blockIdx.x; c < C; c += gridDim.x) {
+            const uint64_t base = c * chunk;
+            const uint32_t len = uint32_t(min(chunk, a.n - base));
+            for (uint32_t s0 = 0; s0 < len; s0 += sub, ++it) {
+                const uint32_t stage = it % kStages, use = it / kStages;
+                if (use > 0 && !mbar_wait(&empty_bar[stage], (use - 1) & 1u)) report(a.status, SPLITZIP_ERR_TIMEOUT);
+                const SubTile t = subtile_windows<DT>(nibbles, signmant, base + s0, min(sub, len - s0));
+                uint8_t* dst = stages + stage * kStageBytes;
+                mbar_arrive_expect_tx(&full_bar[stage], t.nib.bytes + t.sm.bytes);
+                bulk_load(dst, t.nib.src, t.nib.bytes, &full_bar[stage]);
+                bulk_load(dst + kNibCap, t.sm.src, t.sm.bytes, &full_bar[stage]);
+            }
+        }
+        return;
+    }
+
+    // ---- consumers: dense decode per sub-tile, then the chunk's correction ----
     const uint64_t* offsets = reinterpret_cast<const uint64_t*>(in + L.index_off);
     const uint32_t* counts = reinterpret_cast<const uint32_t*>(in + L.counts_off);
     const uint16_t* esc_pos = reinterpret_cast<const uint16_t*>(in + L.escpos_off);
     const uint8_t* esc_exp = in + L.escexp_off;
-    const uint64_t chunk = hdr.chunk, C = hdr.n_chunks, E = hdr.E;
-
+    uint32_t it = 0;
     for (uint64_t c = blockIdx.x; c < C; c += gridDim.x) {
         const uint64_t base = c * chunk;
         const uint32_t len = uint32_t(min(chunk, a.n - base));
-        // ---- dense path ----
-        for (uint32_t e = uint32_t(tid) * kUnitElems; e < len; e += kDecodeThreads * kUnitElems) {
-            const uint32_t valid = min(len - e, uint32_t(kUnitElems));
-            const uint64_t g = base + e;  // global element index of the unit
-            if constexpr (DT == SPLITZIP_BF16) {
-                uint32_t nib;
-                uint2 sm;
-                if (valid == 8u) {
-                    nib = __ldcs(reinterpret_cast<const uint32_t*>(nibbles + g / 2));
-                    sm = __ldcs(reinterpret_cast<const uint2*>(signmant + g));
-                } else {
-                    nib = 0u;
-                    uint64_t smw = 0;
-                    for (uint32_t b = 0; b < (valid + 1u) / 2u; ++b) nib |= uint32_t(nibbles[g / 2 + b]) << (8u * b);
-                    for (uint32_t b = 0; b < valid; ++b) smw |= uint64_t(signmant[g + b]) << (8u * b);
-                    sm = make_uint2(uint32_t(smw), uint32_t(smw >> 32));
-                }
-                const uint4 o = decode_unit_bf16(nib, sm, lut2);
-                uint16_t* out = static_cast<uint16_t*>(a.out) + g;
-                if (valid == 8u) {
-                    __stcs(reinterpret_cast<uint4*>(out), o);
-                } else {
-                    for (uint32_t k = 0; k < valid; ++k) {
-                        const uint32_t q = k >> 1;
-                        const uint32_t w = q == 0 ? o.x : q == 1 ? o.y : q == 2 ? o.z : o.w;
-                        out[k] = uint16_t(w >> (16u * (k & 1u)));
-                    }
-                }
-            } else {
-                // s3 bytes of this unit: 6 per unit starting at 3 * g / 8.
-                // Fast path: the warp's 32 units are full and 512-aligned in the
-                // chunk, so the warp's 192 bytes are 16-aligned.
-                const uint32_t warp_e0 = e - uint32_t(lane) * kUnitElems;
-                const bool warp_full = (chunk % 512u == 0u) && (warp_e0 + 512u <= len);
-                uint32_t s3lo, s3hi;
-                if (warp_full) {  // warp-uniform
-                    if (lane < 12) {
-                        const uint8_t* src = signmant + (base + warp_e0) / 8 * 3 + 16 * lane;
-                        reinterpret_cast<uint4*>(s3_stage[warp])[lane] = __ldcs(reinterpret_cast<const uint4*>(src));
-                    }
-                    __syncwarp();
-                    const uint16_t* st = reinterpret_cast<const uint16_t*>(&s3_stage[warp][6 * lane]);
-                    s3lo = uint32_t(st[0]) | (uint32_t(st[1]) << 16);
-                    s3hi = st[2];
-                    __syncwarp();
-                } else {
-                    const uint8_t* src = signmant + g / 8 * 3;
-                    const uint32_t nbytes = 3u * ((valid + 7u) / 8u);
-                    uint64_t w = 0;
-                    for (uint32_t b = 0; b < nbytes; ++b) w |= uint64_t(src[b]) << (8u * b);
-                    s3lo = uint32_t(w);
-                    s3hi = uint32_t(w >> 32);
-                }
-                uint2 nib;
-                if (valid == 16u) {
-                    nib = __ldcs(reinterpret_cast<const uint2*>(nibbles + g / 2));
-                } else {
-                    uint64_t w = 0;
-                    for (uint32_t b = 0; b < (valid + 1u) / 2u; ++b) w |= uint64_t(nibbles[g / 2 + b]) << (8u * b);
-                    nib = make_uint2(uint32_t(w), uint32_t(w >> 32));
-                }
-                const uint4 o = decode_unit_e5m2(nib, s3lo, s3hi, lut2);
-                uint8_t* out = static_cast<uint8_t*>(a.out) + g;
-                if (valid == 16u) {
-                    __stcs(reinterpret_cast<uint4*>(out), o);
-                } else {
-                    for (uint32_t k = 0; k < valid; ++k) {
-                        const uint32_t q = k >> 2;
-                        const uint32_t w = q == 0 ? o.x : q == 1 ? o.y : q == 2 ? o.z : o.w;
-                        out[k] = uint8_t(w >> (8u * (k & 3u)));
-                    }
-                }
-            }
-        }
-        __syncthreads();  // the chunk's dense writes are visible to the whole CTA
-
-        // ---- correction: escape records of this chunk ----
+        // index entry of this chunk, fetched early so its latency overlaps the dense work
         const uint64_t off = offsets[c];
         const uint64_t cnt = counts[c];
         const uint64_t expect_off = c == 0 ? 0 : offsets[c - 1] + counts[c - 1];
+        for (uint32_t s0 = 0; s0 < len; s0 += sub, ++it) {
+            const uint32_t stage = it % kStages, use = it / kStages;
+            const uint32_t n_sub = min(sub, len - s0);
+            if (!mbar_wait(&full_bar[stage], use & 1u)) report(a.status, SPLITZIP_ERR_TIMEOUT);
+            const SubTile t = subtile_windows<DT>(nibbles, signmant, base + s0, n_sub);
+            const uint8_t* src = stages + stage * kStageBytes;
+            decode_subtile<DT>(src + t.nib.offset, src + kNibCap + t.sm.offset, a.out, base + s0, n_sub, tid, lut2);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty_bar[stage]);
+        }
+        named_barrier(1, kConsumers);  // the chunk's dense writes are visible to all consumers
+
+        // ---- correction: escape records of this chunk ----
         const bool index_ok = off == expect_off && cnt <= len && off <= E && cnt <= E - off &&
                               (c + 1 < C || off + cnt == E);
         if (!index_ok) {
             if (tid == 0) report(a.status, SPLITZIP_ERR_CORRUPT);
             continue;
         }
-        for (uint64_t i = tid; i < cnt; i += kDecodeThreads) {
+        for (uint64_t i = tid; i < cnt; i += kConsumers) {
             const uint32_t pos = esc_pos[off + i];
             const uint32_t ex = esc_exp[off + i];
             const bool ascending = i == 0 || esc_pos[off + i - 1] < pos;
@@ -242,18 +308,18 @@ __global__ void __launch_bounds__(kDecodeThreads) decode_kernel(const DecodeArgs
 
 cudaError_t launch_decode(const DecodeArgs& a, int grid, cudaStream_t s) {
     if (a.dtype == SPLITZIP_BF16)
-        decode_kernel<SPLITZIP_BF16><<<grid, kDecodeThreads, 0, s>>>(a);
+        decode_kernel<SPLITZIP_BF16><<<grid, kBlock, kDecodeSmem, s>>>(a);
     else
-        decode_kernel<SPLITZIP_FP8_E5M2><<<grid, kDecodeThreads, 0, s>>>(a);
+        decode_kernel<SPLITZIP_FP8_E5M2><<<grid, kBlock, kDecodeSmem, s>>>(a);
     return cudaGetLastError();
 }
 
+// Also raises the kernels' dynamic shared-memory limit (once per device).
 cudaError_t occupancy_decode(int* blocks_per_sm, int dtype) {
-    if (dtype == SPLITZIP_BF16)
-        return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, decode_kernel<SPLITZIP_BF16>,
-                                                             kDecodeThreads, 0);
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, decode_kernel<SPLITZIP_FP8_E5M2>,
-                                                         kDecodeThreads, 0);
+    auto k = dtype == SPLITZIP_BF16 ? decode_kernel<SPLITZIP_BF16> : decode_kernel<SPLITZIP_FP8_E5M2>;
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kDecodeSmem));
+    if (e != cudaSuccess) return e;
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, k, kBlock, kDecodeSmem);
 }
 
 }  // namespace splitzip

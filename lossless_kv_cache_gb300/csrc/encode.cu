@@ -18,6 +18,8 @@
 // The escape order inside a chunk is ascending position because tiles are
 // chunk-aligned, tiles of a chunk are laid out in order, and inside a tile the
 // block scan orders records by element index.
+#include <type_traits>
+
 #include "splitzip_internal.cuh"
 
 namespace splitzip {
@@ -162,154 +164,164 @@ encode_streams_kernel(const EncodeArgs a, const EncodeLut lut_in) {
     for (uint64_t tile = blockIdx.x; tile < a.n_tiles; tile += gridDim.x, parity ^= 1) {
         const uint64_t base = tile * a.tile_elems;  // first element of the tile
         const uint64_t rem = a.n - base;
-        const uint32_t len = rem < a.tile_elems ? uint32_t(rem) : a.tile_elems;
+        const uint32_t len_rt = rem < a.tile_elems ? uint32_t(rem) : a.tile_elems;
         const uint32_t pos0 = uint32_t(base & (a.chunk_elems - 1u));  // in-chunk position of element 0
+        // Full 8192-element tiles (all but the last one) take a copy of the
+        // body in which every bounds test folds away at compile time.
+        auto body = [&](auto full_tag) {
+            constexpr bool FULL = decltype(full_tag)::value;
+            const uint32_t len = FULL ? kTileElems : len_rt;
 
-        uint4 v[J];
+            uint4 v[J];
 #pragma unroll
-        for (int j = 0; j < J; ++j) {
-            const uint32_t e = (uint32_t(j) * kEncodeThreads + tid) * G::kUnitElems;
-            const uint8_t* p = in + (base + e) * G::kElemBytes;
-            if (e + G::kUnitElems <= len)
-                v[j] = __ldcs(reinterpret_cast<const uint4*>(p));
-            else if (e < len)
-                v[j] = load_partial(p, int(len - e) * G::kElemBytes);
-            else
-                v[j] = make_uint4(0u, 0u, 0u, 0u);
-        }
+            for (int j = 0; j < J; ++j) {
+                const uint32_t e = (uint32_t(j) * kEncodeThreads + tid) * G::kUnitElems;
+                const uint8_t* p = in + (base + e) * G::kElemBytes;
+                if (e + G::kUnitElems <= len)
+                    v[j] = __ldcs(reinterpret_cast<const uint4*>(p));
+                else if (e < len)
+                    v[j] = load_partial(p, int(len - e) * G::kElemBytes);
+                else
+                    v[j] = make_uint4(0u, 0u, 0u, 0u);
+            }
 
-        uint32_t esc[J];
-        uint32_t ex[J][4];  // exponents of each unit (BF16 uses [0..1])
+            uint32_t esc[J];
+            uint32_t ex[J][4];  // exponents of each unit (BF16 uses [0..1])
 #pragma unroll
-        for (int j = 0; j < J; ++j) ex[j][2] = ex[j][3] = 0u;
-        PackedCounts<J> cnt;
+            for (int j = 0; j < J; ++j) ex[j][2] = ex[j][3] = 0u;
+            PackedCounts<J> cnt;
 #pragma unroll
-        for (int k = 0; k < kWords; ++k) cnt.w[k] = 0;
+            for (int k = 0; k < kWords; ++k) cnt.w[k] = 0;
 
 #pragma unroll
-        for (int j = 0; j < J; ++j) {
-            const uint32_t e = (uint32_t(j) * kEncodeThreads + tid) * G::kUnitElems;
-            const uint32_t valid = e < len ? min(len - e, uint32_t(G::kUnitElems)) : 0u;
-            if constexpr (DT == SPLITZIP_BF16) {
-                uint32_t nib;
-                uint2 sm;
-                encode_unit_bf16(v[j], lut, nib, sm, esc[j], ex[j][0], ex[j][1]);
-                uint8_t* nb = a.nibbles + (base + e) / 2;
-                uint8_t* sb = a.signmant + (base + e);
-                if (valid == 8u) {
-                    __stcs(reinterpret_cast<uint32_t*>(nb), nib);
-                    __stcs(reinterpret_cast<uint2*>(sb), sm);
-                } else if (valid > 0u) {
-                    esc[j] &= (1u << valid) - 1u;
-                    nib &= (1u << (4u * valid)) - 1u;
-                    for (uint32_t b = 0; b < (valid + 1u) / 2u; ++b) nb[b] = uint8_t(nib >> (8u * b));
-                    const uint64_t smw = uint64_t(sm.x) | (uint64_t(sm.y) << 32);
-                    for (uint32_t b = 0; b < valid; ++b) sb[b] = uint8_t(smw >> (8u * b));
-                } else {
-                    esc[j] = 0u;
-                }
-            } else {
-                uint2 nib;
-                uint32_t s3lo, s3hi;
-                encode_unit_e5m2(v[j], lut, nib, s3lo, s3hi, esc[j], ex[j]);
-                uint8_t* nb = a.nibbles + (base + e) / 2;
-                // s3 bytes of this unit start at 3 * (element index) / 8
-                uint8_t* sb = a.signmant + (base + e) / 8 * 3;
-                // fast path: the warp's 32 units are full and the tile is a
-                // multiple of 512 elements, so its 192 s3 bytes are 16-aligned
-                const uint32_t warp_e0 = (uint32_t(j) * kEncodeThreads + warp * 32u) * G::kUnitElems;
-                const bool warp_full = (a.tile_elems % 512u == 0u) && (warp_e0 + 512u <= len);
-                if (valid == 16u) {
-                    __stcs(reinterpret_cast<uint2*>(nb), nib);
-                } else if (valid > 0u) {
-                    esc[j] &= (1u << valid) - 1u;
-                    uint64_t nw = uint64_t(nib.x) | (uint64_t(nib.y) << 32);
-                    nw &= (uint64_t(1) << (4u * valid)) - 1u;
-                    for (uint32_t b = 0; b < (valid + 1u) / 2u; ++b) nb[b] = uint8_t(nw >> (8u * b));
-                } else {
-                    esc[j] = 0u;
-                }
-                if (warp_full) {  // warp-uniform
-                    uint16_t* st = reinterpret_cast<uint16_t*>(&s3_stage[warp][6 * lane]);
-                    st[0] = uint16_t(s3lo);
-                    st[1] = uint16_t(s3lo >> 16);
-                    st[2] = uint16_t(s3hi);
-                    __syncwarp();
-                    if (lane < 12) {
-                        const uint4 q = reinterpret_cast<const uint4*>(s3_stage[warp])[lane];
-                        uint8_t* dst = a.signmant + (base + warp_e0) / 8 * 3 + 16 * lane;
-                        __stcs(reinterpret_cast<uint4*>(dst), q);
-                    }
-                    __syncwarp();
-                } else if (valid > 0u) {
-                    // 3 bytes per started group of 8 elements (pad bits are 0)
-                    const uint32_t nbytes = 3u * ((valid + 7u) / 8u);
-                    uint16_t* d16 = reinterpret_cast<uint16_t*>(sb);  // 6*unit is even
-                    if (nbytes == 6u) {
-                        d16[0] = uint16_t(s3lo);
-                        d16[1] = uint16_t(s3lo >> 16);
-                        d16[2] = uint16_t(s3hi);
+            for (int j = 0; j < J; ++j) {
+                const uint32_t e = (uint32_t(j) * kEncodeThreads + tid) * G::kUnitElems;
+                const uint32_t valid = e < len ? min(len - e, uint32_t(G::kUnitElems)) : 0u;
+                if constexpr (DT == SPLITZIP_BF16) {
+                    uint32_t nib;
+                    uint2 sm;
+                    encode_unit_bf16(v[j], lut, nib, sm, esc[j], ex[j][0], ex[j][1]);
+                    uint8_t* nb = a.nibbles + (base + e) / 2;
+                    uint8_t* sb = a.signmant + (base + e);
+                    if (valid == 8u) {
+                        __stcs(reinterpret_cast<uint32_t*>(nb), nib);
+                        __stcs(reinterpret_cast<uint2*>(sb), sm);
+                    } else if (valid > 0u) {
+                        esc[j] &= (1u << valid) - 1u;
+                        nib &= (1u << (4u * valid)) - 1u;
+                        for (uint32_t b = 0; b < (valid + 1u) / 2u; ++b) nb[b] = uint8_t(nib >> (8u * b));
+                        const uint64_t smw = uint64_t(sm.x) | (uint64_t(sm.y) << 32);
+                        for (uint32_t b = 0; b < valid; ++b) sb[b] = uint8_t(smw >> (8u * b));
                     } else {
-                        d16[0] = uint16_t(s3lo);
-                        sb[2] = uint8_t(s3lo >> 16);
+                        esc[j] = 0u;
+                    }
+                } else {
+                    uint2 nib;
+                    uint32_t s3lo, s3hi;
+                    encode_unit_e5m2(v[j], lut, nib, s3lo, s3hi, esc[j], ex[j]);
+                    uint8_t* nb = a.nibbles + (base + e) / 2;
+                    // s3 bytes of this unit start at 3 * (element index) / 8
+                    uint8_t* sb = a.signmant + (base + e) / 8 * 3;
+                    // fast path: the warp's 32 units are full and the tile is a
+                    // multiple of 512 elements, so its 192 s3 bytes are 16-aligned
+                    const uint32_t warp_e0 = (uint32_t(j) * kEncodeThreads + warp * 32u) * G::kUnitElems;
+                    const bool warp_full = (FULL || a.tile_elems % 512u == 0u) && (warp_e0 + 512u <= len);
+                    if (valid == 16u) {
+                        __stcs(reinterpret_cast<uint2*>(nb), nib);
+                    } else if (valid > 0u) {
+                        esc[j] &= (1u << valid) - 1u;
+                        uint64_t nw = uint64_t(nib.x) | (uint64_t(nib.y) << 32);
+                        nw &= (uint64_t(1) << (4u * valid)) - 1u;
+                        for (uint32_t b = 0; b < (valid + 1u) / 2u; ++b) nb[b] = uint8_t(nw >> (8u * b));
+                    } else {
+                        esc[j] = 0u;
+                    }
+                    if (warp_full) {  // warp-uniform
+                        uint16_t* st = reinterpret_cast<uint16_t*>(&s3_stage[warp][6 * lane]);
+                        st[0] = uint16_t(s3lo);
+                        st[1] = uint16_t(s3lo >> 16);
+                        st[2] = uint16_t(s3hi);
+                        __syncwarp();
+                        if (lane < 12) {
+                            const uint4 q = reinterpret_cast<const uint4*>(s3_stage[warp])[lane];
+                            uint8_t* dst = a.signmant + (base + warp_e0) / 8 * 3 + 16 * lane;
+                            __stcs(reinterpret_cast<uint4*>(dst), q);
+                        }
+                        __syncwarp();
+                    } else if (valid > 0u) {
+                        // 3 bytes per started group of 8 elements (pad bits are 0)
+                        const uint32_t nbytes = 3u * ((valid + 7u) / 8u);
+                        uint16_t* d16 = reinterpret_cast<uint16_t*>(sb);  // 6*unit is even
+                        if (nbytes == 6u) {
+                            d16[0] = uint16_t(s3lo);
+                            d16[1] = uint16_t(s3lo >> 16);
+                            d16[2] = uint16_t(s3hi);
+                        } else {
+                            d16[0] = uint16_t(s3lo);
+                            sb[2] = uint8_t(s3lo >> 16);
+                        }
                     }
                 }
+                const uint32_t c = __popc(esc[j]);
+                cnt.w[j >> 1] |= c << (16 * (j & 1));
             }
-            const uint32_t c = __popc(esc[j]);
-            cnt.w[j >> 1] |= c << (16 * (j & 1));
-        }
 
-        // ---- block-wide exclusive scan of the per-thread escape counts, in
-        // element order (unit group j major, then thread) ----
-        uint32_t incl[kWords];
+            // ---- block-wide exclusive scan of the per-thread escape counts, in
+            // element order (unit group j major, then thread) ----
+            uint32_t incl[kWords];
 #pragma unroll
-        for (int k = 0; k < kWords; ++k) incl[k] = cnt.w[k];
+            for (int k = 0; k < kWords; ++k) incl[k] = cnt.w[k];
 #pragma unroll
-        for (int d = 1; d < 32; d <<= 1) {
+            for (int d = 1; d < 32; d <<= 1) {
 #pragma unroll
-            for (int k = 0; k < kWords; ++k) {
-                const uint32_t y = __shfl_up_sync(kFull, incl[k], d);
-                if (lane >= d) incl[k] += y;
+                for (int k = 0; k < kWords; ++k) {
+                    const uint32_t y = __shfl_up_sync(kFull, incl[k], d);
+                    if (lane >= d) incl[k] += y;
+                }
             }
-        }
-        if (lane == 31) {
+            if (lane == 31) {
 #pragma unroll
-            for (int k = 0; k < kWords; ++k) warp_sums[parity][warp][k] = incl[k];
-        }
-        __syncthreads();
-        uint32_t before[kWords], total[kWords];
-#pragma unroll
-        for (int k = 0; k < kWords; ++k) before[k] = total[k] = 0u;
-#pragma unroll
-        for (int w = 0; w < kWarps; ++w) {
-#pragma unroll
-            for (int k = 0; k < kWords; ++k) {
-                const uint32_t s = warp_sums[parity][w][k];
-                if (w < warp) before[k] += s;
-                total[k] += s;
+                for (int k = 0; k < kWords; ++k) warp_sums[parity][warp][k] = incl[k];
             }
-        }
+            __syncthreads();
+            uint32_t before[kWords], total[kWords];
+#pragma unroll
+            for (int k = 0; k < kWords; ++k) before[k] = total[k] = 0u;
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w) {
+#pragma unroll
+                for (int k = 0; k < kWords; ++k) {
+                    const uint32_t s = warp_sums[parity][w][k];
+                    if (w < warp) before[k] += s;
+                    total[k] += s;
+                }
+            }
 
-        uint32_t group_base = 0;  // escapes of the tile in unit groups < j
-        uint32_t* slot = a.staging + tile * a.tile_elems;
+            uint32_t group_base = 0;  // escapes of the tile in unit groups < j
+            uint32_t* slot = a.staging + tile * a.tile_elems;
 #pragma unroll
-        for (int j = 0; j < J; ++j) {
-            const int k = j >> 1, sh = 16 * (j & 1);
-            const uint32_t excl = ((before[k] + incl[k] - cnt.w[k]) >> sh) & 0xFFFFu;
-            uint32_t idx = group_base + excl;
-            uint32_t m = esc[j];
-            const uint32_t upos = pos0 + (uint32_t(j) * kEncodeThreads + tid) * G::kUnitElems;
-            while (m) {
-                const uint32_t b = __ffs(m) - 1;
-                m &= m - 1;
-                const uint32_t q = b >> 2;  // which exponent word (select, no local memory)
-                const uint32_t ew = q == 0 ? ex[j][0] : q == 1 ? ex[j][1] : q == 2 ? ex[j][2] : ex[j][3];
-                const uint32_t exponent = (ew >> (8u * (b & 3u))) & 0xFFu;
-                slot[idx++] = ((upos + b) << 8) | exponent;
+            for (int j = 0; j < J; ++j) {
+                const int k = j >> 1, sh = 16 * (j & 1);
+                const uint32_t excl = ((before[k] + incl[k] - cnt.w[k]) >> sh) & 0xFFFFu;
+                uint32_t idx = group_base + excl;
+                uint32_t m = esc[j];
+                const uint32_t upos = pos0 + (uint32_t(j) * kEncodeThreads + tid) * G::kUnitElems;
+                while (m) {
+                    const uint32_t b = __ffs(m) - 1;
+                    m &= m - 1;
+                    const uint32_t q = b >> 2;  // which exponent word (select, no local memory)
+                    const uint32_t ew = q == 0 ? ex[j][0] : q == 1 ? ex[j][1] : q == 2 ? ex[j][2] : ex[j][3];
+                    const uint32_t exponent = (ew >> (8u * (b & 3u))) & 0xFFu;
+                    slot[idx++] = ((upos + b) << 8) | exponent;
+                }
+                group_base += (total[k] >> sh) & 0xFFFFu;
             }
-            group_base += (total[k] >> sh) & 0xFFFFu;
-        }
-        if (tid == 0) a.tile_counts[tile] = group_base;
+            if (tid == 0) a.tile_counts[tile] = group_base;
+        };
+        if (len_rt == kTileElems)
+            body(std::true_type{});
+        else
+            body(std::false_type{});
     }
 }
 
