@@ -266,17 +266,14 @@ def run_ours(args, world, rank, local):
     def step(ev=None):
         if ev is not None:
             ev[0].record(stream)
-        check(sz.splitzip_encode_streams(xp, n, sz.BF16, cb, CHUNK, op, cap, wp, ws, h), "encode_streams")
+        check(sz.splitzip_encode(xp, n, sz.BF16, cb, CHUNK, op, cap, wp, ws, bufs.size.data_ptr(),
+                                 bufs.status.data_ptr(), h), "encode")
         if ev is not None:
             ev[1].record(stream)
-        check(sz.splitzip_encode_escapes(n, sz.BF16, CHUNK, op, cap, wp, ws, bufs.size.data_ptr(),
-                                         bufs.status.data_ptr(), h), "encode_escapes")
+        # decode bound: the buffer; the header carries the container's real size
+        check(sz.splitzip_decode(op, cap, out.data_ptr(), n, sz.BF16, dstatus.data_ptr(), h), "decode")
         if ev is not None:
             ev[2].record(stream)
-        size_now = bufs.capacity  # decode bound: the buffer; the header carries the real size
-        check(sz.splitzip_decode(op, size_now, out.data_ptr(), n, sz.BF16, dstatus.data_ptr(), h), "decode")
-        if ev is not None:
-            ev[3].record(stream)
 
     for _ in range(max(args.warmup, 1)):
         step()
@@ -288,7 +285,7 @@ def run_ours(args, world, rank, local):
 
     # ---- timed region: K steps, events around every kernel launch group ----
     K = args.steps
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
     clocks = ClockSampler(local)
     clocks.start()
     barrier(world)
@@ -300,24 +297,25 @@ def run_ours(args, world, rank, local):
     t_wall1 = time.time()
     barrier(world)
     clk = clocks.stop(t_wall0, t_wall1)
-    total_ms = evs[0][0].elapsed_time(evs[-1][3])
+    total_ms = evs[0][0].elapsed_time(evs[-1][2])
     total_ms = max_over_ranks(total_ms, world, device)
-    dense_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
-    esc_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
-    dec_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in evs)
-    enc_ms = dense_ms + esc_ms
+    enc_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
+    dec_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
     ms_per_step = total_ms / K
     all_bytes = sum_over_ranks(raw_bytes * K, world, device)
     value = all_bytes / (total_ms * 1e-3) / 1e9
 
     # ---- roofline of the dominant kernel (algorithmic bytes / event time) ----
+    # encode: read BF16, write nibbles + sign|mantissa + 3 B per escape + index
+    # decode: the same bytes in the other direction.  Each call is one kernel
+    # (plus one or two 4-byte/workspace memsets, inside the events).
     peaks, peak_kind = measured_peaks()
     hbm = float(peaks["hbm_gbs"])
     C = n // CHUNK
-    alg_dense = 2 * n + n // 2 + n                 # read BF16, write nibbles + sign|mantissa
-    alg_decode = n // 2 + n + 3 * E + 12 * C + 2 * n  # read streams + escapes + index, write BF16
-    if dense_ms >= dec_ms:
-        name, alg, ms = "encode_streams_kernel<bf16>", alg_dense, dense_ms
+    alg_encode = 2 * n + n // 2 + n + 3 * E + 12 * C
+    alg_decode = n // 2 + n + 3 * E + 12 * C + 2 * n
+    if enc_ms >= dec_ms:
+        name, alg, ms = "encode_kernel<bf16>", alg_encode, enc_ms
     else:
         name, alg, ms = "decode_kernel<bf16>", alg_decode, dec_ms
     achieved = alg / (ms * 1e-3) / 1e9
@@ -325,16 +323,13 @@ def run_ours(args, world, rank, local):
                 "frac": round(achieved / hbm, 4), "peak_source": "%s hbm_gbs (copy)" % peak_kind,
                 "algorithmic_bytes_per_launch": alg, "traffic": None}
     per_kernel = {
-        "encode_streams": {"ms": round(dense_ms, 4), "alg_bytes": alg_dense,
-                           "gbs": round(alg_dense / (dense_ms * 1e-3) / 1e9, 1)},
-        "encode_escapes": {"ms": round(esc_ms, 4), "alg_bytes": 3 * E + 12 * C,
-                           "gbs": round((3 * E + 12 * C) / (esc_ms * 1e-3) / 1e9, 1)},
+        "encode": {"ms": round(enc_ms, 4), "alg_bytes": alg_encode,
+                   "gbs": round(alg_encode / (enc_ms * 1e-3) / 1e9, 1)},
         "decode": {"ms": round(dec_ms, 4), "alg_bytes": alg_decode,
                    "gbs": round(alg_decode / (dec_ms * 1e-3) / 1e9, 1)},
     }
     enc_gbs = raw_bytes / (enc_ms * 1e-3) / 1e9
     dec_gbs = raw_bytes / (dec_ms * 1e-3) / 1e9
-    enc_alg = alg_dense + 3 * E + 12 * C
     link = {}
     for L in LINKS_GBS:
         t_plain = raw_bytes / (L * 1e9)
@@ -393,13 +388,13 @@ def run_ours(args, world, rank, local):
         "data": "synthetic (seeded torch CUDA generator; recipe of the workload module)",
         "config": config_dict(world, args.layers),
         "encode_gbs": round(enc_gbs, 2), "decode_gbs": round(dec_gbs, 2),
-        "encode_hbm_frac": round(enc_alg / (enc_ms * 1e-3) / 1e9 / hbm, 4),
+        "encode_hbm_frac": round(alg_encode / (enc_ms * 1e-3) / 1e9 / hbm, 4),
         "decode_hbm_frac": round(alg_decode / (dec_ms * 1e-3) / 1e9 / hbm, 4),
         "ratio": round(raw_bytes / blob_size, 5), "compressed_bytes": blob_size, "escapes": E,
         "escape_rate": round(esc_rate, 6), "verified_bit_exact": verified,
         "per_kernel": per_kernel, "link_model": link,
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clk,
-        "gpu_launches": 4 * K,
+        "gpu_launches": 2 * K,
     }
 
 

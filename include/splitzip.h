@@ -49,11 +49,12 @@
  *           (sign << 7) | mantissa7; FP8-E5M2 3 bits per element,
  *           (sign << 2) | mantissa2, LSB-first bitstream, element i at bits
  *           [3i, 3i+3), padded with zero bits to 3*ceil(n/8) bytes
- *   A16     esc_pos u16[E]: in-chunk positions, chunk by chunk, ascending
- *   A16     esc_exp u8[E]: the original exponents, same order (E5M2: the
- *           5-bit exponent zero-extended); the container ends here.
- * Size = A16(64 + 12C) + A16(ceil(n/2)) + A16(S) + A16(2E) + E, A16 = round
- * up to 16, S = n (BF16) or 3*ceil(n/8) (FP8-E5M2).
+ *   A16     escape records, 3 bytes each: the in-chunk position (u16,
+ *           little-endian) then the original exponent (u8; E5M2: the 5-bit
+ *           exponent zero-extended); chunk by chunk, ascending position
+ *           within a chunk; the container ends after the last record.
+ * Size = A16(64 + 12C) + A16(ceil(n/2)) + A16(S) + 3E, A16 = round up to 16,
+ * S = n (BF16) or 3*ceil(n/8) (FP8-E5M2).
  * chunk_elems is a power of two in [64, 65536] (the 16-bit position field of
  * the escape records bounds it; the page uses 65,536-element chunks).
  */
@@ -78,7 +79,7 @@ typedef enum {
     SPLITZIP_ERR_CAPACITY = 2,    /* output or workspace smaller than required */
     SPLITZIP_ERR_CORRUPT = 3,     /* container inconsistent (header, index, escapes, size) */
     SPLITZIP_ERR_CUDA = 4,        /* a CUDA runtime call or launch failed */
-    SPLITZIP_ERR_TIMEOUT = 5,     /* reserved: a bounded device wait gave up */
+    SPLITZIP_ERR_TIMEOUT = 5,     /* a bounded device wait gave up (never expected) */
     SPLITZIP_ERR_UNSUPPORTED = 6  /* no sm_103a device, or a size beyond the limits */
 } splitzip_status_t;
 
@@ -97,7 +98,7 @@ typedef struct {
     uint64_t n_elems;
     uint64_t total_escapes;
     uint64_t size;          /* total container bytes */
-    uint64_t index_off, counts_off, nibble_off, signmant_off, escpos_off, escexp_off;
+    uint64_t index_off, counts_off, nibble_off, signmant_off, escrec_off;
     uint32_t chunk_elems;
     uint32_t n_chunks;
     uint8_t dtype;
@@ -132,36 +133,28 @@ int splitzip_compressed_size(uint64_t n, int dtype, uint32_t chunk_elems, uint64
  * splitzip_encode requires of d_out. */
 int splitzip_max_compressed_size(uint64_t n, int dtype, uint32_t chunk_elems, uint64_t* out_bytes);
 
-/* Device scratch bytes splitzip_encode needs for n elements (about 4 bytes
- * per element: the per-tile escape staging area, plus per-tile counts). */
+/* Device scratch bytes splitzip_encode needs for n elements: about 4 bytes
+ * per element (each tile of 8,192 elements, or each chunk when chunks are
+ * smaller, has a staging slot big enough for all of its elements to escape)
+ * plus 4 bytes per tile and per 256 tiles. */
 int splitzip_encode_workspace_size(uint64_t n, int dtype, uint32_t chunk_elems, uint64_t* out_bytes);
 
-/* Encode n elements (Method, "Encoding strategy").
+/* Encode n elements (Method, "Encoding strategy").  Two kernels, no waits
+ * between blocks: a streaming pass that writes the nibble and sign|mantissa
+ * streams and stages each tile's escape records in element order, then a
+ * pass that computes the index (per-chunk offsets and counts) and moves the
+ * records into the escape stream.
  * d_in: n elements; cb: host codebook of the same dtype; d_out: container,
  * out_capacity >= splitzip_max_compressed_size; d_ws: ws_bytes >=
- * splitzip_encode_workspace_size, contents need not be initialised;
- * d_out_size: device u64 that receives the container size; d_status: device
- * int set to SPLITZIP_OK when the container is complete.  n = 0 is valid and
- * gives a 64-byte container.  Equivalent to splitzip_encode_streams followed
- * by splitzip_encode_escapes on the same stream. */
+ * splitzip_encode_workspace_size, contents need not be initialised (the call
+ * clears what must start at zero); d_out_size: device u64 that receives the
+ * container size; d_status: device int, cleared by the call; it becomes
+ * SPLITZIP_ERR_TIMEOUT only if a bounded wait on a bulk copy ran out (not
+ * expected).  n = 0 is valid and gives a 64-byte container.  Calls that share
+ * d_ws must not overlap on the GPU. */
 int splitzip_encode(const void* d_in, uint64_t n, int dtype, const splitzip_codebook_t* cb,
                     uint32_t chunk_elems, void* d_out, uint64_t out_capacity, void* d_ws,
                     uint64_t ws_bytes, uint64_t* d_out_size, int* d_status, cudaStream_t stream);
-
-/* First encode stage: writes the header (without E), the nibble and the
- * sign|mantissa streams, and stages each tile's escapes and count in d_ws.
- * After it completes on `stream` the two dense streams are final, so a caller
- * can start moving them while the second stage runs. */
-int splitzip_encode_streams(const void* d_in, uint64_t n, int dtype, const splitzip_codebook_t* cb,
-                            uint32_t chunk_elems, void* d_out, uint64_t out_capacity, void* d_ws,
-                            uint64_t ws_bytes, cudaStream_t stream);
-
-/* Second encode stage: per-chunk counts and prefix offsets, E, the escape
- * stream in ascending position order, all padding, *d_out_size and
- * *d_status.  Arguments must match the preceding splitzip_encode_streams. */
-int splitzip_encode_escapes(uint64_t n, int dtype, uint32_t chunk_elems, void* d_out,
-                            uint64_t out_capacity, void* d_ws, uint64_t ws_bytes,
-                            uint64_t* d_out_size, int* d_status, cudaStream_t stream);
 
 /* Size of the device array that splitzip_encode_noalloc uses as scratch. */
 #define SPLITZIP_NOALLOC_SCRATCH_BYTES (32ull << 20)
@@ -182,8 +175,9 @@ int splitzip_encode_escapes(uint64_t n, int dtype, uint32_t chunk_elems, void* d
  * the array's device address (cudaGetSymbolAddress) with that device current;
  * make that first call before any stream capture.  Every call on a device
  * shares the array, so calls whose GPU work overlaps (other streams or host
- * threads) race and must be serialised by the caller; no clearing between
- * calls is needed, the encoder writes every scratch byte it reads. */
+ * threads) race and must be serialised by the caller.  Each call clears the
+ * part of the array that must start at zero, on its own stream, before its
+ * kernel runs. */
 int splitzip_encode_noalloc(const void* d_in, uint64_t n, int dtype, const splitzip_codebook_t* cb,
                             uint32_t chunk_elems, void* d_out, uint64_t out_capacity,
                             uint64_t* d_out_size, int* d_status, cudaStream_t stream);

@@ -57,8 +57,7 @@ class Header(ctypes.Structure):
         ("counts_off", ctypes.c_uint64),
         ("nibble_off", ctypes.c_uint64),
         ("signmant_off", ctypes.c_uint64),
-        ("escpos_off", ctypes.c_uint64),
-        ("escexp_off", ctypes.c_uint64),
+        ("escrec_off", ctypes.c_uint64),
         ("chunk_elems", ctypes.c_uint32),
         ("n_chunks", ctypes.c_uint32),
         ("dtype", ctypes.c_uint8),
@@ -79,9 +78,6 @@ SIGNATURES = {
     "splitzip_encode_workspace_size": (_int, [_u64, _int, _u32, _P_u64]),
     "splitzip_encode": (_int, [_vp, _u64, _int, ctypes.POINTER(Codebook), _u32, _vp, _u64, _vp, _u64, _vp,
                                _vp, _vp]),
-    "splitzip_encode_streams": (_int, [_vp, _u64, _int, ctypes.POINTER(Codebook), _u32, _vp, _u64, _vp,
-                                       _u64, _vp]),
-    "splitzip_encode_escapes": (_int, [_u64, _int, _u32, _vp, _u64, _vp, _u64, _vp, _vp, _vp]),
     "splitzip_encode_noalloc": (_int, [_vp, _u64, _int, ctypes.POINTER(Codebook), _u32, _vp, _u64, _vp, _vp,
                                        _vp]),
     "splitzip_decode": (_int, [_vp, _u64, _vp, _u64, _int, _vp, _vp]),
@@ -137,17 +133,6 @@ def splitzip_encode(d_in, n, dtype, cb, chunk_elems, d_out, out_capacity, d_ws, 
                     d_status, stream):
     return lib().splitzip_encode(d_in, n, dtype, ctypes.byref(cb), chunk_elems, d_out, out_capacity, d_ws,
                                  ws_bytes, d_out_size, d_status, stream)
-
-
-def splitzip_encode_streams(d_in, n, dtype, cb, chunk_elems, d_out, out_capacity, d_ws, ws_bytes, stream):
-    return lib().splitzip_encode_streams(d_in, n, dtype, ctypes.byref(cb), chunk_elems, d_out, out_capacity,
-                                         d_ws, ws_bytes, stream)
-
-
-def splitzip_encode_escapes(n, dtype, chunk_elems, d_out, out_capacity, d_ws, ws_bytes, d_out_size, d_status,
-                            stream):
-    return lib().splitzip_encode_escapes(n, dtype, chunk_elems, d_out, out_capacity, d_ws, ws_bytes,
-                                         d_out_size, d_status, stream)
 
 
 def splitzip_encode_noalloc(d_in, n, dtype, cb, chunk_elems, d_out, out_capacity, d_out_size, d_status, stream):

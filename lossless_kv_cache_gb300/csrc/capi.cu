@@ -18,7 +18,7 @@ struct DeviceState {
     bool ready;
     int status;
     int sms;
-    int encode_bpsm[2], decode_bpsm[2], hist_bpsm[2], gather_bpsm;
+    int encode_bpsm[2], decode_bpsm[2], hist_bpsm[2];
 };
 
 std::mutex g_mutex;
@@ -51,10 +51,6 @@ int device_state(DeviceState* out) {
                     cudaGetLastError();
                     return SPLITZIP_ERR_CUDA;
                 }
-            }
-            if (occupancy_gather(&d.gather_bpsm) != cudaSuccess) {
-                cudaGetLastError();
-                return SPLITZIP_ERR_CUDA;
             }
         }
         d.ready = true;
@@ -90,40 +86,38 @@ int grid_for(uint64_t work_items, int sms, int blocks_per_sm) {
     return int(std::max<uint64_t>(1, std::min<uint64_t>(work_items, cap)));
 }
 
-// Shared checks of the two encode stages; fills the kernel arguments.
-int prepare_encode(const void* d_in, uint64_t n, int dtype, const splitzip_codebook_t* cb, bool need_input,
-                   uint32_t chunk, void* d_out, uint64_t out_capacity, void* d_ws, uint64_t ws_bytes,
-                   EncodeArgs* a) {
+// Argument checks of splitzip_encode; fills the kernel arguments.
+int prepare_encode(const void* d_in, uint64_t n, int dtype, const splitzip_codebook_t* cb, uint32_t chunk,
+                   void* d_out, uint64_t out_capacity, void* d_ws, uint64_t ws_bytes, uint64_t* d_out_size,
+                   int* d_status, EncodeArgs* a, Workspace* W) {
     int st = check_geometry(n, dtype, chunk);
     if (st != SPLITZIP_OK) return st;
-    if (need_input) {
-        if ((st = check_codebook(cb, dtype)) != SPLITZIP_OK) return st;
-        if (n > 0 && (!d_in || !aligned(d_in, 16))) return SPLITZIP_ERR_INVALID_ARG;
-    }
+    if ((st = check_codebook(cb, dtype)) != SPLITZIP_OK) return st;
+    if (n > 0 && (!d_in || !aligned(d_in, 16))) return SPLITZIP_ERR_INVALID_ARG;
     if (!d_out || !aligned(d_out, 16)) return SPLITZIP_ERR_INVALID_ARG;
-    const Layout worst = layout_for(n, dtype, chunk, n);
-    if (out_capacity < worst.size) return SPLITZIP_ERR_CAPACITY;
-    const Workspace W = workspace_for(n, chunk);
-    if (ws_bytes < W.bytes) return SPLITZIP_ERR_CAPACITY;
-    if (W.bytes > 0 && (!d_ws || !aligned(d_ws, 16))) return SPLITZIP_ERR_INVALID_ARG;
+    if (!d_out_size || !aligned(d_out_size, 8) || !d_status || !aligned(d_status, 4))
+        return SPLITZIP_ERR_INVALID_ARG;
+    if (out_capacity < layout_for(n, dtype, chunk, n).size) return SPLITZIP_ERR_CAPACITY;
+    *W = workspace_for(n, chunk);
+    if (ws_bytes < W->bytes) return SPLITZIP_ERR_CAPACITY;
+    if (W->bytes > 0 && (!d_ws || !aligned(d_ws, 16))) return SPLITZIP_ERR_INVALID_ARG;
 
-    const Layout L = layout_for(n, dtype, chunk, 0);
-    uint8_t* out = static_cast<uint8_t*>(d_out);
     uint8_t* ws = static_cast<uint8_t*>(d_ws);
     a->in = d_in;
     a->n = n;
-    a->out = out;
-    a->nibbles = out + L.nibble_off;
-    a->signmant = out + L.signmant_off;
-    a->tile_counts = reinterpret_cast<uint32_t*>(ws + W.counts_off);
-    a->staging = reinterpret_cast<uint32_t*>(ws + W.staging_off);
-    a->n_tiles = W.n_tiles;
-    a->tile_elems = W.tile_elems;
+    a->out = static_cast<uint8_t*>(d_out);
+    a->group_totals = reinterpret_cast<uint32_t*>(ws + W->group_off);
+    a->tile_counts = reinterpret_cast<uint32_t*>(ws + W->count_off);
+    a->staging = reinterpret_cast<uint32_t*>(ws + W->staging_off);
+    a->out_size = d_out_size;
+    a->error = d_status;
+    a->n_tiles = W->n_tiles;
+    a->n_groups = W->n_groups;
+    a->tile_elems = W->tile_elems;
     a->chunk_elems = chunk;
-    a->n_chunks = L.n_chunks;
+    a->n_chunks = layout_for(n, dtype, chunk, 0).n_chunks;
     a->dtype = dtype;
-    if (cb) std::memcpy(a->codebook, cb->exps, 16);
-    else std::memset(a->codebook, 0, 16);
+    std::memcpy(a->codebook, cb->exps, 16);
     return SPLITZIP_OK;
 }
 
@@ -210,47 +204,28 @@ int splitzip_exponent_histogram(const void* d_x, uint64_t n, int dtype, uint64_t
                : SPLITZIP_ERR_CUDA;
 }
 
-int splitzip_encode_streams(const void* d_in, uint64_t n, int dtype, const splitzip_codebook_t* cb,
-                            uint32_t chunk_elems, void* d_out, uint64_t out_capacity, void* d_ws,
-                            uint64_t ws_bytes, cudaStream_t stream) {
+int splitzip_encode(const void* d_in, uint64_t n, int dtype, const splitzip_codebook_t* cb, uint32_t chunk_elems,
+                    void* d_out, uint64_t out_capacity, void* d_ws, uint64_t ws_bytes, uint64_t* d_out_size,
+                    int* d_status, cudaStream_t stream) {
     EncodeArgs a;
-    int st = prepare_encode(d_in, n, dtype, cb, true, chunk_elems, d_out, out_capacity, d_ws, ws_bytes, &a);
+    Workspace W;
+    int st = prepare_encode(d_in, n, dtype, cb, chunk_elems, d_out, out_capacity, d_ws, ws_bytes, d_out_size,
+                            d_status, &a, &W);
     if (st != SPLITZIP_OK) return st;
     DeviceState d;
     if ((st = device_state(&d)) != SPLITZIP_OK) return st;
     EncodeLut lut;
     std::memset(lut.code, kEscapeFlag, sizeof(lut.code));
     for (int k = 0; k < 16; ++k) lut.code[cb->exps[k]] = uint8_t(k);
+    // the per-group escape totals are accumulated with atomic adds, and errors
+    // are recorded into the status word with compare-and-swap: both start at 0
+    if ((W.zero_bytes > 0 && cudaMemsetAsync(d_ws, 0, W.zero_bytes, stream) != cudaSuccess) ||
+        cudaMemsetAsync(d_status, 0, sizeof(int), stream) != cudaSuccess) {
+        cudaGetLastError();
+        return SPLITZIP_ERR_CUDA;
+    }
     const int grid = grid_for(a.n_tiles, d.sms, d.encode_bpsm[dtype]);
-    return launch_encode_streams(a, lut, grid, stream) == cudaSuccess ? SPLITZIP_OK : SPLITZIP_ERR_CUDA;
-}
-
-int splitzip_encode_escapes(uint64_t n, int dtype, uint32_t chunk_elems, void* d_out, uint64_t out_capacity,
-                            void* d_ws, uint64_t ws_bytes, uint64_t* d_out_size, int* d_status,
-                            cudaStream_t stream) {
-    if (!d_out_size || !aligned(d_out_size, 8) || !d_status || !aligned(d_status, 4))
-        return SPLITZIP_ERR_INVALID_ARG;
-    EncodeArgs a;
-    int st = prepare_encode(nullptr, n, dtype, nullptr, false, chunk_elems, d_out, out_capacity, d_ws, ws_bytes,
-                            &a);
-    if (st != SPLITZIP_OK) return st;
-    DeviceState d;
-    if ((st = device_state(&d)) != SPLITZIP_OK) return st;
-    const int warps_per_block = kGatherThreads / 32;
-    const int grid = grid_for((a.n_tiles + warps_per_block - 1) / warps_per_block, d.sms, d.gather_bpsm);
-    return launch_encode_escapes(a, d_out_size, d_status, grid, stream) == cudaSuccess ? SPLITZIP_OK
-                                                                                      : SPLITZIP_ERR_CUDA;
-}
-
-int splitzip_encode(const void* d_in, uint64_t n, int dtype, const splitzip_codebook_t* cb, uint32_t chunk_elems,
-                    void* d_out, uint64_t out_capacity, void* d_ws, uint64_t ws_bytes, uint64_t* d_out_size,
-                    int* d_status, cudaStream_t stream) {
-    if (!d_out_size || !aligned(d_out_size, 8) || !d_status || !aligned(d_status, 4))
-        return SPLITZIP_ERR_INVALID_ARG;
-    int st = splitzip_encode_streams(d_in, n, dtype, cb, chunk_elems, d_out, out_capacity, d_ws, ws_bytes, stream);
-    if (st != SPLITZIP_OK) return st;
-    return splitzip_encode_escapes(n, dtype, chunk_elems, d_out, out_capacity, d_ws, ws_bytes, d_out_size,
-                                   d_status, stream);
+    return launch_encode(a, lut, grid, stream) == cudaSuccess ? SPLITZIP_OK : SPLITZIP_ERR_CUDA;
 }
 
 int splitzip_decode(const void* d_in, uint64_t in_bytes, void* d_out, uint64_t n, int dtype, int* d_status,
@@ -313,8 +288,7 @@ int splitzip_parse_header(const void* h_blob, uint64_t bytes, splitzip_header_t*
     h.counts_off = L.counts_off;
     h.nibble_off = L.nibble_off;
     h.signmant_off = L.signmant_off;
-    h.escpos_off = L.escpos_off;
-    h.escexp_off = L.escexp_off;
+    h.escrec_off = L.escrec_off;
     *out = h;
     return SPLITZIP_OK;
 }

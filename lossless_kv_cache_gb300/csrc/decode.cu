@@ -250,14 +250,14 @@ __global__ void __launch_bounds__(kBlock) decode_kernel(const DecodeArgs a) {
                 bulk_load(dst + kNibCap, t.sm.src, t.sm.bytes, &full_bar[stage]);
             }
         }
+        if (!drain_stages(full_bar, kStages, it)) report(a.status, SPLITZIP_ERR_TIMEOUT);
         return;
     }
 
     // ---- consumers: dense decode per sub-tile, then the chunk's correction ----
     const uint64_t* offsets = reinterpret_cast<const uint64_t*>(in + L.index_off);
     const uint32_t* counts = reinterpret_cast<const uint32_t*>(in + L.counts_off);
-    const uint16_t* esc_pos = reinterpret_cast<const uint16_t*>(in + L.escpos_off);
-    const uint8_t* esc_exp = in + L.escexp_off;
+    const uint8_t* records = in + L.escrec_off;  // 3 bytes each: position u16 LE, exponent
     uint32_t it = 0;
     for (uint64_t c = blockIdx.x; c < C; c += gridDim.x) {
         const uint64_t base = c * chunk;
@@ -286,9 +286,10 @@ __global__ void __launch_bounds__(kBlock) decode_kernel(const DecodeArgs a) {
             continue;
         }
         for (uint64_t i = tid; i < cnt; i += kConsumers) {
-            const uint32_t pos = esc_pos[off + i];
-            const uint32_t ex = esc_exp[off + i];
-            const bool ascending = i == 0 || esc_pos[off + i - 1] < pos;
+            const uint8_t* r = records + 3 * (off + i);
+            const uint32_t pos = uint32_t(r[0]) | (uint32_t(r[1]) << 8);
+            const uint32_t ex = r[2];
+            const bool ascending = i == 0 || (uint32_t(r[-3]) | (uint32_t(r[-2]) << 8)) < pos;
             if (pos >= len || !ascending || ex >= (DT == SPLITZIP_BF16 ? 256u : 32u)) {
                 report(a.status, SPLITZIP_ERR_CORRUPT);
                 continue;

@@ -1,36 +1,45 @@
 // SplitZip encode kernels for sm_103a.
 //
 // Method: "SplitZip: Ultra Fast Lossless KV Compression for Disaggregated LLM
-// Serving", section "Method: SplitZip", "Encoding strategy".  Three kernels:
+// Serving", section "Method: SplitZip", "Encoding strategy": each element's
+// exponent goes through the offline-calibrated Top-16 codebook to a 4-bit code,
+// two codes per byte ("Fixed-length coding"); sign and mantissa are kept raw
+// ("Sign/mantissa preservation"); an exponent outside the codebook becomes a
+// (16-bit position, 8-bit exponent) escape record ("Escape stream").
 //
-//   encode_streams_kernel  the dense pass over the input (HBM-bound): per
-//       element split sign|mantissa from the exponent, map the exponent
-//       through the Top-16 table to a 4-bit code, pack two codes per byte,
-//       and detect escapes.  Each tile's escapes are ordered by a block scan
-//       and written to the tile's own staging slot in the workspace together
-//       with the tile's escape count.  No atomics, no inter-block waits.
-//   encode_index_kernel    one CTA: per-chunk counts (sum of the chunk's tile
-//       counts), their exclusive prefix (the container index), E, the size,
-//       the status word and all section padding.
-//   encode_gather_kernel   one warp per tile: copies the staged records of
-//       the tile to their final place in the position and exponent arrays.
-//
-// The escape order inside a chunk is ascending position because tiles are
-// chunk-aligned, tiles of a chunk are laid out in order, and inside a tile the
-// block scan orders records by element index.
+// Two kernels, no inter-block waits:
+//   encode_kernel (the streaming pass, persistent CTAs of 8 consumer warps +
+//     1 producer warp): the producer streams each of the CTA's tiles into a
+//     4-stage shared-memory ring with bulk copies (TMA, cp.async.bulk +
+//     mbarrier); consumers split, code and pack the tile from shared memory
+//     and write the nibble and sign|mantissa streams with coalesced stores; a
+//     block scan orders the tile's escapes by element index and writes them
+//     to the tile's staging slot; the tile's count goes to the workspace and,
+//     by an integer atomic add, to its group's total.
+//   encode_finish_kernel (one CTA per group of 256 tiles): the sum of the
+//     earlier groups' totals plus a block scan of the group's tile counts give
+//     every tile's first record index; the CTA writes the index entries of the
+//     group's chunks and moves the staged records to the escape stream; the
+//     last group writes E and the container size.
 #include <type_traits>
 
 #include "splitzip_internal.cuh"
+#include "tma_pipeline.cuh"
 
 namespace splitzip {
 namespace {
 
 constexpr uint32_t kFull = 0xFFFFFFFFu;
-constexpr int kWarps = kEncodeThreads / 32;
+constexpr int kConsumerWarps = 8;
+constexpr int kConsumers = kConsumerWarps * 32;
+constexpr int kBlock = kConsumers + 32;  // + one producer warp
+constexpr int kStages = 4;
+constexpr uint32_t kStageBytes = kTileElems * 2;  // one BF16 tile
+constexpr uint32_t kEncodeSmem = kStages * kStageBytes;
+constexpr int kFinishThreads = kGroupTiles;  // one thread per tile of the group
 
-// Units: BF16 8 elements (one 16-byte load), E5M2 16 elements.  Each thread
-// handles kUnitsPerThread units per tile, unit u = j * 256 + threadIdx.x, so
-// every warp-wide load covers 512 contiguous bytes.
+// Units: BF16 8 elements, E5M2 16 elements (16 bytes either way).  Thread t
+// handles units j * 256 + t of a tile, so each warp reads 512 contiguous bytes.
 template <int DT> struct Geometry;
 template <> struct Geometry<SPLITZIP_BF16> {
     static constexpr int kElemBytes = 2, kUnitElems = 8, kUnitsPerThread = 4;
@@ -38,8 +47,8 @@ template <> struct Geometry<SPLITZIP_BF16> {
 template <> struct Geometry<SPLITZIP_FP8_E5M2> {
     static constexpr int kElemBytes = 1, kUnitElems = 16, kUnitsPerThread = 2;
 };
-static_assert(kEncodeThreads * 8 * 4 == kTileElems, "BF16 tile");
-static_assert(kEncodeThreads * 16 * 2 == kTileElems, "E5M2 tile");
+static_assert(kConsumers * 8 * 4 == kTileElems, "BF16 tile");
+static_assert(kConsumers * 16 * 2 == kTileElems, "E5M2 tile");
 
 // Load `nbytes` (< 16) bytes into a zero-filled vector (only the final unit
 // of a tensor is partial).
@@ -118,7 +127,9 @@ __device__ __forceinline__ void encode_unit_e5m2(const uint4 v, const uint8_t* l
     s3hi = (g2 >> 8) | (g3 << 4);
 }
 
-__device__ __forceinline__ void write_header(const EncodeArgs& a) {
+// Header fields known before any tile is encoded (E is written at the end),
+// and the zero padding between sections, whose places depend only on n.
+__device__ void write_header_and_padding(const EncodeArgs& a) {
     uint8_t* h = a.out;
     uint32_t* h32 = reinterpret_cast<uint32_t*>(h);
     h32[0] = kMagic;
@@ -126,7 +137,6 @@ __device__ __forceinline__ void write_header(const EncodeArgs& a) {
     reinterpret_cast<uint64_t*>(h)[1] = a.n;
     h32[4] = a.chunk_elems;
     h32[5] = uint32_t(a.n_chunks);
-    // h[24..31] (E) is written by the index kernel
     uint32_t cb[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i)
@@ -134,40 +144,80 @@ __device__ __forceinline__ void write_header(const EncodeArgs& a) {
                 (uint32_t(a.codebook[4 * i + 2]) << 16) | (uint32_t(a.codebook[4 * i + 3]) << 24);
     reinterpret_cast<uint4*>(h)[2] = make_uint4(cb[0], cb[1], cb[2], cb[3]);
     reinterpret_cast<uint4*>(h)[3] = make_uint4(0u, 0u, 0u, 0u);
+    const Layout L = layout_for(a.n, a.dtype, a.chunk_elems, 0);
+    for (uint64_t i = L.index_end; i < L.nibble_off; ++i) h[i] = 0;
+    for (uint64_t i = L.nibble_off + (a.n + 1) / 2; i < L.signmant_off; ++i) h[i] = 0;
+    for (uint64_t i = L.signmant_off + signmant_bytes(a.dtype, a.n); i < L.escrec_off; ++i) h[i] = 0;
+    if (a.n_tiles == 0) {  // no tile will finish the header
+        reinterpret_cast<uint64_t*>(h)[3] = 0;
+        *a.out_size = L.size;
+    }
 }
 
-// Per-thread escape counts (<= 16 each) are scanned as 16-bit fields, two per
-// word; a tile holds at most 8192 escapes so no field overflows.
-template <int J>
-struct PackedCounts {
-    static constexpr int kWords = (J + 1) / 2;
-    uint32_t w[kWords];
-};
+__device__ __forceinline__ void report(int* status, int code) { atomicCAS(status, SPLITZIP_OK, code); }
 
 template <int DT>
-__global__ void __launch_bounds__(kEncodeThreads)
-encode_streams_kernel(const EncodeArgs a, const EncodeLut lut_in) {
+__global__ void __launch_bounds__(kBlock, 3) encode_kernel(const EncodeArgs a, const EncodeLut lut_in) {
     using G = Geometry<DT>;
     constexpr int J = G::kUnitsPerThread;
-    constexpr int kWords = PackedCounts<J>::kWords;
+    constexpr int kWords = (J + 1) / 2;  // per-thread counts as 16-bit fields, two per word
+    extern __shared__ __align__(128) uint8_t stages[];
+    __shared__ __align__(8) uint64_t full_bar[kStages];
+    __shared__ __align__(8) uint64_t empty_bar[kStages];
     __shared__ uint8_t lut[256];
-    __shared__ uint32_t warp_sums[2][kWarps][kWords];
-    __shared__ __align__(16) uint8_t s3_stage[kWarps][192];
+    __shared__ uint32_t warp_sums[2][kConsumerWarps][kWords];
+    __shared__ __align__(16) uint8_t s3_stage[kConsumerWarps][192];
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    for (int i = tid; i < 256; i += kEncodeThreads) lut[i] = lut_in.code[i];
-    if (blockIdx.x == 0 && tid == 0) write_header(a);
+    for (int i = tid; i < 256; i += kBlock) lut[i] = lut_in.code[i];
+    if (tid == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&full_bar[s], 1);
+            mbar_init(&empty_bar[s], kConsumerWarps);
+        }
+        mbar_init_fence();
+        if (blockIdx.x == 0) write_header_and_padding(a);
+    }
     __syncthreads();
 
     const uint8_t* in = static_cast<const uint8_t*>(a.in);
-    int parity = 0;
-    for (uint64_t tile = blockIdx.x; tile < a.n_tiles; tile += gridDim.x, parity ^= 1) {
-        const uint64_t base = tile * a.tile_elems;  // first element of the tile
+    if (warp == kConsumerWarps) {
+        // ---- producer: stream the CTA's tiles (blockIdx.x + k * gridDim.x) ----
+        if (lane != 0) return;
+        uint32_t it = 0;
+        for (uint64_t t = blockIdx.x; t < a.n_tiles; t += gridDim.x, ++it) {
+            const uint32_t stage = it % kStages, use = it / kStages;
+            if (use > 0 && !mbar_wait(&empty_bar[stage], (use - 1) & 1u)) report(a.error, SPLITZIP_ERR_TIMEOUT);
+            const uint64_t base = t * a.tile_elems;
+            const uint64_t len = min(uint64_t(a.tile_elems), a.n - base);
+            // whole 16-byte units only: the input has no padding after element n-1
+            const uint32_t bytes = uint32_t(len * G::kElemBytes) & ~15u;
+            mbar_arrive_expect_tx(&full_bar[stage], bytes);
+            if (bytes) bulk_load(stages + stage * kStageBytes, in + base * G::kElemBytes, bytes, &full_bar[stage]);
+        }
+        if (!drain_stages(full_bar, kStages, it)) report(a.error, SPLITZIP_ERR_TIMEOUT);
+        return;
+    }
+
+    // ---- consumers ----
+    const Layout L0 = layout_for(a.n, a.dtype, a.chunk_elems, 0);
+    uint8_t* nibbles = a.out + L0.nibble_off;
+    uint8_t* signmant = a.out + L0.signmant_off;
+
+    uint32_t it = 0;
+    for (uint64_t tile = blockIdx.x; tile < a.n_tiles; tile += gridDim.x, ++it) {
+        const uint32_t stage = it % kStages, use = it / kStages, parity = it & 1u;
+        // on a time-out the tile is processed anyway (its addresses do not
+        // depend on the data), so every consumer still meets every barrier
+        if (!mbar_wait(&full_bar[stage], use & 1u)) report(a.error, SPLITZIP_ERR_TIMEOUT);
+        const uint64_t base = tile * a.tile_elems;
         const uint64_t rem = a.n - base;
         const uint32_t len_rt = rem < a.tile_elems ? uint32_t(rem) : a.tile_elems;
         const uint32_t pos0 = uint32_t(base & (a.chunk_elems - 1u));  // in-chunk position of element 0
-        // Full 8192-element tiles (all but the last one) take a copy of the
-        // body in which every bounds test folds away at compile time.
+        const uint8_t* tile_smem = stages + stage * kStageBytes;
+
+        // Full 8192-element tiles take a copy of the body in which every
+        // bounds test folds away at compile time.
         auto body = [&](auto full_tag) {
             constexpr bool FULL = decltype(full_tag)::value;
             const uint32_t len = FULL ? kTileElems : len_rt;
@@ -175,34 +225,35 @@ encode_streams_kernel(const EncodeArgs a, const EncodeLut lut_in) {
             uint4 v[J];
 #pragma unroll
             for (int j = 0; j < J; ++j) {
-                const uint32_t e = (uint32_t(j) * kEncodeThreads + tid) * G::kUnitElems;
-                const uint8_t* p = in + (base + e) * G::kElemBytes;
+                const uint32_t e = (uint32_t(j) * kConsumers + tid) * G::kUnitElems;
                 if (e + G::kUnitElems <= len)
-                    v[j] = __ldcs(reinterpret_cast<const uint4*>(p));
-                else if (e < len)
-                    v[j] = load_partial(p, int(len - e) * G::kElemBytes);
+                    v[j] = *reinterpret_cast<const uint4*>(tile_smem + e * G::kElemBytes);
+                else if (e < len)  // the tensor's final bytes were not bulk-copied
+                    v[j] = load_partial(in + (base + e) * G::kElemBytes, int(len - e) * G::kElemBytes);
                 else
                     v[j] = make_uint4(0u, 0u, 0u, 0u);
             }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty_bar[stage]);  // the stage may be refilled
 
             uint32_t esc[J];
             uint32_t ex[J][4];  // exponents of each unit (BF16 uses [0..1])
+            uint32_t cnt[kWords];
 #pragma unroll
             for (int j = 0; j < J; ++j) ex[j][2] = ex[j][3] = 0u;
-            PackedCounts<J> cnt;
 #pragma unroll
-            for (int k = 0; k < kWords; ++k) cnt.w[k] = 0;
+            for (int k = 0; k < kWords; ++k) cnt[k] = 0;
 
 #pragma unroll
             for (int j = 0; j < J; ++j) {
-                const uint32_t e = (uint32_t(j) * kEncodeThreads + tid) * G::kUnitElems;
+                const uint32_t e = (uint32_t(j) * kConsumers + tid) * G::kUnitElems;
                 const uint32_t valid = e < len ? min(len - e, uint32_t(G::kUnitElems)) : 0u;
                 if constexpr (DT == SPLITZIP_BF16) {
                     uint32_t nib;
                     uint2 sm;
                     encode_unit_bf16(v[j], lut, nib, sm, esc[j], ex[j][0], ex[j][1]);
-                    uint8_t* nb = a.nibbles + (base + e) / 2;
-                    uint8_t* sb = a.signmant + (base + e);
+                    uint8_t* nb = nibbles + (base + e) / 2;
+                    uint8_t* sb = signmant + (base + e);
                     if (valid == 8u) {
                         __stcs(reinterpret_cast<uint32_t*>(nb), nib);
                         __stcs(reinterpret_cast<uint2*>(sb), sm);
@@ -219,12 +270,11 @@ encode_streams_kernel(const EncodeArgs a, const EncodeLut lut_in) {
                     uint2 nib;
                     uint32_t s3lo, s3hi;
                     encode_unit_e5m2(v[j], lut, nib, s3lo, s3hi, esc[j], ex[j]);
-                    uint8_t* nb = a.nibbles + (base + e) / 2;
-                    // s3 bytes of this unit start at 3 * (element index) / 8
-                    uint8_t* sb = a.signmant + (base + e) / 8 * 3;
+                    uint8_t* nb = nibbles + (base + e) / 2;
+                    uint8_t* sb = signmant + (base + e) / 8 * 3;  // 6 s3 bytes per unit
                     // fast path: the warp's 32 units are full and the tile is a
                     // multiple of 512 elements, so its 192 s3 bytes are 16-aligned
-                    const uint32_t warp_e0 = (uint32_t(j) * kEncodeThreads + warp * 32u) * G::kUnitElems;
+                    const uint32_t warp_e0 = (uint32_t(j) * kConsumers + warp * 32u) * G::kUnitElems;
                     const bool warp_full = (FULL || a.tile_elems % 512u == 0u) && (warp_e0 + 512u <= len);
                     if (valid == 16u) {
                         __stcs(reinterpret_cast<uint2*>(nb), nib);
@@ -244,7 +294,7 @@ encode_streams_kernel(const EncodeArgs a, const EncodeLut lut_in) {
                         __syncwarp();
                         if (lane < 12) {
                             const uint4 q = reinterpret_cast<const uint4*>(s3_stage[warp])[lane];
-                            uint8_t* dst = a.signmant + (base + warp_e0) / 8 * 3 + 16 * lane;
+                            uint8_t* dst = signmant + (base + warp_e0) / 8 * 3 + 16 * lane;
                             __stcs(reinterpret_cast<uint4*>(dst), q);
                         }
                         __syncwarp();
@@ -262,15 +312,14 @@ encode_streams_kernel(const EncodeArgs a, const EncodeLut lut_in) {
                         }
                     }
                 }
-                const uint32_t c = __popc(esc[j]);
-                cnt.w[j >> 1] |= c << (16 * (j & 1));
+                cnt[j >> 1] |= uint32_t(__popc(esc[j])) << (16 * (j & 1));
             }
 
-            // ---- block-wide exclusive scan of the per-thread escape counts, in
-            // element order (unit group j major, then thread) ----
+            // ---- block-wide exclusive scan of the per-thread escape counts,
+            // in element order (unit group j major, then thread) ----
             uint32_t incl[kWords];
 #pragma unroll
-            for (int k = 0; k < kWords; ++k) incl[k] = cnt.w[k];
+            for (int k = 0; k < kWords; ++k) incl[k] = cnt[k];
 #pragma unroll
             for (int d = 1; d < 32; d <<= 1) {
 #pragma unroll
@@ -283,12 +332,12 @@ encode_streams_kernel(const EncodeArgs a, const EncodeLut lut_in) {
 #pragma unroll
                 for (int k = 0; k < kWords; ++k) warp_sums[parity][warp][k] = incl[k];
             }
-            __syncthreads();
+            named_barrier(1, kConsumers);
             uint32_t before[kWords], total[kWords];
 #pragma unroll
             for (int k = 0; k < kWords; ++k) before[k] = total[k] = 0u;
 #pragma unroll
-            for (int w = 0; w < kWarps; ++w) {
+            for (int w = 0; w < kConsumerWarps; ++w) {
 #pragma unroll
                 for (int k = 0; k < kWords; ++k) {
                     const uint32_t s = warp_sums[parity][w][k];
@@ -296,16 +345,25 @@ encode_streams_kernel(const EncodeArgs a, const EncodeLut lut_in) {
                     total[k] += s;
                 }
             }
+            uint32_t tile_total = 0;
+#pragma unroll
+            for (int j = 0; j < J; ++j) tile_total += (total[j >> 1] >> (16 * (j & 1))) & 0xFFFFu;
 
-            uint32_t group_base = 0;  // escapes of the tile in unit groups < j
+            if (tid == 0) {
+                a.tile_counts[tile] = tile_total;
+                if (tile_total) atomicAdd(a.group_totals + tile / kGroupTiles, tile_total);
+            }
+
+            // ---- escape records, in element order, to the tile's staging slot ----
             uint32_t* slot = a.staging + tile * a.tile_elems;
+            uint32_t group_base = 0;  // escapes of the tile in unit groups < j
 #pragma unroll
             for (int j = 0; j < J; ++j) {
                 const int k = j >> 1, sh = 16 * (j & 1);
-                const uint32_t excl = ((before[k] + incl[k] - cnt.w[k]) >> sh) & 0xFFFFu;
+                const uint32_t excl = ((before[k] + incl[k] - cnt[k]) >> sh) & 0xFFFFu;
                 uint32_t idx = group_base + excl;
                 uint32_t m = esc[j];
-                const uint32_t upos = pos0 + (uint32_t(j) * kEncodeThreads + tid) * G::kUnitElems;
+                const uint32_t upos = pos0 + (uint32_t(j) * kConsumers + tid) * G::kUnitElems;
                 while (m) {
                     const uint32_t b = __ffs(m) - 1;
                     m &= m - 1;
@@ -316,7 +374,6 @@ encode_streams_kernel(const EncodeArgs a, const EncodeLut lut_in) {
                 }
                 group_base += (total[k] >> sh) & 0xFFFFu;
             }
-            if (tid == 0) a.tile_counts[tile] = group_base;
         };
         if (len_rt == kTileElems)
             body(std::true_type{});
@@ -325,129 +382,101 @@ encode_streams_kernel(const EncodeArgs a, const EncodeLut lut_in) {
     }
 }
 
-// ---------------------------------------------------------------------------
-// index: per-chunk counts, exclusive prefix, E, size, status, padding
-
-__device__ __forceinline__ void zero_bytes(uint8_t* p, uint64_t from, uint64_t to) {
-    for (uint64_t i = from; i < to; ++i) p[i] = 0;
-}
-
-__global__ void __launch_bounds__(kIndexThreads)
-encode_index_kernel(const EncodeArgs a, uint64_t* out_size, int* status) {
-    __shared__ uint64_t sums[kIndexThreads];
-    const int tid = threadIdx.x;
-    const uint64_t C = a.n_chunks;
-    const uint32_t tpc = a.chunk_elems / a.tile_elems;
-    const Layout L = layout_for(a.n, a.dtype, a.chunk_elems, 0);
-    uint32_t* counts = reinterpret_cast<uint32_t*>(a.out + L.counts_off);
-    uint64_t* offsets = reinterpret_cast<uint64_t*>(a.out + L.index_off);
-
-    // phase 1: chunk counts, coalesced over chunks
-    for (uint64_t c = tid; c < C; c += kIndexThreads) {
-        const uint64_t t0 = c * tpc;
-        const uint64_t t1 = min(t0 + tpc, a.n_tiles);
-        uint32_t s = 0;
-        for (uint64_t t = t0; t < t1; ++t) s += a.tile_counts[t];
-        counts[c] = s;
-    }
-    __syncthreads();
-    // phase 2: each thread owns a contiguous range of chunks
-    const uint64_t per = (C + kIndexThreads - 1) / kIndexThreads;
-    const uint64_t c0 = min(C, uint64_t(tid) * per), c1 = min(C, c0 + per);
-    uint64_t mine = 0;
-    for (uint64_t c = c0; c < c1; ++c) mine += counts[c];
-    sums[tid] = mine;
-    __syncthreads();
-    // Hillis-Steele inclusive scan over the block
-    for (int d = 1; d < kIndexThreads; d <<= 1) {
-        const uint64_t y = tid >= d ? sums[tid - d] : 0;
-        __syncthreads();
-        sums[tid] += y;
-        __syncthreads();
-    }
-    uint64_t run = sums[tid] - mine;
-    for (uint64_t c = c0; c < c1; ++c) {
-        offsets[c] = run;
-        run += counts[c];
-    }
-    if (tid == 0) {
-        const uint64_t E = sums[kIndexThreads - 1];
-        const Layout F = layout_for(a.n, a.dtype, a.chunk_elems, E);
-        reinterpret_cast<uint64_t*>(a.out)[3] = E;
-        zero_bytes(a.out, F.index_end, F.nibble_off);
-        zero_bytes(a.out, F.nibble_off + (a.n + 1) / 2, F.signmant_off);
-        zero_bytes(a.out, F.signmant_off + signmant_bytes(a.dtype, a.n), F.escpos_off);
-        zero_bytes(a.out, F.escpos_off + 2 * E, F.escexp_off);
-        *out_size = F.size;
-        *status = SPLITZIP_OK;
-    }
-}
-
-// ---------------------------------------------------------------------------
-// gather: one warp per tile moves the staged records to the escape arrays
-
-__global__ void __launch_bounds__(kGatherThreads) encode_gather_kernel(const EncodeArgs a) {
-    const int lane = threadIdx.x & 31;
-    const uint64_t warps = uint64_t(gridDim.x) * (kGatherThreads / 32);
-    const uint64_t first_warp = uint64_t(blockIdx.x) * (kGatherThreads / 32) + (threadIdx.x >> 5);
-    const uint64_t E = reinterpret_cast<const uint64_t*>(a.out)[3];
-    const Layout L = layout_for(a.n, a.dtype, a.chunk_elems, E);
-    const uint64_t* offsets = reinterpret_cast<const uint64_t*>(a.out + L.index_off);
-    uint16_t* pos = reinterpret_cast<uint16_t*>(a.out + L.escpos_off);
-    uint8_t* exps = a.out + L.escexp_off;
-    const uint32_t tpc = a.chunk_elems / a.tile_elems;
-
-    for (uint64_t tile = first_warp; tile < a.n_tiles; tile += warps) {
-        const uint32_t cnt = a.tile_counts[tile];
-        if (cnt == 0) continue;
-        const uint64_t c = tile / tpc, first = c * tpc;
-        // escapes of the earlier tiles of the same chunk (fewer than 32 tiles)
-        const uint32_t earlier = uint32_t(tile - first);
-        uint32_t s = (uint32_t(lane) < earlier) ? a.tile_counts[first + lane] : 0u;
+__device__ __forceinline__ uint64_t warp_sum_u64(uint64_t v) {
 #pragma unroll
-        for (int d = 16; d > 0; d >>= 1) s += __shfl_xor_sync(kFull, s, d);
-        const uint64_t off = offsets[c] + s;
-        const uint32_t* slot = a.staging + tile * a.tile_elems;
+    for (int d = 16; d > 0; d >>= 1) v += __shfl_xor_sync(kFull, v, d);
+    return v;
+}
+
+// One CTA per group of kGroupTiles tiles (groups are chunk-aligned: tiles per
+// chunk is a power of two <= 8).
+__global__ void __launch_bounds__(kFinishThreads) encode_finish_kernel(const EncodeArgs a) {
+    constexpr int kWarps = kFinishThreads / 32;
+    __shared__ uint64_t warp_part[kWarps];
+    __shared__ uint32_t warp_incl[kWarps];
+    __shared__ uint32_t tile_off[kFinishThreads + 1];  // exclusive prefix of the group's tile counts
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const uint64_t g = blockIdx.x;
+
+    // records of all earlier groups
+    uint64_t before = 0;
+    for (uint64_t q = tid; q < g; q += kFinishThreads) before += a.group_totals[q];
+    before = warp_sum_u64(before);
+    if (lane == 0) warp_part[warp] = before;
+
+    // exclusive scan of the group's tile counts
+    const uint64_t t = g * kGroupTiles + tid;
+    const uint32_t c = t < a.n_tiles ? a.tile_counts[t] : 0u;
+    uint32_t incl = c;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const uint32_t y = __shfl_up_sync(kFull, incl, d);
+        if (lane >= d) incl += y;
+    }
+    if (lane == 31) warp_incl[warp] = incl;
+    __syncthreads();
+    uint64_t group_base = 0;
+    uint32_t warp_before = 0, group_total = 0;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+        group_base += warp_part[w];
+        if (w < warp) warp_before += warp_incl[w];
+        group_total += warp_incl[w];
+    }
+    tile_off[tid] = warp_before + incl - c;
+    if (tid == 0) tile_off[kFinishThreads] = group_total;
+    __syncthreads();
+
+    const Layout L0 = layout_for(a.n, a.dtype, a.chunk_elems, 0);
+    // index entries of the chunks that start in this group
+    const uint32_t tpc = a.chunk_elems / a.tile_elems;
+    if (t < a.n_tiles && t % tpc == 0) {
+        const uint64_t chunk = t / tpc;
+        reinterpret_cast<uint64_t*>(a.out + L0.index_off)[chunk] = group_base + tile_off[tid];
+        reinterpret_cast<uint32_t*>(a.out + L0.counts_off)[chunk] = tile_off[tid + tpc] - tile_off[tid];
+    }
+
+    // staged records -> 3-byte records in the escape stream (a warp per tile)
+    uint8_t* records = a.out + L0.escrec_off;
+    for (int k = warp; k < kFinishThreads; k += kWarps) {
+        const uint64_t tk = g * kGroupTiles + k;
+        if (tk >= a.n_tiles) break;
+        const uint32_t cnt = tile_off[k + 1] - tile_off[k];
+        const uint32_t* slot = a.staging + tk * a.tile_elems;
+        uint8_t* dst = records + 3 * (group_base + tile_off[k]);
         for (uint32_t i = lane; i < cnt; i += 32) {
             const uint32_t r = slot[i];
-            pos[off + i] = uint16_t(r >> 8);
-            exps[off + i] = uint8_t(r & 0xFFu);
+            dst[3 * i] = uint8_t(r >> 8);
+            dst[3 * i + 1] = uint8_t(r >> 16);
+            dst[3 * i + 2] = uint8_t(r);
         }
+    }
+
+    if (g + 1 == a.n_groups && tid == 0) {  // the last group knows E
+        const uint64_t E = group_base + group_total;
+        reinterpret_cast<uint64_t*>(a.out)[3] = E;
+        *a.out_size = layout_for(a.n, a.dtype, a.chunk_elems, E).size;
     }
 }
 
 }  // namespace
 
-cudaError_t launch_encode_streams(const EncodeArgs& a, const EncodeLut& lut, int grid, cudaStream_t s) {
+cudaError_t launch_encode(const EncodeArgs& a, const EncodeLut& lut, int grid, cudaStream_t s) {
     if (a.dtype == SPLITZIP_BF16)
-        encode_streams_kernel<SPLITZIP_BF16><<<grid, kEncodeThreads, 0, s>>>(a, lut);
+        encode_kernel<SPLITZIP_BF16><<<grid, kBlock, kEncodeSmem, s>>>(a, lut);
     else
-        encode_streams_kernel<SPLITZIP_FP8_E5M2><<<grid, kEncodeThreads, 0, s>>>(a, lut);
-    return cudaGetLastError();
-}
-
-cudaError_t launch_encode_escapes(const EncodeArgs& a, uint64_t* d_out_size, int* d_status, int grid,
-                                  cudaStream_t s) {
-    encode_index_kernel<<<1, kIndexThreads, 0, s>>>(a, d_out_size, d_status);
-    cudaError_t err = cudaGetLastError();
-    if (err != cudaSuccess || a.n_tiles == 0) return err;
-    encode_gather_kernel<<<grid, kGatherThreads, 0, s>>>(a);
+        encode_kernel<SPLITZIP_FP8_E5M2><<<grid, kBlock, kEncodeSmem, s>>>(a, lut);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess || a.n_groups == 0) return e;
+    encode_finish_kernel<<<unsigned(a.n_groups), kFinishThreads, 0, s>>>(a);
     return cudaGetLastError();
 }
 
 cudaError_t occupancy_encode(int* blocks_per_sm, int dtype) {
-    if (dtype == SPLITZIP_BF16)
-        return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm,
-                                                             encode_streams_kernel<SPLITZIP_BF16>,
-                                                             kEncodeThreads, 0);
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm,
-                                                         encode_streams_kernel<SPLITZIP_FP8_E5M2>,
-                                                         kEncodeThreads, 0);
-}
-
-cudaError_t occupancy_gather(int* blocks_per_sm) {
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, encode_gather_kernel,
-                                                         kGatherThreads, 0);
+    auto k = dtype == SPLITZIP_BF16 ? encode_kernel<SPLITZIP_BF16> : encode_kernel<SPLITZIP_FP8_E5M2>;
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kEncodeSmem));
+    if (e != cudaSuccess) return e;
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, k, kBlock, kEncodeSmem);
 }
 
 }  // namespace splitzip

@@ -12,8 +12,9 @@
 // GPU that loads this library, for the life of the process.  All calls on a
 // device share it: calls whose GPU work overlaps in time (different streams,
 // or several host threads) race on it and must be serialised by the caller.
-// The encoder writes every scratch byte before it reads it, so the contents
-// left by an earlier call never need clearing.
+// splitzip_encode clears the part of the scratch that must start at zero (on
+// the caller's stream, before its kernel), so the contents left by an earlier
+// call do no harm.
 #include <mutex>
 
 #include "splitzip_internal.cuh"

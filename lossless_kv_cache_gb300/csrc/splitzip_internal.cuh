@@ -14,16 +14,11 @@ constexpr uint64_t kHeaderBytes = 64;
 constexpr uint32_t kMinChunk = 64;
 constexpr uint32_t kMaxChunk = 65536;
 
-// Work decomposition.  A tile is the unit one CTA processes per loop trip:
-// 256 threads x 32 elements.  A tile never straddles a chunk (chunk sizes are
-// powers of two >= 64, so tile_elems = min(kTileElems, chunk_elems) divides
-// chunk_elems).
-constexpr int kEncodeThreads = 256;
+// Work decomposition.  A tile is the unit of work of one encode CTA trip:
+// 8,192 elements, or the chunk when chunks are smaller, so a tile never
+// straddles a chunk (chunk sizes are powers of two >= 64).
 constexpr uint32_t kTileElems = 8192;
-constexpr int kDecodeThreads = 512;
 constexpr int kHistThreads = 256;
-constexpr int kIndexThreads = 1024;
-constexpr int kGatherThreads = 256;
 
 // Encoder table entry: low 4 bits = code, bit 4 = escape flag.
 constexpr uint8_t kEscapeFlag = 0x10;
@@ -37,7 +32,7 @@ __host__ __device__ inline uint64_t signmant_bytes(int dtype, uint64_t n) {
 // Byte offsets of every section of a container (format v1, see splitzip.h).
 struct Layout {
     uint64_t n_chunks;
-    uint64_t index_off, counts_off, index_end, nibble_off, signmant_off, escpos_off, escexp_off, size;
+    uint64_t index_off, counts_off, index_end, nibble_off, signmant_off, escrec_off, size;
 };
 
 __host__ __device__ inline Layout layout_for(uint64_t n, int dtype, uint32_t chunk, uint64_t E) {
@@ -48,9 +43,8 @@ __host__ __device__ inline Layout layout_for(uint64_t n, int dtype, uint32_t chu
     L.index_end = L.counts_off + 4u * L.n_chunks;
     L.nibble_off = align16(L.index_end);
     L.signmant_off = L.nibble_off + align16((n + 1u) / 2u);
-    L.escpos_off = L.signmant_off + align16(signmant_bytes(dtype, n));
-    L.escexp_off = L.escpos_off + align16(2u * E);
-    L.size = L.escexp_off + E;
+    L.escrec_off = L.signmant_off + align16(signmant_bytes(dtype, n));
+    L.size = L.escrec_off + 3u * E;
     return L;
 }
 
@@ -58,20 +52,28 @@ __host__ __device__ inline uint32_t tile_elems_for(uint32_t chunk) {
     return chunk < kTileElems ? chunk : kTileElems;
 }
 
-// Encoder workspace: per-tile escape counts, then per-tile staging slots of
-// tile_elems records each.  A record is (in-chunk position << 8) | exponent.
+// Encoder workspace: per-tile escape counts, per-group totals (a group is
+// kGroupTiles consecutive tiles), then one staging slot of tile_elems records
+// per tile; a record is (in-chunk position << 8) | exponent.  Only the group
+// totals must be zero when the encode starts (`zero_bytes`); everything else
+// is written before it is read.
+constexpr uint32_t kGroupTiles = 256;
+
 struct Workspace {
-    uint64_t n_tiles;
+    uint64_t n_tiles, n_groups;
     uint32_t tile_elems;
-    uint64_t counts_off, staging_off, bytes;
+    uint64_t group_off, count_off, staging_off, zero_bytes, bytes;
 };
 
 __host__ __device__ inline Workspace workspace_for(uint64_t n, uint32_t chunk) {
     Workspace W;
     W.tile_elems = tile_elems_for(chunk);
     W.n_tiles = (n + W.tile_elems - 1u) / W.tile_elems;
-    W.counts_off = 0;
-    W.staging_off = align16(4u * W.n_tiles);
+    W.n_groups = (W.n_tiles + kGroupTiles - 1u) / kGroupTiles;
+    W.group_off = 0;
+    W.zero_bytes = align16(4u * W.n_groups);
+    W.count_off = W.zero_bytes;
+    W.staging_off = align16(W.count_off + 4u * W.n_tiles);
     W.bytes = W.staging_off + 4u * W.n_tiles * W.tile_elems;
     return W;
 }
@@ -83,12 +85,13 @@ struct EncodeLut {
 struct EncodeArgs {
     const void* in;
     uint64_t n;
-    uint8_t* out;           // container base
-    uint8_t* nibbles;       // out + nibble_off
-    uint8_t* signmant;      // out + signmant_off
-    uint32_t* tile_counts;  // workspace
-    uint32_t* staging;      // workspace
-    uint64_t n_tiles;
+    uint8_t* out;            // container base
+    uint32_t* group_totals;  // workspace, per group of kGroupTiles tiles
+    uint32_t* tile_counts;   // workspace, per tile
+    uint32_t* staging;       // workspace, tile_elems records per tile
+    uint64_t* out_size;
+    int* error;              // device status word
+    uint64_t n_tiles, n_groups;
     uint32_t tile_elems;
     uint32_t chunk_elems;
     uint64_t n_chunks;
@@ -106,23 +109,16 @@ struct DecodeArgs {
 };
 
 // Launchers (encode.cu, decode.cu, histogram.cu).  Each returns the result of
-// cudaGetLastError() after its launches.
-cudaError_t launch_encode_streams(const EncodeArgs& a, const EncodeLut& lut, int grid, cudaStream_t s);
-cudaError_t launch_encode_escapes(const EncodeArgs& a, uint64_t* d_out_size, int* d_status, int grid,
-                                  cudaStream_t s);
+// cudaGetLastError() after its launch.
+cudaError_t launch_encode(const EncodeArgs& a, const EncodeLut& lut, int grid, cudaStream_t s);
 cudaError_t launch_decode(const DecodeArgs& a, int grid, cudaStream_t s);
 cudaError_t launch_histogram(const void* x, uint64_t n, int dtype, unsigned long long* hist, int grid,
                              cudaStream_t s);
 
-// Resident-CTA counts per SM for each kernel (filled once per device).
-struct DeviceInfo {
-    int sm_count;
-    int cc_major, cc_minor;
-    int encode_blocks_per_sm, decode_blocks_per_sm, gather_blocks_per_sm, hist_blocks_per_sm;
-};
+// Resident CTAs per SM of each kernel; the encode/decode versions also raise
+// the kernels' dynamic shared-memory limit (call once per device).
 cudaError_t occupancy_encode(int* blocks_per_sm, int dtype);
 cudaError_t occupancy_decode(int* blocks_per_sm, int dtype);
-cudaError_t occupancy_gather(int* blocks_per_sm);
 cudaError_t occupancy_histogram(int* blocks_per_sm, int dtype);
 
 }  // namespace splitzip

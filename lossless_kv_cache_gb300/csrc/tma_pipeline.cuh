@@ -75,6 +75,35 @@ __device__ __forceinline__ void named_barrier(uint32_t id, uint32_t threads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
+// Named barrier that also ANDs a predicate over the participating threads:
+// every participant gets the same answer, so a decision taken on it keeps all
+// of them on the same path through later barriers.
+__device__ __forceinline__ bool named_barrier_and(uint32_t id, uint32_t threads, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "barrier.cta.red.and.pred q, %2, %3, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"(uint32_t(pred)), "r"(id), "r"(threads)
+        : "memory");
+    return r != 0;
+}
+
+// Before a producer thread leaves: wait (bounded) until the last bulk copy of
+// every stage has landed, so no copy is still writing into shared memory when
+// the CTA exits.  `issued` = number of stage uses so far.
+__device__ __forceinline__ bool drain_stages(uint64_t* full_bar, uint32_t stages, uint32_t issued) {
+    bool ok = true;
+    for (uint32_t s = 0; s < stages && s < issued; ++s) {
+        // the last use of stage (issued - 1 - s) % stages
+        const uint32_t it = issued - 1 - s;
+        ok &= mbar_wait(&full_bar[it % stages], (it / stages) & 1u);
+    }
+    return ok;
+}
+
 // A 16-byte-aligned window that covers [p, p + bytes): the bulk copy moves the
 // window, the reader skips `offset` bytes.
 struct Window {

@@ -39,10 +39,11 @@
  *                 64+8C u32 esc_count[C]
  *                 A16 nibble stream ceil(n/2) bytes
  *                 A16 sign|mantissa stream (BF16 n bytes, E5M2 3*ceil(n/8))
- *                 A16 esc_pos u16[E]  (chunk-major, ascending in-chunk pos)
- *                 A16 esc_exp u8[E]   (same order); the blob ends here.
- *   READING R9  escape records stored as two arrays (positions, then
- *               exponents): still 16 + 8 bits per escape.
+ *                 A16 escape records, E x 3 bytes (chunk-major, ascending
+ *                     in-chunk position); the blob ends here.
+ *   READING R9  one escape record = 3 bytes: the 16-bit in-chunk position
+ *               (little-endian) then the 8-bit exponent, exactly the
+ *               (position, exponent) pair the page describes.
  *   READING R10 fixed chunk_elems, a power of two in [64, 65536] (the 16-bit
  *               position field bounds it); the final chunk may be short.
  *   READING R11 the 16-bit position is the in-chunk index.
@@ -134,7 +135,7 @@ static uint64_t sm_stream_bytes(int dtype, uint64_t n) {
 
 typedef struct {
     uint64_t n_chunks;
-    uint64_t index_off, counts_off, nib_off, sm_off, pos_off, exp_off, size;
+    uint64_t index_off, counts_off, nib_off, sm_off, rec_off, size;
 } layout_t;
 
 static layout_t layout_of(uint64_t n, int dtype, uint32_t chunk, uint64_t E) {
@@ -144,9 +145,8 @@ static layout_t layout_of(uint64_t n, int dtype, uint32_t chunk, uint64_t E) {
     L.counts_off = L.index_off + 8u * L.n_chunks;
     L.nib_off = align16(L.counts_off + 4u * L.n_chunks);
     L.sm_off = L.nib_off + align16((n + 1u) / 2u);
-    L.pos_off = L.sm_off + align16(sm_stream_bytes(dtype, n));
-    L.exp_off = L.pos_off + align16(2u * E);
-    L.size = L.exp_off + E;
+    L.rec_off = L.sm_off + align16(sm_stream_bytes(dtype, n));
+    L.size = L.rec_off + 3u * E;
     return L;
 }
 
@@ -280,8 +280,8 @@ int oracle_encode(const void* x, uint64_t n, int dtype, const uint8_t* cb16, uin
         int code = code_of(cb16, e);
         if (code < 0) {
             uint64_t pos = i % chunk;
-            put_u16(out + L.pos_off + 2u * next_escape, (uint16_t)pos);
-            out[L.exp_off + next_escape] = (uint8_t)e;
+            put_u16(out + L.rec_off + 3u * next_escape, (uint16_t)pos);
+            out[L.rec_off + 3u * next_escape + 2u] = (uint8_t)e;
             next_escape++;
             code = 0;
         }
@@ -383,10 +383,11 @@ int oracle_decode(const uint8_t* blob, uint64_t bytes, void* out, uint64_t n, in
         uint64_t cnt = get_u32(blob + L.counts_off + 4u * c);
         uint64_t len = (c + 1 < C) ? chunk : n - c * chunk;
         for (uint64_t j = 0; j < cnt; j++) {
-            uint64_t pos = get_u16(blob + L.pos_off + 2u * (off + j));
-            unsigned e = blob[L.exp_off + off + j];
+            const uint8_t* rec = blob + L.rec_off + 3u * (off + j);
+            uint64_t pos = get_u16(rec);
+            unsigned e = rec[2];
             if (pos >= len) return OR_CORRUPT;
-            if (j > 0 && pos <= get_u16(blob + L.pos_off + 2u * (off + j - 1))) return OR_CORRUPT;
+            if (j > 0 && pos <= get_u16(rec - 3)) return OR_CORRUPT;
             if (e >= exponent_bins(dtype)) return OR_CORRUPT;
             uint64_t i = c * chunk + pos;
             unsigned v = read_element(out, dtype, i);

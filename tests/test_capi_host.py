@@ -56,10 +56,14 @@ def test_sizes_match_oracle(splitzip_lib, dtype, chunk):
 
 
 def test_workspace_size(splitzip_lib):
-    # per-tile counts + 4 bytes of staging per element slot
+    # per-group totals, per-tile counts, then a staging slot of tile_elems
+    # 4-byte records per tile
+    a16 = lambda x: -(-x // 16) * 16
     n = 5 * 8192 + 3
     tiles = 6
-    assert sz.workspace_size(n, sz.BF16, 65536) == -(-4 * tiles // 16) * 16 + 4 * tiles * 8192
+    assert sz.workspace_size(n, sz.BF16, 65536) == a16(a16(4) + 4 * tiles) + 4 * tiles * 8192
+    tiles = -(-n // 1024)  # tiles = chunks when chunks are smaller than 8192
+    assert sz.workspace_size(n, sz.BF16, 1024) == a16(a16(4) + 4 * tiles) + 4 * tiles * 1024
     assert sz.workspace_size(0, sz.BF16, 65536) == 0
 
 

@@ -178,25 +178,27 @@ def test_histogram_e5m2_and_tail():
     np.testing.assert_array_equal(h2.numpy().view(np.uint64), oracle.histogram(np_bits(y, 0), 0))
 
 
-# ------------------------------------------------------------- encode stages
+# ----------------------------------------------------- streams and reuse
 
-def test_encode_stages_equal_one_shot():
-    x = W.escape_stress(5, chunks=5, chunk_elems=65536)[:300001].to(DEV)
-    cb = codebook_of(np.arange(120, 136), 0)
-    one = gpu_encode(x, cb, 0, 65536).cpu()
+def test_side_stream_and_reused_workspace():
+    """Encode on a non-default stream twice into the same buffers (the
+    workspace keeps the first call's look-back state); both match the oracle."""
+    x = W.escape_stress(5, chunks=5, chunk_elems=65536)[:300001]
+    bits = np_bits(x, 0)
+    cb_exps = np.arange(120, 136)
+    ref = oracle.encode(bits, 0, cb_exps.astype(np.uint8), 65536)
+    xd = x.to(DEV)
     bufs = sz.EncodeBuffers(x.numel(), 0, 65536)
-    bufs.out.fill_(0x11)
     s = torch.cuda.Stream()
-    with torch.cuda.stream(s):
-        h = s.cuda_stream
-        assert sz.splitzip_encode_streams(x.data_ptr(), x.numel(), 0, cb, 65536, bufs.out.data_ptr(),
-                                          bufs.capacity, bufs.ws.data_ptr(), bufs.ws_bytes, h) == sz.OK
-        assert sz.splitzip_encode_escapes(x.numel(), 0, 65536, bufs.out.data_ptr(), bufs.capacity,
-                                          bufs.ws.data_ptr(), bufs.ws_bytes, bufs.size.data_ptr(),
-                                          bufs.status.data_ptr(), h) == sz.OK
-    s.synchronize()
-    assert int(bufs.status[0]) == sz.OK
-    assert torch.equal(bufs.out[: int(bufs.size[0])].cpu(), one)
+    for fill in (0x11, 0xEE):
+        bufs.out.fill_(fill)
+        torch.cuda.synchronize()
+        with torch.cuda.stream(s):
+            sz.encode_into(xd, codebook_of(cb_exps, 0), bufs, stream=s)
+        s.synchronize()
+        assert int(bufs.status[0]) == sz.OK
+        got = bufs.out[: int(bufs.size[0])].cpu().numpy()
+        np.testing.assert_array_equal(got, ref)
 
 
 # ------------------------------------------------------------- corruption
@@ -240,8 +242,9 @@ def test_chunk_aligned_shards_match_single_container():
     cp = np.concatenate([p[h.counts_off: h.counts_off + 4 * h.n_chunks].view(np.uint32) for p, h in zip(parts, hp)])
     np.testing.assert_array_equal(cw, cp)
     E0 = hp[0].total_escapes
-    pw = whole[hw.escpos_off: hw.escpos_off + 2 * hw.total_escapes]
-    np.testing.assert_array_equal(pw[: 2 * E0], parts[0][hp[0].escpos_off: hp[0].escpos_off + 2 * E0])
+    rw = whole[hw.escrec_off: hw.escrec_off + 3 * hw.total_escapes]
+    np.testing.assert_array_equal(rw[: 3 * E0], parts[0][hp[0].escrec_off: hp[0].escrec_off + 3 * E0])
+    np.testing.assert_array_equal(rw[3 * E0:], parts[1][hp[1].escrec_off: hp[1].size])
 
 
 # ------------------------------------------- the 4.3 GB workloads, sampled
@@ -251,9 +254,8 @@ def _layout(n, dtype, chunk, E):
     nib = a16(64 + 12 * C)
     sm = nib + a16((n + 1) // 2)
     sm_bytes = n if dtype == 0 else 3 * (-(-n // 8))
-    pos = sm + a16(sm_bytes)
-    ex = pos + a16(2 * E)
-    return dict(C=C, index=64, counts=64 + 8 * C, nib=nib, sm=sm, pos=pos, exp=ex, size=ex + E)
+    rec = sm + a16(sm_bytes)
+    return dict(C=C, index=64, counts=64 + 8 * C, nib=nib, sm=sm, rec=rec, size=rec + 3 * E)
 
 
 def _full_size_check(name, sample_chunks=12):
@@ -308,10 +310,9 @@ def _full_size_check(name, sample_chunks=12):
         got_sm = blob[L["sm"] + c * sm_per_chunk: L["sm"] + (c + 1) * sm_per_chunk].cpu().numpy()
         np.testing.assert_array_equal(got_sm, ref[R["sm"]: R["sm"] + sm_per_chunk])
         k, o = int(cnt[c]), int(off[c])
-        assert k == R["size"] - R["exp"]
-        np.testing.assert_array_equal(blob[L["pos"] + 2 * o: L["pos"] + 2 * (o + k)].cpu().numpy(),
-                                      ref[R["pos"]: R["pos"] + 2 * k])
-        np.testing.assert_array_equal(blob[L["exp"] + o: L["exp"] + o + k].cpu().numpy(), ref[R["exp"]: R["exp"] + k])
+        assert 3 * k == R["size"] - R["rec"]
+        np.testing.assert_array_equal(blob[L["rec"] + 3 * o: L["rec"] + 3 * (o + k)].cpu().numpy(),
+                                      ref[R["rec"]: R["rec"] + 3 * k])
 
     st, y = gpu_decode(blob, n, dtype)
     assert st == sz.OK

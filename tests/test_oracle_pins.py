@@ -59,9 +59,10 @@ def test_hand_split_bf16(bits, exp, sm):
     # codebook without `exp`: the element escapes with its exponent and position 0
     cb = np.array([v for v in range(256) if v != exp][:16], dtype=np.uint8)
     blob = oracle.encode(x, BF16, cb, 64)
-    # C=1: nibbles at 80, sign|mantissa at 96, esc_pos at 112, esc_exp at 128
+    # C=1: nibbles at 80, sign|mantissa at 96, the escape record at 112
     assert blob[96] == sm
-    assert blob[80] == 0 and blob[112] == 0 and blob[113] == 0 and blob[128] == exp
+    assert blob.size == 115
+    assert blob[80] == 0 and blob[112] == 0 and blob[113] == 0 and blob[114] == exp
     # codebook with `exp` as code 5: the nibble holds 5, no escape
     cb2 = cb.copy()
     cb2[5] = exp
@@ -74,7 +75,7 @@ def test_hand_split_e5m2(bits, exp, s3):
     x = np.array([bits], dtype=np.uint8)
     cb = np.array([v for v in range(32) if v != exp][:16], dtype=np.uint8)
     blob = oracle.encode(x, E5M2, cb, 64)
-    assert blob[96] == s3 and blob[128] == exp
+    assert blob[96] == s3 and blob[114] == exp
 
 
 # ------------------------------------------------------------- exhaustive sets
@@ -276,7 +277,7 @@ def corruptions(blob):
     st, h = oracle.parse_header(blob)
     C, E, n = h.n_chunks, h.total_escapes, h.n
     nib_off = a16(64 + 12 * C)
-    pos_off = nib_off + a16((n + 1) // 2) + a16(n)
+    rec_off = nib_off + a16((n + 1) // 2) + a16(n)
     out = []
 
     def mut(name, f):
@@ -294,8 +295,8 @@ def corruptions(blob):
     mut("codebook_dup", lambda b: b.__setitem__(33, b[32]))
     mut("offset_not_prefix", lambda b: b.__setitem__(64 + 8, b[64 + 8] ^ 1))
     mut("count_changed", lambda b: b.__setitem__(64 + 8 * C, b[64 + 8 * C] ^ 1))
-    mut("pos_out_of_chunk", lambda b: b[pos_off : pos_off + 2].__setitem__(slice(None), [0xFF, 0xFF]))
-    mut("pos_not_ascending", lambda b: b[pos_off + 2 : pos_off + 4].__setitem__(slice(None), b[pos_off : pos_off + 2]))
+    mut("pos_out_of_chunk", lambda b: b[rec_off : rec_off + 2].__setitem__(slice(None), [0xFF, 0xFF]))
+    mut("pos_not_ascending", lambda b: b[rec_off + 3 : rec_off + 5].__setitem__(slice(None), b[rec_off : rec_off + 2]))
     out.append(("truncated", blob[:-1].copy()))
     return out
 

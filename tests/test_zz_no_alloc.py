@@ -48,7 +48,7 @@ def test_noalloc_matches_encode_on_two_calls_in_a_row(splitzip_lib):
     got1 = _noalloc(x1, cb1, sz.BF16, 65536)
     assert torch.equal(got1, _regular(x1, cb1, sz.BF16, 65536))
     # call 2: heavier escapes, a ragged size and a smaller chunk, so the
-    # scratch still holds call 1's records at other offsets
+    # scratch still holds call 1's staged records at other offsets
     x2 = W.escape_stress(1, chunks=96, chunk_elems=65536)[: 6_000_001].to("cuda")
     cb2 = sz.Codebook.make(sz.BF16, range(118, 134))
     got2 = _noalloc(x2, cb2, sz.BF16, 4096)
