@@ -1,6 +1,10 @@
-"""Benchmark of the SplitZip GB300 codec: one step = encode + decode of the
-32-layer BF16 KV cache (32 x 2 x 32768 x 8 x 128 = 2,147,483,648 elements,
-4.29 GB), inputs resident in HBM.
+"""Benchmark of the SplitZip GB300 codec.
+
+One step = encode + decode of one KV tensor, inputs resident in HBM.  The
+default workload is the 32-layer BF16 KV cache (32 x 2 x 32768 x 8 x 128 =
+2,147,483,648 elements, 4.29 GB); `--workload` selects another of the five
+workloads of lossless_kv_cache_gb300.workloads (for reporting; the default is
+the headline line).
 
 Prints one JSON line.  `value` is the round-trip throughput in GB/s of
 uncompressed bytes (bytes of the tensor / (encode + decode time)); encode and
@@ -9,6 +13,7 @@ link-transfer model are reported beside it.  `--impl reference` times the CPU
 oracle on a bounded sample of the same workload instead.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                       [--workload NAME] [--layers L]
 Under torchrun each rank encodes/decodes its own copy of the workload (chunks
 are independent, no data exchange): weak scaling, max time over ranks.
 """
@@ -28,9 +33,10 @@ import numpy as np  # noqa: E402
 import torch  # noqa: E402
 
 METRIC = "encode/decode GB/s (uncompressed) on 1 GB300, % HBM roofline, ratio"
-WORKLOAD = "kv_cache_32x2x32768x8x128_bf16"
+DEFAULT_WORKLOAD = "kv_cache_32x2x32768x8x128_bf16"
 CHUNK = 65536
 LINKS_GBS = (50.0, 100.0)
+L2_BYTES = 129 * 1000 * 1000
 
 
 def parse_args():
@@ -39,12 +45,14 @@ def parse_args():
     p.add_argument("--steps", type=int, default=300)
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", default=DEFAULT_WORKLOAD)
     p.add_argument("--e2e-steps", type=int, default=5)
     p.add_argument("--cpu-seconds", type=float, default=10.0, help="oracle time budget for cpu_baseline")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--layers", type=int, default=32,
-                   help="encode only the first L layers (a smaller case for profiling; not a bench line)")
+                   help="32-layer workloads: encode only the first L layers (a smaller case for profiling; "
+                        "not a bench line)")
     return p.parse_args()
 
 
@@ -65,21 +73,13 @@ def barrier(world):
         dist.barrier()
 
 
-def max_over_ranks(x, world, device):
+def reduce_over_ranks(x, world, device, op):
+    """MAX or SUM of a float over the ranks (the value itself at world 1)."""
     if world == 1:
         return x
     import torch.distributed as dist
     t = torch.tensor([x], dtype=torch.float64, device=device)
-    dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    return float(t.item())
-
-
-def sum_over_ranks(x, world, device):
-    if world == 1:
-        return x
-    import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device=device)
-    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX if op == "max" else dist.ReduceOp.SUM)
     return float(t.item())
 
 
@@ -152,31 +152,57 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": n}
 
 
-# ------------------------------------------------------------ workload
+# ------------------------------------------------------------ workloads
 
-def generate(seed, device, layers):
-    from lossless_kv_cache_gb300 import workloads as W
-    _, layer = W.layers_of(WORKLOAD)
-    parts = [layer(seed, l, device) for l in range(layers)]
-    return torch.cat(parts)
+class Workload:
+    """One of the five workloads: raw-bit tensors and their sizes."""
 
+    def __init__(self, name, layers=32):
+        from lossless_kv_cache_gb300 import workloads as W
+        self.W = W
+        self.name = name
+        self.dtype = W.dtype_of(name)
+        self.elem_bytes = W.bytes_per_element(self.dtype)
+        self.layered = name in ("kv_cache_32x2x32768x8x128_bf16", "kv_cache_32x2x65536x8x128_e5m2")
+        self.layers = layers if self.layered else None
+        full = W.numel(name)
+        self.n = full // 32 * layers if self.layered else full
 
-def config_dict(world, layers=32):
-    name = WORKLOAD if layers == 32 else "%s (first %d layers only: profiling case)" % (WORKLOAD, layers)
-    return {"workload": name, "shape": [layers, 2, 32768, 8, 128], "elements": layers * 2 * 32768 * 1024,
-            "element_dtype": "bf16", "chunk_elems": CHUNK, "codebook": "Top-16 from layer 0 of seed 1",
-            "l2": "inputs 4.29 GB > 129 MB L2 (no flush needed)",
-            "parallelism": "replicas of the workload per GPU, no collective" if world > 1 else "single GPU"}
+    def make(self, seed, device):
+        if self.layered:
+            _, layer = self.W.layers_of(self.name)
+            return torch.cat([layer(seed, l, device) for l in range(self.layers)])
+        return self.W.make(self.name, seed, device)
 
+    def calibration(self, device):
+        return self.W.calibration_tensor(self.name, device)
 
-def escape_rate_of(blob_hdr_bytes, n):
-    E = int(np.frombuffer(blob_hdr_bytes[24:32], dtype=np.uint64)[0])
-    return E, E / n
+    def config(self, world):
+        label = self.name
+        if self.layered and self.layers != 32:
+            label = "%s (first %d layers only: profiling case)" % (self.name, self.layers)
+        return {"workload": label, "elements": self.n,
+                "element_dtype": "bf16" if self.dtype == 0 else "fp8_e5m2", "chunk_elems": CHUNK,
+                "codebook": "Top-16 from the seed-1 calibration tensor"
+                            + (" (layer 0)" if self.layered else ""),
+                "l2": ("inputs %.2f GB > 129 MB L2 (no flush needed)" % (self.n * self.elem_bytes / 1e9))
+                if self.n * self.elem_bytes > L2_BYTES else "L2 flushed (512 MB write) before every step",
+                "parallelism": "replicas of the workload per GPU, no collective" if world > 1 else "single GPU"}
+
+    def algorithmic_bytes(self, E):
+        """(encode, decode) bytes the method must move: the elements, the two
+        dense streams, 3 bytes per escape record and 12 bytes of index per
+        chunk."""
+        n = self.n
+        C = -(-n // CHUNK)
+        streams = (n + 1) // 2 + (n if self.dtype == 0 else 3 * (-(-n // 8)))
+        moved = n * self.elem_bytes + streams + 3 * E + 12 * C
+        return moved, moved
 
 
 # --------------------------------------------------------- CPU oracle
 
-def oracle_throughput(x_dev, cb_exps, seconds):
+def oracle_throughput(x_dev, dtype, cb_exps, seconds):
     """Encode + decode successive 64-chunk blocks of the workload with the
     scalar oracle until `seconds` of CPU time are spent; returns (GB/s
     uncompressed, elements, seconds)."""
@@ -184,16 +210,18 @@ def oracle_throughput(x_dev, cb_exps, seconds):
     block = 64 * CHUNK
     done, t_total = 0, 0.0
     cb = np.asarray(cb_exps, dtype=np.uint8)
-    while t_total < seconds and done + block <= x_dev.numel():
-        xs = x_dev[done: done + block].cpu().numpy().view(np.uint16)
+    eb = 2 if dtype == 0 else 1
+    while t_total < seconds and done < x_dev.numel():
+        xs = x_dev[done: done + block].cpu().numpy()
+        xs = xs.view(np.uint16) if dtype == 0 else xs
         t0 = time.perf_counter()
-        blob = oracle.encode(xs, 0, cb, CHUNK)
-        y = oracle.decode(blob, xs.size, 0)
+        blob = oracle.encode(xs, dtype, cb, CHUNK)
+        y = oracle.decode(blob, xs.size, dtype)
         t_total += time.perf_counter() - t0
         if not np.array_equal(y, xs):
             raise RuntimeError("oracle round trip failed")
-        done += block
-    return 2.0 * done / t_total / 1e9, done, t_total
+        done += xs.size
+    return eb * done / t_total / 1e9, done, t_total
 
 
 # ---------------------------------------------------------------- arms
@@ -202,34 +230,41 @@ def run_reference(args, world, rank):
     """The CPU oracle on a bounded sample of the workload, per step."""
     if rank != 0:
         return None
-    from lossless_kv_cache_gb300 import workloads as W
-    _, layer = W.layers_of(WORKLOAD)
-    x = layer(0, 0, "cpu").numpy().view(np.uint16)  # layer 0 of seed 0
-    cal = layer(1, 0, "cpu").numpy().view(np.uint16)
     import oracle
-    cb = oracle.calibrate(oracle.histogram(cal, 0), 0)
-    per_step = 16 * CHUNK  # elements per step (a bounded sample)
+    wl = Workload(args.workload, args.layers)
+    if wl.layered:
+        _, layer = wl.W.layers_of(wl.name)
+        x = layer(0, 0, "cpu").numpy()  # layer 0 of seed 0
+        cal = layer(1, 0, "cpu").numpy()
+    else:
+        x = wl.make(0, "cpu").numpy()
+        cal = wl.calibration("cpu").numpy()
+    if wl.dtype == 0:
+        x, cal = x.view(np.uint16), cal.view(np.uint16)
+    cb = oracle.calibrate(oracle.histogram(cal, wl.dtype), wl.dtype)
+    per_step = min(16 * CHUNK, x.size)  # elements per step (a bounded sample)
     times = []
     for s in range(args.warmup + args.steps):
         off = (s * per_step) % (x.size - per_step + 1)
         xs = x[off: off + per_step]
         t0 = time.perf_counter()
-        blob = oracle.encode(xs, 0, cb, CHUNK)
-        y = oracle.decode(blob, xs.size, 0)
+        blob = oracle.encode(xs, wl.dtype, cb, CHUNK)
+        y = oracle.decode(blob, xs.size, wl.dtype)
         dt = time.perf_counter() - t0
         if not np.array_equal(y, xs):
             raise RuntimeError("oracle round trip failed")
         if s >= args.warmup:
             times.append(dt)
     total = sum(times)
-    value = 2.0 * per_step * len(times) / total / 1e9
-    sample = "%d elements (%d chunks of 65536) of layer 0 per step, scalar C oracle, 1 thread" % (
-        per_step, per_step // CHUNK)
+    value = wl.elem_bytes * per_step * len(times) / total / 1e9
+    sample = "%d elements (%d chunks of 65536) of %s per step, scalar C oracle, 1 thread" % (
+        per_step, -(-per_step // CHUNK), "layer 0" if wl.layered else "the tensor")
     return {
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * total / len(times), 3),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u16",
-        "data": "synthetic (seeded torch CPU generator)", "config": config_dict(world),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "u16" if wl.dtype == 0 else "u8",
+        "data": "synthetic (seeded torch CPU generator)", "config": wl.config(world),
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -241,23 +276,22 @@ def run_ours(args, world, rank, local):
     device = torch.device("cuda", local)
     torch.cuda.set_device(device)
     sz.lib()  # fails loudly when the CUDA library is missing
-    n = args.layers * 2 * 32768 * 1024
-    raw_bytes = 2 * n
+    wl = Workload(args.workload, args.layers)
+    n, dtype = wl.n, wl.dtype
+    raw_bytes = wl.elem_bytes * n
 
-    x = generate(rank, device, args.layers)  # weak scaling: every rank has its own workload
-    from lossless_kv_cache_gb300 import workloads as W
-    _, layer = W.layers_of(WORKLOAD)
-    cal = layer(1, 0, device)
-    cb, _ = sz.calibrate(cal, sz.BF16)
-    del cal
+    x = wl.make(rank, device)  # weak scaling: every rank has its own workload
+    assert x.numel() == n
+    cb, _ = sz.calibrate(wl.calibration(device), dtype)
 
-    bufs = sz.EncodeBuffers(n, sz.BF16, CHUNK, device=device)
-    out = torch.empty(n, dtype=torch.int16, device=device)
+    bufs = sz.EncodeBuffers(n, dtype, CHUNK, device=device)
+    out = torch.empty(n, dtype=x.dtype, device=device)
     dstatus = torch.zeros(4, dtype=torch.int32, device=device)
     stream = torch.cuda.current_stream()
     h = stream.cuda_stream
     xp, op, wp, ws = x.data_ptr(), bufs.out.data_ptr(), bufs.ws.data_ptr(), bufs.ws_bytes
     cap = bufs.capacity
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=device) if raw_bytes <= L2_BYTES else None
 
     def check(st, what):
         if st != sz.OK:
@@ -266,12 +300,12 @@ def run_ours(args, world, rank, local):
     def step(ev=None):
         if ev is not None:
             ev[0].record(stream)
-        check(sz.splitzip_encode(xp, n, sz.BF16, cb, CHUNK, op, cap, wp, ws, bufs.size.data_ptr(),
+        check(sz.splitzip_encode(xp, n, dtype, cb, CHUNK, op, cap, wp, ws, bufs.size.data_ptr(),
                                  bufs.status.data_ptr(), h), "encode")
         if ev is not None:
             ev[1].record(stream)
         # decode bound: the buffer; the header carries the container's real size
-        check(sz.splitzip_decode(op, cap, out.data_ptr(), n, sz.BF16, dstatus.data_ptr(), h), "decode")
+        check(sz.splitzip_decode(op, cap, out.data_ptr(), n, dtype, dstatus.data_ptr(), h), "decode")
         if ev is not None:
             ev[2].record(stream)
 
@@ -281,9 +315,9 @@ def run_ours(args, world, rank, local):
     assert int(bufs.status[0]) == sz.OK and int(dstatus[0]) == sz.OK
     verified = bool(torch.equal(out, x))
     blob_size = int(bufs.size[0])
-    E, esc_rate = escape_rate_of(bufs.out[:64].cpu().numpy().tobytes(), n)
+    E = int(bufs.out[24:32].cpu().numpy().view(np.uint64)[0])
 
-    # ---- timed region: K steps, events around every kernel launch group ----
+    # ---- timed region: K steps, CUDA events around each launch group ----
     K = args.steps
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
     clocks = ClockSampler(local)
@@ -292,32 +326,33 @@ def run_ours(args, world, rank, local):
     torch.cuda.synchronize()
     t_wall0 = time.time()
     for k in range(K):
+        if flush is not None:
+            flush.fill_(k & 0xFF)  # small inputs: evict them from L2 between steps
         step(evs[k])
     torch.cuda.synchronize()
     t_wall1 = time.time()
     barrier(world)
     clk = clocks.stop(t_wall0, t_wall1)
-    total_ms = evs[0][0].elapsed_time(evs[-1][2])
-    total_ms = max_over_ranks(total_ms, world, device)
-    enc_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
-    dec_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
+    enc = [e[0].elapsed_time(e[1]) for e in evs]
+    dec = [e[1].elapsed_time(e[2]) for e in evs]
+    total_ms = evs[0][0].elapsed_time(evs[-1][2]) if flush is None else sum(enc) + sum(dec)
+    total_ms = reduce_over_ranks(total_ms, world, device, "max")
+    enc_ms, dec_ms = statistics.mean(enc), statistics.mean(dec)
     ms_per_step = total_ms / K
-    all_bytes = sum_over_ranks(raw_bytes * K, world, device)
+    all_bytes = reduce_over_ranks(raw_bytes * K, world, device, "sum")
     value = all_bytes / (total_ms * 1e-3) / 1e9
 
     # ---- roofline of the dominant kernel (algorithmic bytes / event time) ----
-    # encode: read BF16, write nibbles + sign|mantissa + 3 B per escape + index
-    # decode: the same bytes in the other direction.  Each call is one kernel
-    # (plus one or two 4-byte/workspace memsets, inside the events).
+    # Each call is essentially one streaming kernel (encode adds a short finish
+    # kernel and a 4-byte memset, decode a 4-byte memset, inside the events).
     peaks, peak_kind = measured_peaks()
     hbm = float(peaks["hbm_gbs"])
-    C = n // CHUNK
-    alg_encode = 2 * n + n // 2 + n + 3 * E + 12 * C
-    alg_decode = n // 2 + n + 3 * E + 12 * C + 2 * n
+    alg_encode, alg_decode = wl.algorithmic_bytes(E)
+    tag = "bf16" if dtype == 0 else "e5m2"
     if enc_ms >= dec_ms:
-        name, alg, ms = "encode_kernel<bf16>", alg_encode, enc_ms
+        name, alg, ms = "encode_kernel<%s> (+ encode_finish_kernel)" % tag, alg_encode, enc_ms
     else:
-        name, alg, ms = "decode_kernel<bf16>", alg_decode, dec_ms
+        name, alg, ms = "decode_kernel<%s>" % tag, alg_decode, dec_ms
     achieved = alg / (ms * 1e-3) / 1e9
     roofline = {"bound": "hbm", "kernel": name, "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
                 "frac": round(achieved / hbm, 4), "peak_source": "%s hbm_gbs (copy)" % peak_kind,
@@ -341,17 +376,17 @@ def run_ours(args, world, rank, local):
     # ---- e2e: host pinned input -> H2D -> encode -> decode -> D2H ----
     e2e = None
     if not args.no_e2e:
-        x_host = torch.empty(n, dtype=torch.int16, pin_memory=True)
+        x_host = torch.empty(n, dtype=x.dtype, pin_memory=True)
         x_host.copy_(x)
-        y_host = torch.empty(n, dtype=torch.int16, pin_memory=True)
+        y_host = torch.empty(n, dtype=x.dtype, pin_memory=True)
         xin = torch.empty_like(x)
         xin_p = xin.data_ptr()
 
         def e2e_step():
             xin.copy_(x_host, non_blocking=True)
-            check(sz.splitzip_encode(xin_p, n, sz.BF16, cb, CHUNK, op, cap, wp, ws, bufs.size.data_ptr(),
+            check(sz.splitzip_encode(xin_p, n, dtype, cb, CHUNK, op, cap, wp, ws, bufs.size.data_ptr(),
                                      bufs.status.data_ptr(), h), "encode")
-            check(sz.splitzip_decode(op, cap, out.data_ptr(), n, sz.BF16, dstatus.data_ptr(), h), "decode")
+            check(sz.splitzip_decode(op, cap, out.data_ptr(), n, dtype, dstatus.data_ptr(), h), "decode")
             y_host.copy_(out, non_blocking=True)
 
         e2e_step()
@@ -363,9 +398,9 @@ def run_ours(args, world, rank, local):
             e2e_step()
         eb.record(stream)
         torch.cuda.synchronize()
-        e2e_ms = max_over_ranks(ea.elapsed_time(eb), world, device)
+        e2e_ms = reduce_over_ranks(ea.elapsed_time(eb), world, device, "max")
         e2e_ok = bool(torch.equal(y_host, x_host))
-        e2e_bytes = sum_over_ranks(raw_bytes * args.e2e_steps, world, device)
+        e2e_bytes = reduce_over_ranks(raw_bytes * args.e2e_steps, world, device, "sum")
         e2e = {"value": round(e2e_bytes / (e2e_ms * 1e-3) / 1e9, 3), "unit": "GB/s",
                "h2d_bytes_per_step": raw_bytes, "d2h_bytes_per_step": raw_bytes,
                "ms_per_step": round(e2e_ms / args.e2e_steps, 3), "verified": e2e_ok}
@@ -374,27 +409,27 @@ def run_ours(args, world, rank, local):
     # ---- CPU oracle on a bounded sample (rank 0 only) ----
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
-        gbs, elems, secs = oracle_throughput(x, cb.values(), args.cpu_seconds)
+        gbs, elems, secs = oracle_throughput(x, dtype, cb.values(), args.cpu_seconds)
         cpu = {"value": round(gbs, 5), "unit": "GB/s", "cores": 1, "kind": "oracle",
-               "sample": "%d elements (first %d chunks of the workload), encode+decode, %.1f s, scalar C "
-                         "oracle, 1 thread" % (elems, elems // CHUNK, secs)}
+               "sample": "%d elements (the first %d chunks of the workload), encode+decode, %.1f s, scalar C "
+                         "oracle, 1 thread" % (elems, -(-elems // CHUNK), secs)}
 
     if rank != 0:
         return None
     return {
         "metric": METRIC, "value": round(value, 3), "unit": "GB/s", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "u16",
+        "scaling": "weak", "vs_baseline": None, "dtype": "u16" if dtype == 0 else "u8",
         "data": "synthetic (seeded torch CUDA generator; recipe of the workload module)",
-        "config": config_dict(world, args.layers),
+        "config": wl.config(world),
         "encode_gbs": round(enc_gbs, 2), "decode_gbs": round(dec_gbs, 2),
         "encode_hbm_frac": round(alg_encode / (enc_ms * 1e-3) / 1e9 / hbm, 4),
         "decode_hbm_frac": round(alg_decode / (dec_ms * 1e-3) / 1e9 / hbm, 4),
         "ratio": round(raw_bytes / blob_size, 5), "compressed_bytes": blob_size, "escapes": E,
-        "escape_rate": round(esc_rate, 6), "verified_bit_exact": verified,
+        "escape_rate": round(E / n, 6), "verified_bit_exact": verified,
         "per_kernel": per_kernel, "link_model": link,
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clk,
-        "gpu_launches": 2 * K,
+        "gpu_launches": 3 * K,
     }
 
 
