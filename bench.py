@@ -343,14 +343,14 @@ def run_ours(args, world, rank, local):
     value = all_bytes / (total_ms * 1e-3) / 1e9
 
     # ---- roofline of the dominant kernel (algorithmic bytes / event time) ----
-    # Each call is essentially one streaming kernel (encode adds a short finish
-    # kernel and a 4-byte memset, decode a 4-byte memset, inside the events).
+    # Each call is essentially one streaming kernel (encode adds two short
+    # kernels and two small memsets, decode a 4-byte memset, inside the events).
     peaks, peak_kind = measured_peaks()
     hbm = float(peaks["hbm_gbs"])
     alg_encode, alg_decode = wl.algorithmic_bytes(E)
     tag = "bf16" if dtype == 0 else "e5m2"
     if enc_ms >= dec_ms:
-        name, alg, ms = "encode_kernel<%s> (+ encode_finish_kernel)" % tag, alg_encode, enc_ms
+        name, alg, ms = "encode_kernel<%s> (+ index and record kernels)" % tag, alg_encode, enc_ms
     else:
         name, alg, ms = "decode_kernel<%s>" % tag, alg_decode, dec_ms
     achieved = alg / (ms * 1e-3) / 1e9
@@ -429,7 +429,7 @@ def run_ours(args, world, rank, local):
         "escape_rate": round(E / n, 6), "verified_bit_exact": verified,
         "per_kernel": per_kernel, "link_model": link,
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clk,
-        "gpu_launches": 3 * K,
+        "gpu_launches": 4 * K,  # encode: streaming, index, records kernels; decode: one kernel
     }
 
 

@@ -108,6 +108,7 @@ int prepare_encode(const void* d_in, uint64_t n, int dtype, const splitzip_codeb
     a->out = static_cast<uint8_t*>(d_out);
     a->group_totals = reinterpret_cast<uint32_t*>(ws + W->group_off);
     a->tile_counts = reinterpret_cast<uint32_t*>(ws + W->count_off);
+    a->tile_first = reinterpret_cast<uint64_t*>(ws + W->tile_off_off);
     a->staging = reinterpret_cast<uint32_t*>(ws + W->staging_off);
     a->out_size = d_out_size;
     a->error = d_status;

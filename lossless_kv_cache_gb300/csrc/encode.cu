@@ -16,11 +16,12 @@
 //     block scan orders the tile's escapes by element index and writes them
 //     to the tile's staging slot; the tile's count goes to the workspace and,
 //     by an integer atomic add, to its group's total.
-//   encode_finish_kernel (one CTA per group of 256 tiles): the sum of the
+//   encode_index_kernel (one CTA per group of 256 tiles): the sum of the
 //     earlier groups' totals plus a block scan of the group's tile counts give
-//     every tile's first record index; the CTA writes the index entries of the
-//     group's chunks and moves the staged records to the escape stream; the
-//     last group writes E and the container size.
+//     every tile's first record index; the CTA writes them and the index
+//     entries of the group's chunks; the last group writes E and the size.
+//   encode_records_kernel (a warp per 4 tiles): moves every tile's staged
+//     records to their place in the escape stream.
 #include <type_traits>
 
 #include "splitzip_internal.cuh"
@@ -389,8 +390,9 @@ __device__ __forceinline__ uint64_t warp_sum_u64(uint64_t v) {
 }
 
 // One CTA per group of kGroupTiles tiles (groups are chunk-aligned: tiles per
-// chunk is a power of two <= 8).
-__global__ void __launch_bounds__(kFinishThreads) encode_finish_kernel(const EncodeArgs a) {
+// chunk is a power of two <= 8): the first record index of every tile of the
+// group, the index entries of the group's chunks, and E from the last group.
+__global__ void __launch_bounds__(kFinishThreads) encode_index_kernel(const EncodeArgs a) {
     constexpr int kWarps = kFinishThreads / 32;
     __shared__ uint64_t warp_part[kWarps];
     __shared__ uint32_t warp_incl[kWarps];
@@ -426,36 +428,63 @@ __global__ void __launch_bounds__(kFinishThreads) encode_finish_kernel(const Enc
     tile_off[tid] = warp_before + incl - c;
     if (tid == 0) tile_off[kFinishThreads] = group_total;
     __syncthreads();
+    if (t < a.n_tiles) a.tile_first[t] = group_base + tile_off[tid];
 
-    const Layout L0 = layout_for(a.n, a.dtype, a.chunk_elems, 0);
     // index entries of the chunks that start in this group
+    const Layout L0 = layout_for(a.n, a.dtype, a.chunk_elems, 0);
     const uint32_t tpc = a.chunk_elems / a.tile_elems;
     if (t < a.n_tiles && t % tpc == 0) {
         const uint64_t chunk = t / tpc;
         reinterpret_cast<uint64_t*>(a.out + L0.index_off)[chunk] = group_base + tile_off[tid];
         reinterpret_cast<uint32_t*>(a.out + L0.counts_off)[chunk] = tile_off[tid + tpc] - tile_off[tid];
     }
-
-    // staged records -> 3-byte records in the escape stream (a warp per tile)
-    uint8_t* records = a.out + L0.escrec_off;
-    for (int k = warp; k < kFinishThreads; k += kWarps) {
-        const uint64_t tk = g * kGroupTiles + k;
-        if (tk >= a.n_tiles) break;
-        const uint32_t cnt = tile_off[k + 1] - tile_off[k];
-        const uint32_t* slot = a.staging + tk * a.tile_elems;
-        uint8_t* dst = records + 3 * (group_base + tile_off[k]);
-        for (uint32_t i = lane; i < cnt; i += 32) {
-            const uint32_t r = slot[i];
-            dst[3 * i] = uint8_t(r >> 8);
-            dst[3 * i + 1] = uint8_t(r >> 16);
-            dst[3 * i + 2] = uint8_t(r);
-        }
-    }
-
     if (g + 1 == a.n_groups && tid == 0) {  // the last group knows E
         const uint64_t E = group_base + group_total;
         reinterpret_cast<uint64_t*>(a.out)[3] = E;
         *a.out_size = layout_for(a.n, a.dtype, a.chunk_elems, E).size;
+    }
+}
+
+// Staged records -> 3-byte records in the escape stream.  Each warp serves
+// kRecordTiles consecutive tiles and interleaves them, so every lane keeps
+// kRecordTiles independent loads in flight per round.
+constexpr int kRecordTiles = 4;
+constexpr int kRecordThreads = 256;
+
+__global__ void __launch_bounds__(kRecordThreads) encode_records_kernel(const EncodeArgs a) {
+    const int lane = threadIdx.x & 31;
+    const uint64_t t0 = (uint64_t(blockIdx.x) * (kRecordThreads / 32) + (threadIdx.x >> 5)) * kRecordTiles;
+    if (t0 >= a.n_tiles) return;
+    uint64_t first = 0;
+    uint32_t cnt = 0;
+    if (lane < kRecordTiles && t0 + lane < a.n_tiles) {
+        first = a.tile_first[t0 + lane];
+        cnt = a.tile_counts[t0 + lane];
+    }
+    uint64_t f[kRecordTiles];
+    uint32_t c[kRecordTiles], most = 0;
+#pragma unroll
+    for (int k = 0; k < kRecordTiles; ++k) {
+        f[k] = __shfl_sync(kFull, first, k);
+        c[k] = __shfl_sync(kFull, cnt, k);
+        most = max(most, c[k]);
+    }
+    const Layout L0 = layout_for(a.n, a.dtype, a.chunk_elems, 0);
+    uint8_t* records = a.out + L0.escrec_off;
+    for (uint32_t i = lane; i < most; i += 32) {
+        uint32_t r[kRecordTiles];
+#pragma unroll
+        for (int k = 0; k < kRecordTiles; ++k)
+            r[k] = i < c[k] ? __ldcs(a.staging + (t0 + k) * a.tile_elems + i) : 0u;
+#pragma unroll
+        for (int k = 0; k < kRecordTiles; ++k) {
+            if (i < c[k]) {
+                uint8_t* d = records + 3 * (f[k] + i);
+                d[0] = uint8_t(r[k] >> 8);
+                d[1] = uint8_t(r[k] >> 16);
+                d[2] = uint8_t(r[k]);
+            }
+        }
     }
 }
 
@@ -468,7 +497,11 @@ cudaError_t launch_encode(const EncodeArgs& a, const EncodeLut& lut, int grid, c
         encode_kernel<SPLITZIP_FP8_E5M2><<<grid, kBlock, kEncodeSmem, s>>>(a, lut);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess || a.n_groups == 0) return e;
-    encode_finish_kernel<<<unsigned(a.n_groups), kFinishThreads, 0, s>>>(a);
+    encode_index_kernel<<<unsigned(a.n_groups), kFinishThreads, 0, s>>>(a);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    const uint64_t warps = (a.n_tiles + kRecordTiles - 1) / kRecordTiles;
+    encode_records_kernel<<<unsigned((warps + kRecordThreads / 32 - 1) / (kRecordThreads / 32)), kRecordThreads, 0,
+                            s>>>(a);
     return cudaGetLastError();
 }
 

@@ -52,9 +52,10 @@ __host__ __device__ inline uint32_t tile_elems_for(uint32_t chunk) {
     return chunk < kTileElems ? chunk : kTileElems;
 }
 
-// Encoder workspace: per-tile escape counts, per-group totals (a group is
-// kGroupTiles consecutive tiles), then one staging slot of tile_elems records
-// per tile; a record is (in-chunk position << 8) | exponent.  Only the group
+// Encoder workspace: per-group escape totals (a group is kGroupTiles
+// consecutive tiles), per-tile escape counts, per-tile first record indices,
+// then one staging slot of tile_elems records per tile; a record is
+// (in-chunk position << 8) | exponent.  Only the group
 // totals must be zero when the encode starts (`zero_bytes`); everything else
 // is written before it is read.
 constexpr uint32_t kGroupTiles = 256;
@@ -62,7 +63,7 @@ constexpr uint32_t kGroupTiles = 256;
 struct Workspace {
     uint64_t n_tiles, n_groups;
     uint32_t tile_elems;
-    uint64_t group_off, count_off, staging_off, zero_bytes, bytes;
+    uint64_t group_off, count_off, tile_off_off, staging_off, zero_bytes, bytes;
 };
 
 __host__ __device__ inline Workspace workspace_for(uint64_t n, uint32_t chunk) {
@@ -73,7 +74,8 @@ __host__ __device__ inline Workspace workspace_for(uint64_t n, uint32_t chunk) {
     W.group_off = 0;
     W.zero_bytes = align16(4u * W.n_groups);
     W.count_off = W.zero_bytes;
-    W.staging_off = align16(W.count_off + 4u * W.n_tiles);
+    W.tile_off_off = align16(W.count_off + 4u * W.n_tiles);
+    W.staging_off = align16(W.tile_off_off + 8u * W.n_tiles);
     W.bytes = W.staging_off + 4u * W.n_tiles * W.tile_elems;
     return W;
 }
@@ -88,6 +90,7 @@ struct EncodeArgs {
     uint8_t* out;            // container base
     uint32_t* group_totals;  // workspace, per group of kGroupTiles tiles
     uint32_t* tile_counts;   // workspace, per tile
+    uint64_t* tile_first;    // workspace, per tile: index of its first record
     uint32_t* staging;       // workspace, tile_elems records per tile
     uint64_t* out_size;
     int* error;              // device status word

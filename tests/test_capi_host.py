@@ -56,14 +56,16 @@ def test_sizes_match_oracle(splitzip_lib, dtype, chunk):
 
 
 def test_workspace_size(splitzip_lib):
-    # per-group totals, per-tile counts, then a staging slot of tile_elems
-    # 4-byte records per tile
+    # per-group totals, per-tile counts, per-tile first record indices, then a
+    # staging slot of tile_elems 4-byte records per tile
     a16 = lambda x: -(-x // 16) * 16
     n = 5 * 8192 + 3
     tiles = 6
-    assert sz.workspace_size(n, sz.BF16, 65536) == a16(a16(4) + 4 * tiles) + 4 * tiles * 8192
+    head = a16(a16(a16(4) + 4 * tiles) + 8 * tiles)
+    assert sz.workspace_size(n, sz.BF16, 65536) == head + 4 * tiles * 8192
     tiles = -(-n // 1024)  # tiles = chunks when chunks are smaller than 8192
-    assert sz.workspace_size(n, sz.BF16, 1024) == a16(a16(4) + 4 * tiles) + 4 * tiles * 1024
+    head = a16(a16(a16(4) + 4 * tiles) + 8 * tiles)
+    assert sz.workspace_size(n, sz.BF16, 1024) == head + 4 * tiles * 1024
     assert sz.workspace_size(0, sz.BF16, 65536) == 0
 
 
