@@ -125,6 +125,12 @@ constexpr uint32_t kNibCap = kSub / 2 + 32;  // + room for a 16-byte window shif
 constexpr uint32_t kSmCap = kSub + 32;
 constexpr uint32_t kStageBytes = (kNibCap + kSmCap + 127u) & ~127u;
 constexpr uint32_t kDecodeSmem = kStages * kStageBytes;
+// A chunk's escape records are brought into shared memory with one bulk copy
+// when they fit (at most kRecCap records, 1.2 % of a 65,536-element chunk), so
+// each sub-tile is patched right after its stores, while its lines are still
+// in L2; a chunk with more escapes is patched from global memory instead.
+constexpr uint32_t kRecCap = 768;
+constexpr uint32_t kRecBytes = 3 * kRecCap + 32;  // + room for a 16-byte window shift
 
 struct SubTile {
     Window nib, sm;
@@ -201,14 +207,37 @@ __device__ __forceinline__ void decode_subtile(const uint8_t* nb, const uint8_t*
     }
 }
 
+// Escape-record check and patch of one element (returns false on a corrupt
+// record).  `prev` is the previous record's position in the chunk (or -1).
+template <int DT>
+__device__ __forceinline__ bool patch_one(void* out, uint64_t base, uint32_t len, int64_t prev, uint32_t pos,
+                                          uint32_t ex) {
+    if (pos >= len || int64_t(pos) <= prev || ex >= (DT == SPLITZIP_BF16 ? 256u : 32u)) return false;
+    if constexpr (DT == SPLITZIP_BF16) {
+        uint16_t* o = static_cast<uint16_t*>(out) + base + pos;
+        *o = uint16_t((*o & 0x807Fu) | (ex << 7));
+    } else {
+        uint8_t* o = static_cast<uint8_t*>(out) + base + pos;
+        *o = uint8_t((*o & 0x83u) | (ex << 2));
+    }
+    return true;
+}
+
+__device__ __forceinline__ uint32_t rec_pos(const uint8_t* r) { return uint32_t(r[0]) | (uint32_t(r[1]) << 8); }
+
 template <int DT>
 __global__ void __launch_bounds__(kBlock) decode_kernel(const DecodeArgs a) {
     extern __shared__ __align__(128) uint8_t stages[];
     __shared__ __align__(8) uint64_t full_bar[kStages];
     __shared__ __align__(8) uint64_t empty_bar[kStages];
+    __shared__ __align__(8) uint64_t rec_full[2];
+    __shared__ __align__(8) uint64_t rec_empty[2];
+    __shared__ __align__(16) uint8_t rec_buf[2][kRecBytes];
+    __shared__ uint32_t rec_offset[2];  // window shift of the records in rec_buf, or kNoRecords
     __shared__ Header hdr;
     __shared__ int header_ok;
     __shared__ uint16_t lut2[256];  // nibble byte -> (exponent of low code) | (exponent of high code) << 8
+    constexpr uint32_t kNoRecords = 0xFFFFFFFFu;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     if (tid == 0) {
@@ -217,6 +246,10 @@ __global__ void __launch_bounds__(kBlock) decode_kernel(const DecodeArgs a) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&full_bar[s], 1);
             mbar_init(&empty_bar[s], kConsumerWarps);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&rec_full[b], 1);
+            mbar_init(&rec_empty[b], kConsumerWarps);
         }
         mbar_init_fence();
     }
@@ -230,16 +263,34 @@ __global__ void __launch_bounds__(kBlock) decode_kernel(const DecodeArgs a) {
     const Layout L = hdr.L;
     const uint8_t* nibbles = in + L.nibble_off;
     const uint8_t* signmant = in + L.signmant_off;
+    const uint64_t* offsets = reinterpret_cast<const uint64_t*>(in + L.index_off);
+    const uint32_t* counts = reinterpret_cast<const uint32_t*>(in + L.counts_off);
+    const uint8_t* records = in + L.escrec_off;  // 3 bytes each: position u16 LE, exponent
     const uint64_t chunk = hdr.chunk, C = hdr.n_chunks, E = hdr.E;
     const uint32_t sub = uint32_t(min(uint64_t(kSub), chunk));
 
     if (warp == kConsumerWarps) {
-        // ---- producer: one thread streams the sub-tiles into the stages ----
+        // ---- producer: per chunk its escape records (when they fit), then
+        // its sub-tiles, streamed into shared memory ----
         if (lane != 0) return;
-        uint32_t it = 0;
-        for (uint64_t c = blockIdx.x; c < C; c += gridDim.x) {
+        uint32_t it = 0, ci = 0;
+        for (uint64_t c = blockIdx.x; c < C; c += gridDim.x, ++ci) {
             const uint64_t base = c * chunk;
             const uint32_t len = uint32_t(min(chunk, a.n - base));
+            const uint32_t rb = ci & 1u;
+            if (ci >= 2 && !mbar_wait(&rec_empty[rb], ((ci >> 1) - 1) & 1u)) report(a.status, SPLITZIP_ERR_TIMEOUT);
+            const uint64_t off = offsets[c], cnt = counts[c];
+            // only a range that lies inside the escape stream is copied; the
+            // consumers check the index entry in full
+            if (cnt > 0 && cnt <= kRecCap && cnt <= len && off <= E && cnt <= E - off) {
+                const Window w = window_of(records + 3 * off, 3 * cnt);
+                rec_offset[rb] = w.offset;
+                mbar_arrive_expect_tx(&rec_full[rb], w.bytes);
+                bulk_load(rec_buf[rb], w.src, w.bytes, &rec_full[rb]);
+            } else {
+                rec_offset[rb] = cnt == 0 ? 0u : kNoRecords;
+                mbar_arrive(&rec_full[rb]);
+            }
             for (uint32_t s0 = 0; s0 < len; s0 += sub, ++it) {
                 const uint32_t stage = it % kStages, use = it / kStages;
                 if (use > 0 && !mbar_wait(&empty_bar[stage], (use - 1) & 1u)) report(a.status, SPLITZIP_ERR_TIMEOUT);
@@ -250,22 +301,30 @@ __global__ void __launch_bounds__(kBlock) decode_kernel(const DecodeArgs a) {
                 bulk_load(dst + kNibCap, t.sm.src, t.sm.bytes, &full_bar[stage]);
             }
         }
-        if (!drain_stages(full_bar, kStages, it)) report(a.status, SPLITZIP_ERR_TIMEOUT);
+        bool ok = drain_stages(full_bar, kStages, it);
+        ok &= drain_stages(rec_full, 2, ci);
+        if (!ok) report(a.status, SPLITZIP_ERR_TIMEOUT);
         return;
     }
 
-    // ---- consumers: dense decode per sub-tile, then the chunk's correction ----
-    const uint64_t* offsets = reinterpret_cast<const uint64_t*>(in + L.index_off);
-    const uint32_t* counts = reinterpret_cast<const uint32_t*>(in + L.counts_off);
-    const uint8_t* records = in + L.escrec_off;  // 3 bytes each: position u16 LE, exponent
-    uint32_t it = 0;
-    for (uint64_t c = blockIdx.x; c < C; c += gridDim.x) {
+    // ---- consumers: dense decode per sub-tile, each sub-tile patched right
+    // after its stores ----
+    uint32_t it = 0, ci = 0;
+    for (uint64_t c = blockIdx.x; c < C; c += gridDim.x, ++ci) {
         const uint64_t base = c * chunk;
         const uint32_t len = uint32_t(min(chunk, a.n - base));
-        // index entry of this chunk, fetched early so its latency overlaps the dense work
+        const uint32_t rb = ci & 1u;
         const uint64_t off = offsets[c];
         const uint64_t cnt = counts[c];
         const uint64_t expect_off = c == 0 ? 0 : offsets[c - 1] + counts[c - 1];
+        const bool index_ok = off == expect_off && cnt <= len && off <= E && cnt <= E - off &&
+                              (c + 1 < C || off + cnt == E);
+        if (!mbar_wait(&rec_full[rb], (ci >> 1) & 1u)) report(a.status, SPLITZIP_ERR_TIMEOUT);
+        const uint32_t shift = rec_offset[rb];
+        const bool in_smem = index_ok && shift != kNoRecords;  // the same in every consumer
+        const uint8_t* recs = rec_buf[rb] + (in_smem ? shift : 0u);
+        uint32_t cursor = 0;  // records of this chunk already applied
+        bool bad = false;
         for (uint32_t s0 = 0; s0 < len; s0 += sub, ++it) {
             const uint32_t stage = it % kStages, use = it / kStages;
             const uint32_t n_sub = min(sub, len - s0);
@@ -275,33 +334,37 @@ __global__ void __launch_bounds__(kBlock) decode_kernel(const DecodeArgs a) {
             decode_subtile<DT>(src + t.nib.offset, src + kNibCap + t.sm.offset, a.out, base + s0, n_sub, tid, lut2);
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty_bar[stage]);
+            if (!in_smem) continue;
+            // records are sorted, so this sub-tile's are the next ones with
+            // position < s0 + n_sub; the counting barrier also makes the
+            // sub-tile's stores visible to every consumer
+            while (true) {
+                const uint32_t i = cursor + tid;
+                const bool mine = i < cnt && rec_pos(recs + 3 * i) < s0 + n_sub;
+                const uint32_t n_in = named_barrier_popc(1, kConsumers, mine);
+                if (mine) {
+                    const int64_t prev = i == 0 ? -1 : int64_t(rec_pos(recs + 3 * (i - 1)));
+                    bad |= !patch_one<DT>(a.out, base, len, prev, rec_pos(recs + 3 * i), recs[3 * i + 2]);
+                }
+                cursor += n_in;
+                if (n_in < kConsumers) break;
+            }
         }
-        named_barrier(1, kConsumers);  // the chunk's dense writes are visible to all consumers
-
-        // ---- correction: escape records of this chunk ----
-        const bool index_ok = off == expect_off && cnt <= len && off <= E && cnt <= E - off &&
-                              (c + 1 < C || off + cnt == E);
+        if (in_smem && cursor != cnt) bad = true;  // a record outside the chunk or out of order
+        if (bad) report(a.status, SPLITZIP_ERR_CORRUPT);
         if (!index_ok) {
             if (tid == 0) report(a.status, SPLITZIP_ERR_CORRUPT);
-            continue;
-        }
-        for (uint64_t i = tid; i < cnt; i += kConsumers) {
-            const uint8_t* r = records + 3 * (off + i);
-            const uint32_t pos = uint32_t(r[0]) | (uint32_t(r[1]) << 8);
-            const uint32_t ex = r[2];
-            const bool ascending = i == 0 || (uint32_t(r[-3]) | (uint32_t(r[-2]) << 8)) < pos;
-            if (pos >= len || !ascending || ex >= (DT == SPLITZIP_BF16 ? 256u : 32u)) {
-                report(a.status, SPLITZIP_ERR_CORRUPT);
-                continue;
-            }
-            if constexpr (DT == SPLITZIP_BF16) {
-                uint16_t* o = static_cast<uint16_t*>(a.out) + base + pos;
-                *o = uint16_t((*o & 0x807Fu) | (ex << 7));
-            } else {
-                uint8_t* o = static_cast<uint8_t*>(a.out) + base + pos;
-                *o = uint8_t((*o & 0x83u) | (ex << 2));
+        } else if (!in_smem && cnt > 0) {
+            // too many escapes for shared memory: patch the chunk from global memory
+            named_barrier(1, kConsumers);  // the chunk's dense stores are visible to all consumers
+            for (uint64_t i = tid; i < cnt; i += kConsumers) {
+                const uint8_t* r = records + 3 * (off + i);
+                const int64_t prev = i == 0 ? -1 : int64_t(rec_pos(r - 3));
+                if (!patch_one<DT>(a.out, base, len, prev, rec_pos(r), r[2])) report(a.status, SPLITZIP_ERR_CORRUPT);
             }
         }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&rec_empty[rb]);
     }
 }
 

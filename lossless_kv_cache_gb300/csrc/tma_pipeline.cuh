@@ -91,6 +91,20 @@ __device__ __forceinline__ bool named_barrier_and(uint32_t id, uint32_t threads,
     return r != 0;
 }
 
+// Named barrier that also counts the participating threads whose predicate
+// is true (the same count in every participant).
+__device__ __forceinline__ uint32_t named_barrier_popc(uint32_t id, uint32_t threads, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "barrier.cta.red.popc.u32 %0, %2, %3, p;\n\t}"
+        : "=r"(r)
+        : "r"(uint32_t(pred)), "r"(id), "r"(threads)
+        : "memory");
+    return r;
+}
+
 // Before a producer thread leaves: wait (bounded) until the last bulk copy of
 // every stage has landed, so no copy is still writing into shared memory when
 // the CTA exits.  `issued` = number of stage uses so far.
