@@ -134,20 +134,23 @@ int splitzip_compressed_size(uint64_t n, int dtype, uint32_t chunk_elems, uint64
 int splitzip_max_compressed_size(uint64_t n, int dtype, uint32_t chunk_elems, uint64_t* out_bytes);
 
 /* Device scratch bytes splitzip_encode needs for n elements: about 4 bytes
- * per element (each tile of 8,192 elements, or each chunk when chunks are
- * smaller, has a staging slot big enough for all of its elements to escape)
- * plus 4 bytes per tile and per 256 tiles. */
+ * per element (each tile of 16 KB of input -- 8,192 BF16 or 16,384 E5M2
+ * elements -- or each chunk when chunks are smaller, has a staging slot big
+ * enough for all of its elements to escape) plus 40 bytes per tile and 4 per
+ * 256 tiles. */
 int splitzip_encode_workspace_size(uint64_t n, int dtype, uint32_t chunk_elems, uint64_t* out_bytes);
 
-/* Encode n elements (Method, "Encoding strategy").  Two kernels, no waits
+/* Encode n elements (Method, "Encoding strategy").  Four kernels, no waits
  * between blocks: a streaming pass that writes the nibble and sign|mantissa
- * streams and stages each tile's escape records in element order, then a
- * pass that computes the index (per-chunk offsets and counts) and moves the
- * records into the escape stream.
+ * streams and stages each tile's escape records in element order, a pass
+ * that totals the escapes of every 256 tiles, a pass that computes the index
+ * (per-chunk offsets and counts), and a pass that moves the records into the
+ * escape stream.  The input is read through a
+ * tensor map (cuTensorMapEncodeTiled, fetched from the runtime with
+ * cudaGetDriverEntryPointByVersion); SPLITZIP_ERR_CUDA if that fails.
  * d_in: n elements; cb: host codebook of the same dtype; d_out: container,
  * out_capacity >= splitzip_max_compressed_size; d_ws: ws_bytes >=
- * splitzip_encode_workspace_size, contents need not be initialised (the call
- * clears what must start at zero); d_out_size: device u64 that receives the
+ * splitzip_encode_workspace_size, contents need not be initialised; d_out_size: device u64 that receives the
  * container size; d_status: device int, cleared by the call; it becomes
  * SPLITZIP_ERR_TIMEOUT only if a bounded wait on a bulk copy ran out (not
  * expected).  n = 0 is valid and gives a 64-byte container.  Calls that share
@@ -167,8 +170,8 @@ int splitzip_encode(const void* d_in, uint64_t n, int dtype, const splitzip_code
  * Its scratch is a fixed device array of SPLITZIP_NOALLOC_SCRATCH_BYTES
  * (32 MiB) held by every GPU that loads this library until the process
  * exits.  Limits: n must satisfy splitzip_encode_workspace_size(n, dtype,
- * chunk_elems) <= SPLITZIP_NOALLOC_SCRATCH_BYTES (8,380,416 elements at the
- * default chunk size); larger n returns SPLITZIP_ERR_CAPACITY before any GPU
+ * chunk_elems) <= SPLITZIP_NOALLOC_SCRATCH_BYTES (8,372,224 elements at the
+ * default chunk size, for either dtype); larger n returns SPLITZIP_ERR_CAPACITY before any GPU
  * work.  The call allocates nothing: the caller still passes input, output,
  * d_out_size and d_status exactly as for splitzip_encode, and the output is
  * byte-identical to splitzip_encode's.  The first call on each device looks up

@@ -5,6 +5,8 @@
 #include <cstring>
 #include <mutex>
 
+#include <cudaTypedefs.h>  // PFN_cuTensorMapEncodeTiled
+
 #include "splitzip_internal.cuh"
 
 using namespace splitzip;
@@ -98,7 +100,7 @@ int prepare_encode(const void* d_in, uint64_t n, int dtype, const splitzip_codeb
     if (!d_out_size || !aligned(d_out_size, 8) || !d_status || !aligned(d_status, 4))
         return SPLITZIP_ERR_INVALID_ARG;
     if (out_capacity < layout_for(n, dtype, chunk, n).size) return SPLITZIP_ERR_CAPACITY;
-    *W = workspace_for(n, chunk);
+    *W = workspace_for(n, dtype, chunk);
     if (ws_bytes < W->bytes) return SPLITZIP_ERR_CAPACITY;
     if (W->bytes > 0 && (!d_ws || !aligned(d_ws, 16))) return SPLITZIP_ERR_INVALID_ARG;
 
@@ -107,18 +109,70 @@ int prepare_encode(const void* d_in, uint64_t n, int dtype, const splitzip_codeb
     a->n = n;
     a->out = static_cast<uint8_t*>(d_out);
     a->group_totals = reinterpret_cast<uint32_t*>(ws + W->group_off);
-    a->tile_counts = reinterpret_cast<uint32_t*>(ws + W->count_off);
-    a->tile_first = reinterpret_cast<uint64_t*>(ws + W->tile_off_off);
+    a->warp_counts = reinterpret_cast<uint32_t*>(ws + W->warp_count_off);
+    a->tile_first = reinterpret_cast<uint64_t*>(ws + W->tile_first_off);
     a->staging = reinterpret_cast<uint32_t*>(ws + W->staging_off);
     a->out_size = d_out_size;
     a->error = d_status;
     a->n_tiles = W->n_tiles;
     a->n_groups = W->n_groups;
     a->tile_elems = W->tile_elems;
+    a->region_elems = W->region_elems;
     a->chunk_elems = chunk;
     a->n_chunks = layout_for(n, dtype, chunk, 0).n_chunks;
     a->dtype = dtype;
     std::memcpy(a->codebook, cb->exps, 16);
+    a->tensor_bytes = 0;
+    a->box_bytes = 0;
+    return SPLITZIP_OK;
+}
+
+// The driver's tensor-map encoder, fetched once through the runtime (the
+// library does not link the driver library itself).
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+        else
+            cudaGetLastError();
+    });
+    return fn;
+}
+
+// Tensor map of the encoder's input: a 2-D tensor of 128-byte rows (the
+// input's whole rows; its last partial row, if any, is read by the consumers
+// directly), one box = one tile.  Tiles of 128 bytes and more are copied with
+// the 128-byte swizzle; the only smaller tile (E5M2 with 64-element chunks,
+// 64 bytes) fits in one row and is copied unswizzled.  Row coordinates are
+// 32-bit signed, so at most 2^31 - 256 rows are mapped; bytes past them are
+// also read directly.
+int make_input_map(const void* d_in, int dtype, EncodeArgs* a, CUtensorMap* map) {
+    std::memset(map, 0, sizeof(*map));
+    const uint64_t eb = elem_bytes(dtype);
+    const uint64_t rows = std::min<uint64_t>(a->n * eb / 128u, (uint64_t(1) << 31) - 256u);
+    if (rows == 0) return SPLITZIP_OK;  // every byte is read directly
+    PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
+    if (!encode) return SPLITZIP_ERR_CUDA;
+    const uint32_t tile_bytes = a->tile_elems * uint32_t(eb);
+    const uint32_t box_row_bytes = std::min<uint32_t>(tile_bytes, 128u);
+    const cuuint64_t dims[2] = {128u / eb, rows};
+    const cuuint64_t strides[1] = {128u};
+    const cuuint32_t box[2] = {cuuint32_t(box_row_bytes / eb), cuuint32_t(tile_bytes / box_row_bytes)};
+    const cuuint32_t elem_strides[2] = {1u, 1u};
+    const CUresult r =
+        encode(map, dtype == SPLITZIP_BF16 ? CU_TENSOR_MAP_DATA_TYPE_UINT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 2,
+               const_cast<void*>(d_in), dims, strides, box, elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               box_row_bytes == 128u ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return SPLITZIP_ERR_CUDA;
+    a->tensor_bytes = rows * 128u;
+    a->box_bytes = tile_bytes;
     return SPLITZIP_OK;
 }
 
@@ -156,7 +210,7 @@ int splitzip_encode_workspace_size(uint64_t n, int dtype, uint32_t chunk_elems, 
     int st = check_geometry(n, dtype, chunk_elems);
     if (st != SPLITZIP_OK) return st;
     if (!out_bytes) return SPLITZIP_ERR_INVALID_ARG;
-    *out_bytes = workspace_for(n, chunk_elems).bytes;
+    *out_bytes = workspace_for(n, dtype, chunk_elems).bytes;
     return SPLITZIP_OK;
 }
 
@@ -215,18 +269,18 @@ int splitzip_encode(const void* d_in, uint64_t n, int dtype, const splitzip_code
     if (st != SPLITZIP_OK) return st;
     DeviceState d;
     if ((st = device_state(&d)) != SPLITZIP_OK) return st;
+    CUtensorMap map;
+    if ((st = make_input_map(d_in, dtype, &a, &map)) != SPLITZIP_OK) return st;
     EncodeLut lut;
     std::memset(lut.code, kEscapeFlag, sizeof(lut.code));
     for (int k = 0; k < 16; ++k) lut.code[cb->exps[k]] = uint8_t(k);
-    // the per-group escape totals are accumulated with atomic adds, and errors
-    // are recorded into the status word with compare-and-swap: both start at 0
-    if ((W.zero_bytes > 0 && cudaMemsetAsync(d_ws, 0, W.zero_bytes, stream) != cudaSuccess) ||
-        cudaMemsetAsync(d_status, 0, sizeof(int), stream) != cudaSuccess) {
+    // errors are recorded into the status word with compare-and-swap
+    if (cudaMemsetAsync(d_status, 0, sizeof(int), stream) != cudaSuccess) {
         cudaGetLastError();
         return SPLITZIP_ERR_CUDA;
     }
     const int grid = grid_for(a.n_tiles, d.sms, d.encode_bpsm[dtype]);
-    return launch_encode(a, lut, grid, stream) == cudaSuccess ? SPLITZIP_OK : SPLITZIP_ERR_CUDA;
+    return launch_encode(a, lut, map, grid, stream) == cudaSuccess ? SPLITZIP_OK : SPLITZIP_ERR_CUDA;
 }
 
 int splitzip_decode(const void* d_in, uint64_t in_bytes, void* d_out, uint64_t n, int dtype, int* d_status,

@@ -7,15 +7,20 @@
 // ("Sign/mantissa preservation"); an exponent outside the codebook becomes a
 // (16-bit position, 8-bit exponent) escape record ("Escape stream").
 //
-// Two kernels, no inter-block waits:
+// Four kernels, no inter-block waits:
 //   encode_kernel (the streaming pass, persistent CTAs of 8 consumer warps +
-//     1 producer warp): the producer streams each of the CTA's tiles into a
-//     4-stage shared-memory ring with bulk copies (TMA, cp.async.bulk +
-//     mbarrier); consumers split, code and pack the tile from shared memory
-//     and write the nibble and sign|mantissa streams with coalesced stores; a
-//     block scan orders the tile's escapes by element index and writes them
-//     to the tile's staging slot; the tile's count goes to the workspace and,
-//     by an integer atomic add, to its group's total.
+//     1 producer warp): the producer streams each of the CTA's 16 KB tiles
+//     into a 4-stage shared-memory ring with tensor-map copies (TMA,
+//     cp.async.bulk.tensor, 128-byte swizzle, mbarrier); every consumer
+//     thread owns 64 contiguous bytes of the tile.  Per element it does one
+//     shared-memory lookup in a table for the element's position within its
+//     group of four; the table entries already sit at their final bit
+//     positions, so the sum of four entries is the group's two nibble bytes,
+//     its escape flags and (E5M2) its packed 3-bit sign|mantissa values.  The
+//     nibble and sign|mantissa streams go out with 16-byte stores; a warp scan
+//     orders the warp's escapes and the warp stages them in the tile's slot;
+//     the warp's count goes to the workspace.
+//   encode_group_kernel (one CTA per group of 256 tiles): the group's total.
 //   encode_index_kernel (one CTA per group of 256 tiles): the sum of the
 //     earlier groups' totals plus a block scan of the group's tile counts give
 //     every tile's first record index; the CTA writes them and the index
@@ -31,101 +36,65 @@ namespace splitzip {
 namespace {
 
 constexpr uint32_t kFull = 0xFFFFFFFFu;
-constexpr int kConsumerWarps = 8;
+constexpr int kConsumerWarps = int(kEncodeWarps);
 constexpr int kConsumers = kConsumerWarps * 32;
 constexpr int kBlock = kConsumers + 32;  // + one producer warp
 constexpr int kStages = 4;
-constexpr uint32_t kStageBytes = kTileElems * 2;  // one BF16 tile
-constexpr uint32_t kEncodeSmem = kStages * kStageBytes;
+constexpr uint32_t kStageBytes = kTileBytes;
+// + room to align the ring to 1024 bytes, which the 128-byte swizzle needs
+constexpr uint32_t kEncodeSmem = kStages * kStageBytes + 1024;
 constexpr int kFinishThreads = kGroupTiles;  // one thread per tile of the group
+static_assert(kConsumers * kThreadBytes == kTileBytes, "one tile = 64 bytes per consumer thread");
 
-// Units: BF16 8 elements, E5M2 16 elements (16 bytes either way).  Thread t
-// handles units j * 256 + t of a tile, so each warp reads 512 contiguous bytes.
-template <int DT> struct Geometry;
-template <> struct Geometry<SPLITZIP_BF16> {
-    static constexpr int kElemBytes = 2, kUnitElems = 8, kUnitsPerThread = 4;
-};
-template <> struct Geometry<SPLITZIP_FP8_E5M2> {
-    static constexpr int kElemBytes = 1, kUnitElems = 16, kUnitsPerThread = 2;
-};
-static_assert(kConsumers * 8 * 4 == kTileElems, "BF16 tile");
-static_assert(kConsumers * 16 * 2 == kTileElems, "E5M2 tile");
+// Position table entries (four tables, one per position k = 0..3 of an
+// element within its group of four consecutive elements):
+//   bits 16 + 4k .. 19 + 4k  the element's code (0 when it escapes)
+//   bit  12 + k              the element's escape flag
+//   bits 3k .. 3k + 2        E5M2 only: the element's 3-bit sign|mantissa
+// The four entries of a group have disjoint bits, so their sum is the group's
+// two nibble bytes (bits 16..31, even element in the low nibble), its escape
+// mask (bits 12..15) and its 12 bits of packed sign|mantissa (bits 0..11).
+__device__ __forceinline__ uint32_t table_entry(int dtype, int k, uint32_t index, const uint8_t* code) {
+    uint32_t e = index, s3 = 0;
+    if (dtype != SPLITZIP_BF16) {  // index = the whole E5M2 byte
+        e = (index >> 2) & 31u;
+        s3 = ((index >> 7) << 2) | (index & 3u);
+    }
+    const uint32_t t = code[e];
+    const uint32_t c = (t & kEscapeFlag) ? (1u << (12 + k)) : (uint32_t(t & 15u) << (16 + 4 * k));
+    return c | (s3 << (3 * k));
+}
 
-// Load `nbytes` (< 16) bytes into a zero-filled vector (only the final unit
-// of a tensor is partial).
-__device__ __forceinline__ uint4 load_partial(const uint8_t* p, int nbytes) {
+// Entry of table k at byte offset `off` (index * 4).
+__device__ __forceinline__ uint32_t tab_at(const uint32_t* tab, int k, uint32_t off) {
+    return *reinterpret_cast<const uint32_t*>(reinterpret_cast<const uint8_t*>(tab + 256 * k) + off);
+}
+
+// BF16: the group of four elements in words x (elements 0, 1) and y (2, 3);
+// the table index is the exponent (bits 7..14 of each 16-bit element).
+__device__ __forceinline__ uint32_t group_bf16(const uint32_t* tab, uint32_t x, uint32_t y) {
+    return tab_at(tab, 0, (x >> 5) & 0x3FCu) + tab_at(tab, 1, (x >> 21) & 0x3FCu) +
+           tab_at(tab, 2, (y >> 5) & 0x3FCu) + tab_at(tab, 3, (y >> 21) & 0x3FCu);
+}
+
+// E5M2: the group of four elements in word w; the table index is the byte.
+__device__ __forceinline__ uint32_t group_e5m2(const uint32_t* tab, uint32_t w) {
+    return tab_at(tab, 0, (w << 2) & 0x3FCu) + tab_at(tab, 1, (w >> 6) & 0x3FCu) +
+           tab_at(tab, 2, (w >> 14) & 0x3FCu) + tab_at(tab, 3, (w >> 22) & 0x3FCu);
+}
+
+// Stage position of byte L of a tile: the tensor-map copy stores every
+// 128-byte row r with its 16-byte pieces permuted by XOR with (r mod 8).
+__device__ __forceinline__ uint32_t swizzled(uint32_t L) { return L ^ (((L >> 7) & 7u) << 4); }
+
+// Load `nbytes` (< 16) bytes into a zero-filled vector (only the last bytes
+// of a tensor are not covered by whole rows of the tensor map).
+__device__ __forceinline__ uint4 load_partial(const uint8_t* p, uint32_t nbytes) {
     uint32_t w[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
-    for (int i = 0; i < 16; ++i)
+    for (uint32_t i = 0; i < 16; ++i)
         if (i < nbytes) w[i >> 2] |= uint32_t(p[i]) << (8 * (i & 3));
     return make_uint4(w[0], w[1], w[2], w[3]);
-}
-
-// Four table entries (code | escape flag) for the four exponent bytes of `e`.
-__device__ __forceinline__ uint32_t lookup4(const uint8_t* lut, uint32_t e) {
-    return uint32_t(lut[e & 0xFFu]) | (uint32_t(lut[(e >> 8) & 0xFFu]) << 8) |
-           (uint32_t(lut[(e >> 16) & 0xFFu]) << 16) | (uint32_t(lut[e >> 24]) << 24);
-}
-
-// Escape flags of four table entries -> 4-bit mask (bit k = byte k).
-__device__ __forceinline__ uint32_t escape_bits4(uint32_t t) {
-    const uint32_t f = (t >> 4) & 0x01010101u;
-    return (f * 0x01020408u) >> 24;
-}
-
-// Two words of four codes each (low nibble of every byte) -> the 8 codes
-// packed two per byte, even element in the low nibble.
-__device__ __forceinline__ uint32_t pack_nibbles8(uint32_t t0, uint32_t t1) {
-    const uint32_t k0 = t0 & 0x0F0F0F0Fu, k1 = t1 & 0x0F0F0F0Fu;
-    return __byte_perm(k0 | (k0 >> 4), k1 | (k1 >> 4), 0x6420);
-}
-
-// One BF16 unit: 8 elements in v -> 8 nibbles, 8 sign|mantissa bytes, the
-// escape mask and the 8 exponents (kept for the escape records).
-__device__ __forceinline__ void encode_unit_bf16(const uint4 v, const uint8_t* lut, uint32_t& nib,
-                                                 uint2& sm, uint32_t& esc, uint32_t& e0, uint32_t& e1) {
-    const uint32_t lo0 = __byte_perm(v.x, v.y, 0x6420);  // low bytes of elements 0..3
-    const uint32_t hi0 = __byte_perm(v.x, v.y, 0x7531);  // high bytes of elements 0..3
-    const uint32_t lo1 = __byte_perm(v.z, v.w, 0x6420);
-    const uint32_t hi1 = __byte_perm(v.z, v.w, 0x7531);
-    // sign (bit 7 of the high byte) | mantissa (bits 6..0 of the low byte)
-    sm.x = (hi0 & 0x80808080u) | (lo0 & 0x7F7F7F7Fu);
-    sm.y = (hi1 & 0x80808080u) | (lo1 & 0x7F7F7F7Fu);
-    // exponent = high byte bits 6..0 then low byte bit 7
-    e0 = ((hi0 << 1) & 0xFEFEFEFEu) | ((lo0 >> 7) & 0x01010101u);
-    e1 = ((hi1 << 1) & 0xFEFEFEFEu) | ((lo1 >> 7) & 0x01010101u);
-    const uint32_t t0 = lookup4(lut, e0), t1 = lookup4(lut, e1);
-    esc = escape_bits4(t0) | (escape_bits4(t1) << 4);
-    nib = pack_nibbles8(t0, t1);
-}
-
-// Four E5M2 bytes -> their 3-bit sign|mantissa values packed LSB-first into
-// 12 bits: s3 = (sign << 2) | mantissa2.
-__device__ __forceinline__ uint32_t pack_s3x4(uint32_t w) {
-    const uint32_t s = ((w >> 5) & 0x04040404u) | (w & 0x03030303u);
-    const uint32_t x = s | (s >> 5);            // byte0: s0 | s1<<3, byte2: s2 | s3<<3
-    return (x & 0x3Fu) | ((x >> 10) & 0xFC0u);  // 12 bits
-}
-
-// One E5M2 unit: 16 elements -> 16 nibbles (uint2), 6 bytes of s3 (lo32 +
-// hi16), the escape mask and the exponents.
-__device__ __forceinline__ void encode_unit_e5m2(const uint4 v, const uint8_t* lut, uint2& nib,
-                                                 uint32_t& s3lo, uint32_t& s3hi, uint32_t& esc,
-                                                 uint32_t (&e)[4]) {
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-    uint32_t t[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        e[i] = (w[i] >> 2) & 0x1F1F1F1Fu;
-        t[i] = lookup4(lut, e[i]);
-    }
-    esc = escape_bits4(t[0]) | (escape_bits4(t[1]) << 4) | (escape_bits4(t[2]) << 8) |
-          (escape_bits4(t[3]) << 12);
-    nib.x = pack_nibbles8(t[0], t[1]);
-    nib.y = pack_nibbles8(t[2], t[3]);
-    const uint32_t g0 = pack_s3x4(w[0]), g1 = pack_s3x4(w[1]), g2 = pack_s3x4(w[2]), g3 = pack_s3x4(w[3]);
-    s3lo = g0 | (g1 << 12) | (g2 << 24);
-    s3hi = (g2 >> 8) | (g3 << 4);
 }
 
 // Header fields known before any tile is encoded (E is written at the end),
@@ -157,20 +126,74 @@ __device__ void write_header_and_padding(const EncodeArgs& a) {
 
 __device__ __forceinline__ void report(int* status, int code) { atomicCAS(status, SPLITZIP_OK, code); }
 
+// Per-thread results of one tile: BF16 32 elements, E5M2 64 elements.
+template <int DT> struct ThreadOut;
+template <> struct ThreadOut<SPLITZIP_BF16> {
+    static constexpr uint32_t kElems = 32;
+    uint32_t nib[4];  // 16 nibble bytes
+    uint32_t sm[8];   // 32 sign|mantissa bytes
+    uint32_t mask;    // escape flags, bit b = element b
+};
+template <> struct ThreadOut<SPLITZIP_FP8_E5M2> {
+    static constexpr uint32_t kElems = 64;
+    uint32_t nib[8];  // 32 nibble bytes
+    uint32_t s3[6];   // 24 bytes of packed 3-bit sign|mantissa
+    uint32_t mask[2];
+};
+
+// One 16-byte piece (BF16: 8 elements) into slot i of the thread's results.
+__device__ __forceinline__ void encode_piece(const uint32_t* tab, uint4 v, int i, ThreadOut<SPLITZIP_BF16>& o) {
+    const uint32_t s0 = group_bf16(tab, v.x, v.y), s1 = group_bf16(tab, v.z, v.w);
+    o.nib[i] = __byte_perm(s0, s1, 0x7632);
+    o.mask |= (((s0 >> 12) & 0xFu) | ((s1 >> 8) & 0xF0u)) << (8 * i);
+    // sign (bit 7 of the high byte) | mantissa (bits 6..0 of the low byte)
+    const uint32_t lo0 = __byte_perm(v.x, v.y, 0x6420), hi0 = __byte_perm(v.x, v.y, 0x7531);
+    const uint32_t lo1 = __byte_perm(v.z, v.w, 0x6420), hi1 = __byte_perm(v.z, v.w, 0x7531);
+    o.sm[2 * i] = (hi0 & 0x80808080u) | (lo0 & 0x7F7F7F7Fu);
+    o.sm[2 * i + 1] = (hi1 & 0x80808080u) | (lo1 & 0x7F7F7F7Fu);
+}
+
+// One 16-byte piece (E5M2: 16 elements); the packed sign|mantissa of the
+// piece (48 bits) is left in p[2i], p[2i+1] (24 bits each).
+__device__ __forceinline__ void encode_piece(const uint32_t* tab, uint4 v, int i, ThreadOut<SPLITZIP_FP8_E5M2>& o,
+                                             uint32_t* p) {
+    const uint32_t s0 = group_e5m2(tab, v.x), s1 = group_e5m2(tab, v.y);
+    const uint32_t s2 = group_e5m2(tab, v.z), s3 = group_e5m2(tab, v.w);
+    o.nib[2 * i] = __byte_perm(s0, s1, 0x7632);
+    o.nib[2 * i + 1] = __byte_perm(s2, s3, 0x7632);
+    const uint32_t f = ((s0 >> 12) & 0xFu) | ((s1 >> 8) & 0xF0u) | ((s2 >> 4) & 0xF00u) | (s3 & 0xF000u);
+    o.mask[i >> 1] |= f << (16 * (i & 1));
+    p[2 * i] = (s0 & 0xFFFu) | ((s1 & 0xFFFu) << 12);
+    p[2 * i + 1] = (s2 & 0xFFFu) | ((s3 & 0xFFFu) << 12);
+}
+
+// Eight 24-bit groups -> 24 bytes of the 3-bit stream.
+__device__ __forceinline__ void pack_s3_stream(const uint32_t* p, uint32_t* out) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const uint32_t* q = p + 4 * h;
+        out[3 * h] = q[0] | (q[1] << 24);
+        out[3 * h + 1] = (q[1] >> 8) | (q[2] << 16);
+        out[3 * h + 2] = (q[2] >> 16) | (q[3] << 8);
+    }
+}
+
 template <int DT>
-__global__ void __launch_bounds__(kBlock, 3) encode_kernel(const EncodeArgs a, const EncodeLut lut_in) {
-    using G = Geometry<DT>;
-    constexpr int J = G::kUnitsPerThread;
-    constexpr int kWords = (J + 1) / 2;  // per-thread counts as 16-bit fields, two per word
-    extern __shared__ __align__(128) uint8_t stages[];
+__global__ void __launch_bounds__(kBlock, 3)
+    encode_kernel(const __grid_constant__ EncodeArgs a, const __grid_constant__ CUtensorMap map,
+                  const __grid_constant__ EncodeLut lut) {
+    constexpr uint32_t EB = DT == SPLITZIP_BF16 ? 2u : 1u;
+    using Out = ThreadOut<DT>;
+    constexpr uint32_t TE = Out::kElems;  // elements per consumer thread per tile
+    extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t full_bar[kStages];
     __shared__ __align__(8) uint64_t empty_bar[kStages];
-    __shared__ uint8_t lut[256];
-    __shared__ uint32_t warp_sums[2][kConsumerWarps][kWords];
-    __shared__ __align__(16) uint8_t s3_stage[kConsumerWarps][192];
+    __shared__ __align__(16) uint32_t tab[4 * 256];
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    for (int i = tid; i < 256; i += kBlock) lut[i] = lut_in.code[i];
+    // the ring starts on a 1024-byte boundary of the shared window
+    uint8_t* ring = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    for (int i = tid; i < 4 * 256; i += kBlock) tab[i] = table_entry(DT, i >> 8, uint32_t(i & 255), lut.code);
     if (tid == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&full_bar[s], 1);
@@ -182,6 +205,7 @@ __global__ void __launch_bounds__(kBlock, 3) encode_kernel(const EncodeArgs a, c
     __syncthreads();
 
     const uint8_t* in = static_cast<const uint8_t*>(a.in);
+    const uint32_t tile_bytes = a.tile_elems * EB;
     if (warp == kConsumerWarps) {
         // ---- producer: stream the CTA's tiles (blockIdx.x + k * gridDim.x) ----
         if (lane != 0) return;
@@ -189,197 +213,167 @@ __global__ void __launch_bounds__(kBlock, 3) encode_kernel(const EncodeArgs a, c
         for (uint64_t t = blockIdx.x; t < a.n_tiles; t += gridDim.x, ++it) {
             const uint32_t stage = it % kStages, use = it / kStages;
             if (use > 0 && !mbar_wait(&empty_bar[stage], (use - 1) & 1u)) report(a.error, SPLITZIP_ERR_TIMEOUT);
-            const uint64_t base = t * a.tile_elems;
-            const uint64_t len = min(uint64_t(a.tile_elems), a.n - base);
-            // whole 16-byte units only: the input has no padding after element n-1
-            const uint32_t bytes = uint32_t(len * G::kElemBytes) & ~15u;
-            mbar_arrive_expect_tx(&full_bar[stage], bytes);
-            if (bytes) bulk_load(stages + stage * kStageBytes, in + base * G::kElemBytes, bytes, &full_bar[stage]);
+            const uint64_t tb = t * tile_bytes;
+            if (tb < a.tensor_bytes) {
+                mbar_arrive_expect_tx(&full_bar[stage], a.box_bytes);
+                tensor_load_2d(ring + stage * kStageBytes, &map, int32_t((tb & 127u) / EB), int32_t(tb >> 7),
+                               &full_bar[stage]);
+            } else {
+                mbar_arrive(&full_bar[stage]);  // the consumers read this tile from global memory
+            }
         }
         if (!drain_stages(full_bar, kStages, it)) report(a.error, SPLITZIP_ERR_TIMEOUT);
         return;
     }
 
-    // ---- consumers ----
+    // ---- consumers: thread `tid` owns bytes [64 tid, 64 tid + 64) of a tile ----
     const Layout L0 = layout_for(a.n, a.dtype, a.chunk_elems, 0);
     uint8_t* nibbles = a.out + L0.nibble_off;
     uint8_t* signmant = a.out + L0.signmant_off;
+    const uint32_t my_byte = kThreadBytes * uint32_t(tid);
+    const uint32_t my_elem = my_byte / EB;  // first element of the thread in a tile
+    uint32_t piece_off[4];                  // stage offsets of the thread's four 16-byte pieces
+#pragma unroll
+    for (int i = 0; i < 4; ++i) piece_off[i] = swizzled(my_byte + 16u * i);
 
     uint32_t it = 0;
     for (uint64_t tile = blockIdx.x; tile < a.n_tiles; tile += gridDim.x, ++it) {
-        const uint32_t stage = it % kStages, use = it / kStages, parity = it & 1u;
+        const uint32_t stage = it % kStages, use = it / kStages;
         // on a time-out the tile is processed anyway (its addresses do not
-        // depend on the data), so every consumer still meets every barrier
+        // depend on the data), so every consumer still reaches every barrier
         if (!mbar_wait(&full_bar[stage], use & 1u)) report(a.error, SPLITZIP_ERR_TIMEOUT);
         const uint64_t base = tile * a.tile_elems;
         const uint64_t rem = a.n - base;
-        const uint32_t len_rt = rem < a.tile_elems ? uint32_t(rem) : a.tile_elems;
+        const uint32_t len = rem < a.tile_elems ? uint32_t(rem) : a.tile_elems;
+        const uint64_t tb = base * EB;
+        // bytes of this tile that the tensor-map copy delivered
+        const uint32_t in_stage =
+            tb >= a.tensor_bytes ? 0u : uint32_t(min(uint64_t(tile_bytes), a.tensor_bytes - tb));
         const uint32_t pos0 = uint32_t(base & (a.chunk_elems - 1u));  // in-chunk position of element 0
-        const uint8_t* tile_smem = stages + stage * kStageBytes;
+        const uint8_t* st = ring + stage * kStageBytes;
 
-        // Full 8192-element tiles take a copy of the body in which every
-        // bounds test folds away at compile time.
+        // Full-size tiles delivered whole take a copy of the body in which
+        // every bounds test folds away at compile time; in the other copy each
+        // thread handles only its `ne` elements of the tile.
         auto body = [&](auto full_tag) {
             constexpr bool FULL = decltype(full_tag)::value;
-            const uint32_t len = FULL ? kTileElems : len_rt;
-
-            uint4 v[J];
+            // elements of this thread in the tile (all TE of them in a full tile)
+            const uint32_t ne = FULL ? TE : (len > my_elem ? min(len - my_elem, TE) : 0u);
+            Out o;
+            [[maybe_unused]] uint32_t p[8];  // E5M2 packed sign|mantissa groups
+            if constexpr (DT == SPLITZIP_BF16)
+                o.mask = 0u;
+            else
+                o.mask[0] = o.mask[1] = 0u;
 #pragma unroll
-            for (int j = 0; j < J; ++j) {
-                const uint32_t e = (uint32_t(j) * kConsumers + tid) * G::kUnitElems;
-                if (e + G::kUnitElems <= len)
-                    v[j] = *reinterpret_cast<const uint4*>(tile_smem + e * G::kElemBytes);
-                else if (e < len)  // the tensor's final bytes were not bulk-copied
-                    v[j] = load_partial(in + (base + e) * G::kElemBytes, int(len - e) * G::kElemBytes);
+            for (int i = 0; i < 4; ++i) {
+                uint4 v;
+                const uint32_t L = my_byte + 16u * i;
+                if (FULL || L + 16u <= in_stage)
+                    v = *reinterpret_cast<const uint4*>(st + piece_off[i]);
+                else if (L < len * EB)  // past the tensor map's whole rows: read global memory
+                    v = load_partial(in + tb + L, min(16u, len * EB - L));
                 else
-                    v[j] = make_uint4(0u, 0u, 0u, 0u);
+                    v = make_uint4(0u, 0u, 0u, 0u);
+                if constexpr (DT == SPLITZIP_BF16)
+                    encode_piece(tab, v, i, o);
+                else
+                    encode_piece(tab, v, i, o, p);
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&empty_bar[stage]);  // the stage may be refilled
 
-            uint32_t esc[J];
-            uint32_t ex[J][4];  // exponents of each unit (BF16 uses [0..1])
-            uint32_t cnt[kWords];
-#pragma unroll
-            for (int j = 0; j < J; ++j) ex[j][2] = ex[j][3] = 0u;
-#pragma unroll
-            for (int k = 0; k < kWords; ++k) cnt[k] = 0;
-
-#pragma unroll
-            for (int j = 0; j < J; ++j) {
-                const uint32_t e = (uint32_t(j) * kConsumers + tid) * G::kUnitElems;
-                const uint32_t valid = e < len ? min(len - e, uint32_t(G::kUnitElems)) : 0u;
-                if constexpr (DT == SPLITZIP_BF16) {
-                    uint32_t nib;
-                    uint2 sm;
-                    encode_unit_bf16(v[j], lut, nib, sm, esc[j], ex[j][0], ex[j][1]);
-                    uint8_t* nb = nibbles + (base + e) / 2;
-                    uint8_t* sb = signmant + (base + e);
-                    if (valid == 8u) {
-                        __stcs(reinterpret_cast<uint32_t*>(nb), nib);
-                        __stcs(reinterpret_cast<uint2*>(sb), sm);
-                    } else if (valid > 0u) {
-                        esc[j] &= (1u << valid) - 1u;
-                        nib &= (1u << (4u * valid)) - 1u;
-                        for (uint32_t b = 0; b < (valid + 1u) / 2u; ++b) nb[b] = uint8_t(nib >> (8u * b));
-                        const uint64_t smw = uint64_t(sm.x) | (uint64_t(sm.y) << 32);
-                        for (uint32_t b = 0; b < valid; ++b) sb[b] = uint8_t(smw >> (8u * b));
-                    } else {
-                        esc[j] = 0u;
+            // ---- nibble and sign|mantissa streams ----
+            uint8_t* nb = nibbles + base / 2 + my_elem / 2;
+            if constexpr (DT == SPLITZIP_BF16) {
+                uint8_t* sb = signmant + base + my_elem;
+                if (FULL || ne == TE) {
+                    __stcs(reinterpret_cast<uint4*>(nb), make_uint4(o.nib[0], o.nib[1], o.nib[2], o.nib[3]));
+                    __stcs(reinterpret_cast<uint4*>(sb), make_uint4(o.sm[0], o.sm[1], o.sm[2], o.sm[3]));
+                    __stcs(reinterpret_cast<uint4*>(sb) + 1, make_uint4(o.sm[4], o.sm[5], o.sm[6], o.sm[7]));
+                } else if (ne > 0u) {
+                    o.mask &= (1u << (ne & 31u)) - 1u;  // ne < 32 here
+                    for (uint32_t b = 0; b < ne; b += 2) {
+                        const uint32_t w = o.nib[b >> 3] >> (4 * (b & 7u));
+                        nb[b >> 1] = uint8_t(b + 1 < ne ? (w & 0xFFu) : (w & 0xFu));
                     }
+                    for (uint32_t b = 0; b < ne; ++b) sb[b] = uint8_t(o.sm[b >> 2] >> (8 * (b & 3u)));
                 } else {
-                    uint2 nib;
-                    uint32_t s3lo, s3hi;
-                    encode_unit_e5m2(v[j], lut, nib, s3lo, s3hi, esc[j], ex[j]);
-                    uint8_t* nb = nibbles + (base + e) / 2;
-                    uint8_t* sb = signmant + (base + e) / 8 * 3;  // 6 s3 bytes per unit
-                    // fast path: the warp's 32 units are full and the tile is a
-                    // multiple of 512 elements, so its 192 s3 bytes are 16-aligned
-                    const uint32_t warp_e0 = (uint32_t(j) * kConsumers + warp * 32u) * G::kUnitElems;
-                    const bool warp_full = (FULL || a.tile_elems % 512u == 0u) && (warp_e0 + 512u <= len);
-                    if (valid == 16u) {
-                        __stcs(reinterpret_cast<uint2*>(nb), nib);
-                    } else if (valid > 0u) {
-                        esc[j] &= (1u << valid) - 1u;
-                        uint64_t nw = uint64_t(nib.x) | (uint64_t(nib.y) << 32);
-                        nw &= (uint64_t(1) << (4u * valid)) - 1u;
-                        for (uint32_t b = 0; b < (valid + 1u) / 2u; ++b) nb[b] = uint8_t(nw >> (8u * b));
-                    } else {
-                        esc[j] = 0u;
-                    }
-                    if (warp_full) {  // warp-uniform
-                        uint16_t* st = reinterpret_cast<uint16_t*>(&s3_stage[warp][6 * lane]);
-                        st[0] = uint16_t(s3lo);
-                        st[1] = uint16_t(s3lo >> 16);
-                        st[2] = uint16_t(s3hi);
-                        __syncwarp();
-                        if (lane < 12) {
-                            const uint4 q = reinterpret_cast<const uint4*>(s3_stage[warp])[lane];
-                            uint8_t* dst = signmant + (base + warp_e0) / 8 * 3 + 16 * lane;
-                            __stcs(reinterpret_cast<uint4*>(dst), q);
-                        }
-                        __syncwarp();
-                    } else if (valid > 0u) {
-                        // 3 bytes per started group of 8 elements (pad bits are 0)
-                        const uint32_t nbytes = 3u * ((valid + 7u) / 8u);
-                        uint16_t* d16 = reinterpret_cast<uint16_t*>(sb);  // 6*unit is even
-                        if (nbytes == 6u) {
-                            d16[0] = uint16_t(s3lo);
-                            d16[1] = uint16_t(s3lo >> 16);
-                            d16[2] = uint16_t(s3hi);
-                        } else {
-                            d16[0] = uint16_t(s3lo);
-                            sb[2] = uint8_t(s3lo >> 16);
-                        }
-                    }
+                    o.mask = 0u;
                 }
-                cnt[j >> 1] |= uint32_t(__popc(esc[j])) << (16 * (j & 1));
+            } else {
+                uint32_t s3[6];
+                pack_s3_stream(p, s3);
+                uint8_t* sb = signmant + (base + my_elem) / 8 * 3;
+                if (FULL || ne == TE) {
+                    __stcs(reinterpret_cast<uint4*>(nb), make_uint4(o.nib[0], o.nib[1], o.nib[2], o.nib[3]));
+                    __stcs(reinterpret_cast<uint4*>(nb) + 1, make_uint4(o.nib[4], o.nib[5], o.nib[6], o.nib[7]));
+#pragma unroll
+                    for (int k = 0; k < 3; ++k)
+                        __stcs(reinterpret_cast<uint2*>(sb) + k, make_uint2(s3[2 * k], s3[2 * k + 1]));
+                } else if (ne > 0u) {
+                    if (ne < 32u) {  // ne < 64 here
+                        o.mask[0] &= (1u << (ne & 31u)) - 1u;
+                        o.mask[1] = 0u;
+                    } else {
+                        o.mask[1] &= (1u << ((ne - 32u) & 31u)) - 1u;
+                    }
+                    for (uint32_t b = 0; b < ne; b += 2) {
+                        const uint32_t w = o.nib[b >> 3] >> (4 * (b & 7u));
+                        nb[b >> 1] = uint8_t(b + 1 < ne ? (w & 0xFFu) : (w & 0xFu));
+                    }
+                    // 3 bytes per started group of 8 elements (pad bits are 0)
+                    for (uint32_t b = 0; b < 3u * ((ne + 7u) / 8u); ++b) sb[b] = uint8_t(s3[b >> 2] >> (8 * (b & 3u)));
+                } else {
+                    o.mask[0] = o.mask[1] = 0u;
+                }
             }
 
-            // ---- block-wide exclusive scan of the per-thread escape counts,
-            // in element order (unit group j major, then thread) ----
-            uint32_t incl[kWords];
-#pragma unroll
-            for (int k = 0; k < kWords; ++k) incl[k] = cnt[k];
+            // ---- the warp's escapes, in element order, to its staging region ----
+            uint32_t cnt;
+            if constexpr (DT == SPLITZIP_BF16)
+                cnt = __popc(o.mask);
+            else
+                cnt = __popc(o.mask[0]) + __popc(o.mask[1]);
+            uint32_t incl = cnt;
 #pragma unroll
             for (int d = 1; d < 32; d <<= 1) {
+                const uint32_t y = __shfl_up_sync(kFull, incl, d);
+                if (lane >= d) incl += y;
+            }
+            if (lane == 31) a.warp_counts[tile * kEncodeWarps + warp] = incl;
+            if (cnt) {
+                uint32_t* slot = a.staging + tile * a.tile_elems + warp * a.region_elems + (incl - cnt);
 #pragma unroll
-                for (int k = 0; k < kWords; ++k) {
-                    const uint32_t y = __shfl_up_sync(kFull, incl[k], d);
-                    if (lane >= d) incl[k] += y;
+                for (int h = 0; h < (DT == SPLITZIP_BF16 ? 1 : 2); ++h) {
+                    uint32_t m;
+                    if constexpr (DT == SPLITZIP_BF16)
+                        m = o.mask;
+                    else
+                        m = o.mask[h];
+                    while (m) {
+                        const uint32_t b = 32u * h + uint32_t(__ffs(m) - 1);
+                        m &= m - 1u;
+                        const uint32_t e = my_elem + b;  // element of the tile
+                        const uint32_t B = e * EB;       // its first byte in the tile
+                        uint32_t x;
+                        if (FULL || B + EB <= in_stage)
+                            x = DT == SPLITZIP_BF16 ? uint32_t(*reinterpret_cast<const uint16_t*>(st + swizzled(B)))
+                                                    : uint32_t(st[swizzled(B)]);
+                        else
+                            x = DT == SPLITZIP_BF16 ? uint32_t(reinterpret_cast<const uint16_t*>(in)[base + e])
+                                                    : uint32_t(in[base + e]);
+                        const uint32_t exponent = DT == SPLITZIP_BF16 ? (x >> 7) & 0xFFu : (x >> 2) & 0x1Fu;
+                        *slot++ = ((pos0 + e) << 8) | exponent;
+                    }
                 }
-            }
-            if (lane == 31) {
-#pragma unroll
-                for (int k = 0; k < kWords; ++k) warp_sums[parity][warp][k] = incl[k];
-            }
-            named_barrier(1, kConsumers);
-            uint32_t before[kWords], total[kWords];
-#pragma unroll
-            for (int k = 0; k < kWords; ++k) before[k] = total[k] = 0u;
-#pragma unroll
-            for (int w = 0; w < kConsumerWarps; ++w) {
-#pragma unroll
-                for (int k = 0; k < kWords; ++k) {
-                    const uint32_t s = warp_sums[parity][w][k];
-                    if (w < warp) before[k] += s;
-                    total[k] += s;
-                }
-            }
-            uint32_t tile_total = 0;
-#pragma unroll
-            for (int j = 0; j < J; ++j) tile_total += (total[j >> 1] >> (16 * (j & 1))) & 0xFFFFu;
-
-            if (tid == 0) {
-                a.tile_counts[tile] = tile_total;
-                if (tile_total) atomicAdd(a.group_totals + tile / kGroupTiles, tile_total);
-            }
-
-            // ---- escape records, in element order, to the tile's staging slot ----
-            uint32_t* slot = a.staging + tile * a.tile_elems;
-            uint32_t group_base = 0;  // escapes of the tile in unit groups < j
-#pragma unroll
-            for (int j = 0; j < J; ++j) {
-                const int k = j >> 1, sh = 16 * (j & 1);
-                const uint32_t excl = ((before[k] + incl[k] - cnt[k]) >> sh) & 0xFFFFu;
-                uint32_t idx = group_base + excl;
-                uint32_t m = esc[j];
-                const uint32_t upos = pos0 + (uint32_t(j) * kConsumers + tid) * G::kUnitElems;
-                while (m) {
-                    const uint32_t b = __ffs(m) - 1;
-                    m &= m - 1;
-                    const uint32_t q = b >> 2;  // which exponent word (select, no local memory)
-                    const uint32_t ew = q == 0 ? ex[j][0] : q == 1 ? ex[j][1] : q == 2 ? ex[j][2] : ex[j][3];
-                    const uint32_t exponent = (ew >> (8u * (b & 3u))) & 0xFFu;
-                    slot[idx++] = ((upos + b) << 8) | exponent;
-                }
-                group_base += (total[k] >> sh) & 0xFFFFu;
             }
         };
-        if (len_rt == kTileElems)
+        // (only a full-size tile gives every consumer thread its 64 bytes)
+        if (in_stage == kTileBytes && len * EB == kTileBytes)
             body(std::true_type{});
         else
             body(std::false_type{});
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty_bar[stage]);  // the stage may be refilled
     }
 }
 
@@ -387,6 +381,32 @@ __device__ __forceinline__ uint64_t warp_sum_u64(uint64_t v) {
 #pragma unroll
     for (int d = 16; d > 0; d >>= 1) v += __shfl_xor_sync(kFull, v, d);
     return v;
+}
+
+// Escapes of one tile: the sum of its consumer warps' counts.
+__device__ __forceinline__ uint32_t tile_count(const EncodeArgs& a, uint64_t t) {
+    const uint4* wc = reinterpret_cast<const uint4*>(a.warp_counts + t * kEncodeWarps);
+    const uint4 q0 = wc[0], q1 = wc[1];
+    return q0.x + q0.y + q0.z + q0.w + q1.x + q1.y + q1.z + q1.w;
+}
+
+// One CTA per group of kGroupTiles tiles: the group's escape total (a plain
+// store, so the streaming pass needs no atomics and the totals no clearing).
+__global__ void __launch_bounds__(kFinishThreads) encode_group_kernel(const EncodeArgs a) {
+    __shared__ uint32_t warp_sum[kFinishThreads / 32];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const uint64_t t = uint64_t(blockIdx.x) * kGroupTiles + tid;
+    uint32_t c = t < a.n_tiles ? tile_count(a, t) : 0u;
+#pragma unroll
+    for (int d = 16; d > 0; d >>= 1) c += __shfl_xor_sync(kFull, c, d);
+    if (lane == 0) warp_sum[warp] = c;
+    __syncthreads();
+    if (tid == 0) {
+        uint32_t total = 0;
+#pragma unroll
+        for (int w = 0; w < kFinishThreads / 32; ++w) total += warp_sum[w];
+        a.group_totals[blockIdx.x] = total;
+    }
 }
 
 // One CTA per group of kGroupTiles tiles (groups are chunk-aligned: tiles per
@@ -406,9 +426,10 @@ __global__ void __launch_bounds__(kFinishThreads) encode_index_kernel(const Enco
     before = warp_sum_u64(before);
     if (lane == 0) warp_part[warp] = before;
 
-    // exclusive scan of the group's tile counts
+    // exclusive scan of the group's tile counts (a tile's count = the sum of
+    // its consumer warps' counts)
     const uint64_t t = g * kGroupTiles + tid;
-    const uint32_t c = t < a.n_tiles ? a.tile_counts[t] : 0u;
+    const uint32_t c = t < a.n_tiles ? tile_count(a, t) : 0u;
     uint32_t incl = c;
 #pragma unroll
     for (int d = 1; d < 32; d <<= 1) {
@@ -446,43 +467,63 @@ __global__ void __launch_bounds__(kFinishThreads) encode_index_kernel(const Enco
 }
 
 // Staged records -> 3-byte records in the escape stream.  Each warp serves
-// kRecordTiles consecutive tiles and interleaves them, so every lane keeps
-// kRecordTiles independent loads in flight per round.
+// kRecordTiles consecutive tiles: lane 8k + w holds the count and the
+// exclusive prefix of consumer warp w of tile k, and every round moves one
+// record of each tile per lane, so a lane keeps kRecordTiles independent
+// loads in flight.
 constexpr int kRecordTiles = 4;
 constexpr int kRecordThreads = 256;
+static_assert(kRecordTiles * kEncodeWarps == 32, "one lane per (tile, consumer warp)");
 
 __global__ void __launch_bounds__(kRecordThreads) encode_records_kernel(const EncodeArgs a) {
     const int lane = threadIdx.x & 31;
     const uint64_t t0 = (uint64_t(blockIdx.x) * (kRecordThreads / 32) + (threadIdx.x >> 5)) * kRecordTiles;
     if (t0 >= a.n_tiles) return;
-    uint64_t first = 0;
-    uint32_t cnt = 0;
-    if (lane < kRecordTiles && t0 + lane < a.n_tiles) {
-        first = a.tile_first[t0 + lane];
-        cnt = a.tile_counts[t0 + lane];
+    const int my_tile = lane >> 3, my_region = lane & 7;
+    const bool have = t0 + my_tile < a.n_tiles;
+    const uint32_t c = have ? a.warp_counts[t0 * kEncodeWarps + lane] : 0u;
+    uint32_t o = c;  // inclusive scan within each group of 8 lanes
+#pragma unroll
+    for (int d = 1; d < 8; d <<= 1) {
+        const uint32_t y = __shfl_up_sync(kFull, o, d);
+        if (my_region >= d) o += y;
     }
+    o -= c;  // first record of region my_region within its tile
+    const uint64_t first = have && my_region == 0 ? a.tile_first[t0 + my_tile] : 0u;
     uint64_t f[kRecordTiles];
-    uint32_t c[kRecordTiles], most = 0;
+    uint32_t tot[kRecordTiles], most = 0;
 #pragma unroll
     for (int k = 0; k < kRecordTiles; ++k) {
-        f[k] = __shfl_sync(kFull, first, k);
-        c[k] = __shfl_sync(kFull, cnt, k);
-        most = max(most, c[k]);
+        f[k] = __shfl_sync(kFull, first, 8 * k);
+        tot[k] = __shfl_sync(kFull, o + c, 8 * k + 7);
+        most = max(most, tot[k]);
     }
     const Layout L0 = layout_for(a.n, a.dtype, a.chunk_elems, 0);
     uint8_t* records = a.out + L0.escrec_off;
-    for (uint32_t i = lane; i < most; i += 32) {
-        uint32_t r[kRecordTiles];
-#pragma unroll
-        for (int k = 0; k < kRecordTiles; ++k)
-            r[k] = i < c[k] ? __ldcs(a.staging + (t0 + k) * a.tile_elems + i) : 0u;
+    const uint32_t rounds = (most + 31u) / 32u;
+    for (uint32_t r = 0; r < rounds; ++r) {
+        const uint32_t i = 32u * r + uint32_t(lane);
+        uint32_t v[kRecordTiles];
 #pragma unroll
         for (int k = 0; k < kRecordTiles; ++k) {
-            if (i < c[k]) {
+            // region of record i: the last region whose first record is <= i
+            uint32_t w = 0;
+#pragma unroll
+            for (uint32_t step = 4; step > 0; step >>= 1) {
+                const uint32_t first_w = __shfl_sync(kFull, o, 8 * k + int(w + step));
+                if (i >= first_w) w += step;
+            }
+            const uint32_t first_w = __shfl_sync(kFull, o, 8 * k + int(w));
+            v[k] = i < tot[k] ? __ldcs(a.staging + (t0 + k) * a.tile_elems + w * a.region_elems + (i - first_w))
+                              : 0u;
+        }
+#pragma unroll
+        for (int k = 0; k < kRecordTiles; ++k) {
+            if (i < tot[k]) {
                 uint8_t* d = records + 3 * (f[k] + i);
-                d[0] = uint8_t(r[k] >> 8);
-                d[1] = uint8_t(r[k] >> 16);
-                d[2] = uint8_t(r[k]);
+                d[0] = uint8_t(v[k] >> 8);
+                d[1] = uint8_t(v[k] >> 16);
+                d[2] = uint8_t(v[k]);
             }
         }
     }
@@ -490,13 +531,16 @@ __global__ void __launch_bounds__(kRecordThreads) encode_records_kernel(const En
 
 }  // namespace
 
-cudaError_t launch_encode(const EncodeArgs& a, const EncodeLut& lut, int grid, cudaStream_t s) {
+cudaError_t launch_encode(const EncodeArgs& a, const EncodeLut& lut, const CUtensorMap& map, int grid,
+                          cudaStream_t s) {
     if (a.dtype == SPLITZIP_BF16)
-        encode_kernel<SPLITZIP_BF16><<<grid, kBlock, kEncodeSmem, s>>>(a, lut);
+        encode_kernel<SPLITZIP_BF16><<<grid, kBlock, kEncodeSmem, s>>>(a, map, lut);
     else
-        encode_kernel<SPLITZIP_FP8_E5M2><<<grid, kBlock, kEncodeSmem, s>>>(a, lut);
+        encode_kernel<SPLITZIP_FP8_E5M2><<<grid, kBlock, kEncodeSmem, s>>>(a, map, lut);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess || a.n_groups == 0) return e;
+    encode_group_kernel<<<unsigned(a.n_groups), kFinishThreads, 0, s>>>(a);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
     encode_index_kernel<<<unsigned(a.n_groups), kFinishThreads, 0, s>>>(a);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     const uint64_t warps = (a.n_tiles + kRecordTiles - 1) / kRecordTiles;

@@ -12,9 +12,8 @@
 // GPU that loads this library, for the life of the process.  All calls on a
 // device share it: calls whose GPU work overlaps in time (different streams,
 // or several host threads) race on it and must be serialised by the caller.
-// splitzip_encode clears the part of the scratch that must start at zero (on
-// the caller's stream, before its kernel), so the contents left by an earlier
-// call do no harm.
+// splitzip_encode writes every word of its workspace before reading it, so
+// the contents left by an earlier call do no harm.
 #include <mutex>
 
 #include "splitzip_internal.cuh"

@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cstdint>
+#include <cuda.h>  // CUtensorMap (types only; the encoder of tensor maps is fetched from the runtime)
 #include <cuda_runtime.h>
 
 #include "splitzip.h"
@@ -14,16 +15,23 @@ constexpr uint64_t kHeaderBytes = 64;
 constexpr uint32_t kMinChunk = 64;
 constexpr uint32_t kMaxChunk = 65536;
 
-// Work decomposition.  A tile is the unit of work of one encode CTA trip:
-// 8,192 elements, or the chunk when chunks are smaller, so a tile never
-// straddles a chunk (chunk sizes are powers of two >= 64).
-constexpr uint32_t kTileElems = 8192;
+// Work decomposition of the encoder.  A tile is the unit of work of one
+// encode CTA trip: 16 KB of input (8,192 BF16 or 16,384 E5M2 elements), or the
+// chunk when chunks are smaller, so a tile never straddles a chunk (chunk
+// sizes are powers of two >= 64).  Each of the 8 consumer warps of a CTA owns
+// a contiguous region of 2 KB of the tile (32 threads x 64 bytes).
+constexpr uint32_t kTileBytes = 16384;
+constexpr uint32_t kEncodeWarps = 8;
+constexpr uint32_t kThreadBytes = 64;
+constexpr uint32_t kRegionBytes = 32 * kThreadBytes;
 constexpr int kHistThreads = 256;
 
 // Encoder table entry: low 4 bits = code, bit 4 = escape flag.
 constexpr uint8_t kEscapeFlag = 0x10;
 
 __host__ __device__ inline uint64_t align16(uint64_t x) { return (x + 15u) & ~uint64_t(15); }
+
+__host__ __device__ inline uint32_t elem_bytes(int dtype) { return dtype == SPLITZIP_BF16 ? 2u : 1u; }
 
 __host__ __device__ inline uint64_t signmant_bytes(int dtype, uint64_t n) {
     return dtype == SPLITZIP_BF16 ? n : 3u * ((n + 7u) / 8u);
@@ -48,34 +56,35 @@ __host__ __device__ inline Layout layout_for(uint64_t n, int dtype, uint32_t chu
     return L;
 }
 
-__host__ __device__ inline uint32_t tile_elems_for(uint32_t chunk) {
-    return chunk < kTileElems ? chunk : kTileElems;
+__host__ __device__ inline uint32_t tile_elems_for(int dtype, uint32_t chunk) {
+    const uint32_t full = kTileBytes / elem_bytes(dtype);
+    return chunk < full ? chunk : full;
 }
 
 // Encoder workspace: per-group escape totals (a group is kGroupTiles
-// consecutive tiles), per-tile escape counts, per-tile first record indices,
-// then one staging slot of tile_elems records per tile; a record is
-// (in-chunk position << 8) | exponent.  Only the group
-// totals must be zero when the encode starts (`zero_bytes`); everything else
-// is written before it is read.
+// consecutive tiles), per-(tile, consumer warp) escape counts, per-tile first
+// record indices, then one staging slot of tile_elems records per tile, in
+// which consumer warp w stages its records from element w * region_elems on;
+// a record is (in-chunk position << 8) | exponent.  Every word is written
+// before it is read, so the workspace needs no initialisation.
 constexpr uint32_t kGroupTiles = 256;
 
 struct Workspace {
     uint64_t n_tiles, n_groups;
-    uint32_t tile_elems;
-    uint64_t group_off, count_off, tile_off_off, staging_off, zero_bytes, bytes;
+    uint32_t tile_elems, region_elems;
+    uint64_t group_off, warp_count_off, tile_first_off, staging_off, bytes;
 };
 
-__host__ __device__ inline Workspace workspace_for(uint64_t n, uint32_t chunk) {
+__host__ __device__ inline Workspace workspace_for(uint64_t n, int dtype, uint32_t chunk) {
     Workspace W;
-    W.tile_elems = tile_elems_for(chunk);
+    W.tile_elems = tile_elems_for(dtype, chunk);
+    W.region_elems = kRegionBytes / elem_bytes(dtype);
     W.n_tiles = (n + W.tile_elems - 1u) / W.tile_elems;
     W.n_groups = (W.n_tiles + kGroupTiles - 1u) / kGroupTiles;
     W.group_off = 0;
-    W.zero_bytes = align16(4u * W.n_groups);
-    W.count_off = W.zero_bytes;
-    W.tile_off_off = align16(W.count_off + 4u * W.n_tiles);
-    W.staging_off = align16(W.tile_off_off + 8u * W.n_tiles);
+    W.warp_count_off = align16(4u * W.n_groups);
+    W.tile_first_off = align16(W.warp_count_off + 4u * kEncodeWarps * W.n_tiles);
+    W.staging_off = align16(W.tile_first_off + 8u * W.n_tiles);
     W.bytes = W.staging_off + 4u * W.n_tiles * W.tile_elems;
     return W;
 }
@@ -89,15 +98,19 @@ struct EncodeArgs {
     uint64_t n;
     uint8_t* out;            // container base
     uint32_t* group_totals;  // workspace, per group of kGroupTiles tiles
-    uint32_t* tile_counts;   // workspace, per tile
+    uint32_t* warp_counts;   // workspace, per tile and consumer warp
     uint64_t* tile_first;    // workspace, per tile: index of its first record
     uint32_t* staging;       // workspace, tile_elems records per tile
     uint64_t* out_size;
     int* error;              // device status word
     uint64_t n_tiles, n_groups;
-    uint32_t tile_elems;
+    uint32_t tile_elems, region_elems;
     uint32_t chunk_elems;
     uint64_t n_chunks;
+    // Input bytes the tensor map covers (whole 128-byte rows from the start;
+    // 0 = no tensor map) and the bytes one tensor-map load delivers.
+    uint64_t tensor_bytes;
+    uint32_t box_bytes;
     int dtype;
     uint8_t codebook[16];
 };
@@ -113,7 +126,8 @@ struct DecodeArgs {
 
 // Launchers (encode.cu, decode.cu, histogram.cu).  Each returns the result of
 // cudaGetLastError() after its launch.
-cudaError_t launch_encode(const EncodeArgs& a, const EncodeLut& lut, int grid, cudaStream_t s);
+cudaError_t launch_encode(const EncodeArgs& a, const EncodeLut& lut, const CUtensorMap& map, int grid,
+                          cudaStream_t s);
 cudaError_t launch_decode(const DecodeArgs& a, int grid, cudaStream_t s);
 cudaError_t launch_histogram(const void* x, uint64_t n, int dtype, unsigned long long* hist, int grid,
                              cudaStream_t s);

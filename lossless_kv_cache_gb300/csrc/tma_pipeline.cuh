@@ -1,6 +1,7 @@
 // Bulk-copy (TMA) and mbarrier helpers for the streaming kernels (sm_90+,
-// used here on sm_103a).  One producer thread moves contiguous global ranges
-// into shared-memory stages with cp.async.bulk; each stage has a "full"
+// used here on sm_103a).  One producer thread moves global data into
+// shared-memory stages with cp.async.bulk (contiguous ranges) or
+// cp.async.bulk.tensor (boxes of a tensor map); each stage has a "full"
 // mbarrier (the copy engine completes its transaction count) and an "empty"
 // mbarrier (every consumer warp arrives once it no longer reads the stage).
 //
@@ -67,6 +68,19 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
         "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
             smem_u32(dst)),
         "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// Tiled tensor-map copy of one box of a 2-D tensor into shared memory;
+// completes the box's bytes on the barrier (elements outside the tensor are
+// written as zeros and still counted).  `map` is the address of a
+// __grid_constant__ CUtensorMap kernel parameter; x (innermost, in elements)
+// times the element size must be a multiple of 16 bytes.
+__device__ __forceinline__ void tensor_load_2d(void* dst, const void* map, int32_t x, int32_t y, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::
+            "r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
         : "memory");
 }
 

@@ -56,16 +56,20 @@ def test_sizes_match_oracle(splitzip_lib, dtype, chunk):
 
 
 def test_workspace_size(splitzip_lib):
-    # per-group totals, per-tile counts, per-tile first record indices, then a
-    # staging slot of tile_elems 4-byte records per tile
+    # per-group totals, per-(tile, consumer warp) counts, per-tile first
+    # record indices, then a staging slot of tile_elems 4-byte records per
+    # tile; a tile is 16 KB of input (8,192 BF16 or 16,384 E5M2 elements) or
+    # the chunk when chunks are smaller
     a16 = lambda x: -(-x // 16) * 16
+    head = lambda tiles: a16(a16(a16(4 * -(-tiles // 256)) + 32 * tiles) + 8 * tiles)
     n = 5 * 8192 + 3
-    tiles = 6
-    head = a16(a16(a16(4) + 4 * tiles) + 8 * tiles)
-    assert sz.workspace_size(n, sz.BF16, 65536) == head + 4 * tiles * 8192
-    tiles = -(-n // 1024)  # tiles = chunks when chunks are smaller than 8192
-    head = a16(a16(a16(4) + 4 * tiles) + 8 * tiles)
-    assert sz.workspace_size(n, sz.BF16, 1024) == head + 4 * tiles * 1024
+    assert sz.workspace_size(n, sz.BF16, 65536) == head(6) + 4 * 6 * 8192
+    assert sz.workspace_size(n, sz.FP8_E5M2, 65536) == head(3) + 4 * 3 * 16384
+    tiles = -(-n // 1024)  # tiles = chunks when chunks are smaller than a tile
+    assert sz.workspace_size(n, sz.BF16, 1024) == head(tiles) + 4 * tiles * 1024
+    assert sz.workspace_size(n, sz.FP8_E5M2, 1024) == head(tiles) + 4 * tiles * 1024
+    n = 300 * 8192 * 2
+    assert sz.workspace_size(n, sz.BF16, 65536) == head(600) + 4 * 600 * 8192
     assert sz.workspace_size(0, sz.BF16, 65536) == 0
 
 
