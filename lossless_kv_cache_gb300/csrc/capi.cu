@@ -117,7 +117,6 @@ int prepare_encode(const void* d_in, uint64_t n, int dtype, const splitzip_codeb
     a->n_tiles = W->n_tiles;
     a->n_groups = W->n_groups;
     a->tile_elems = W->tile_elems;
-    a->region_elems = W->region_elems;
     a->chunk_elems = chunk;
     a->n_chunks = layout_for(n, dtype, chunk, 0).n_chunks;
     a->dtype = dtype;

@@ -18,8 +18,11 @@
 //     positions, so the sum of four entries is the group's two nibble bytes,
 //     its escape flags and (E5M2) its packed 3-bit sign|mantissa values.  The
 //     nibble and sign|mantissa streams go out with 16-byte stores; a warp scan
-//     orders the warp's escapes and the warp stages them in the tile's slot;
-//     the warp's count goes to the workspace.
+//     orders the warp's escapes and the warp stages them in the tile's slot,
+//     interleaved with the other warps' (record j of warp w at j * S + w, S =
+//     the tile's warps with elements), so a tile's records share a few
+//     sectors without any synchronisation between the warps; the warp's count
+//     goes to the workspace.
 //   encode_group_kernel (one CTA per group of 256 tiles): the group's total.
 //   encode_index_kernel (one CTA per group of 256 tiles): the sum of the
 //     earlier groups' totals plus a block scan of the group's tile counts give
@@ -231,6 +234,7 @@ __global__ void __launch_bounds__(kBlock, 3)
     uint8_t* nibbles = a.out + L0.nibble_off;
     uint8_t* signmant = a.out + L0.signmant_off;
     const uint32_t my_byte = kThreadBytes * uint32_t(tid);
+    const uint32_t stride = staging_stride(a.tile_elems, EB);
     const uint32_t my_elem = my_byte / EB;  // first element of the thread in a tile
     uint32_t piece_off[4];                  // stage offsets of the thread's four 16-byte pieces
 #pragma unroll
@@ -341,7 +345,7 @@ __global__ void __launch_bounds__(kBlock, 3)
             }
             if (lane == 31) a.warp_counts[tile * kEncodeWarps + warp] = incl;
             if (cnt) {
-                uint32_t* slot = a.staging + tile * a.tile_elems + warp * a.region_elems + (incl - cnt);
+                uint32_t* slot = a.staging + tile * a.tile_elems + (incl - cnt) * stride + warp;
 #pragma unroll
                 for (int h = 0; h < (DT == SPLITZIP_BF16 ? 1 : 2); ++h) {
                     uint32_t m;
@@ -362,7 +366,8 @@ __global__ void __launch_bounds__(kBlock, 3)
                             x = DT == SPLITZIP_BF16 ? uint32_t(reinterpret_cast<const uint16_t*>(in)[base + e])
                                                     : uint32_t(in[base + e]);
                         const uint32_t exponent = DT == SPLITZIP_BF16 ? (x >> 7) & 0xFFu : (x >> 2) & 0x1Fu;
-                        *slot++ = ((pos0 + e) << 8) | exponent;
+                        *slot = ((pos0 + e) << 8) | exponent;
+                        slot += stride;
                     }
                 }
             }
@@ -426,8 +431,7 @@ __global__ void __launch_bounds__(kFinishThreads) encode_index_kernel(const Enco
     before = warp_sum_u64(before);
     if (lane == 0) warp_part[warp] = before;
 
-    // exclusive scan of the group's tile counts (a tile's count = the sum of
-    // its consumer warps' counts)
+    // exclusive scan of the group's tile counts
     const uint64_t t = g * kGroupTiles + tid;
     const uint32_t c = t < a.n_tiles ? tile_count(a, t) : 0u;
     uint32_t incl = c;
@@ -479,17 +483,17 @@ __global__ void __launch_bounds__(kRecordThreads) encode_records_kernel(const En
     const int lane = threadIdx.x & 31;
     const uint64_t t0 = (uint64_t(blockIdx.x) * (kRecordThreads / 32) + (threadIdx.x >> 5)) * kRecordTiles;
     if (t0 >= a.n_tiles) return;
-    const int my_tile = lane >> 3, my_region = lane & 7;
+    const int my_tile = lane >> 3, my_warp = lane & 7;
     const bool have = t0 + my_tile < a.n_tiles;
     const uint32_t c = have ? a.warp_counts[t0 * kEncodeWarps + lane] : 0u;
     uint32_t o = c;  // inclusive scan within each group of 8 lanes
 #pragma unroll
     for (int d = 1; d < 8; d <<= 1) {
         const uint32_t y = __shfl_up_sync(kFull, o, d);
-        if (my_region >= d) o += y;
+        if (my_warp >= d) o += y;
     }
-    o -= c;  // first record of region my_region within its tile
-    const uint64_t first = have && my_region == 0 ? a.tile_first[t0 + my_tile] : 0u;
+    o -= c;  // first record of warp my_warp within its tile
+    const uint64_t first = have && my_warp == 0 ? a.tile_first[t0 + my_tile] : 0u;
     uint64_t f[kRecordTiles];
     uint32_t tot[kRecordTiles], most = 0;
 #pragma unroll
@@ -500,13 +504,14 @@ __global__ void __launch_bounds__(kRecordThreads) encode_records_kernel(const En
     }
     const Layout L0 = layout_for(a.n, a.dtype, a.chunk_elems, 0);
     uint8_t* records = a.out + L0.escrec_off;
+    const uint32_t stride = staging_stride(a.tile_elems, elem_bytes(a.dtype));
     const uint32_t rounds = (most + 31u) / 32u;
     for (uint32_t r = 0; r < rounds; ++r) {
         const uint32_t i = 32u * r + uint32_t(lane);
         uint32_t v[kRecordTiles];
 #pragma unroll
         for (int k = 0; k < kRecordTiles; ++k) {
-            // region of record i: the last region whose first record is <= i
+            // warp of record i: the last warp whose first record is <= i
             uint32_t w = 0;
 #pragma unroll
             for (uint32_t step = 4; step > 0; step >>= 1) {
@@ -514,8 +519,7 @@ __global__ void __launch_bounds__(kRecordThreads) encode_records_kernel(const En
                 if (i >= first_w) w += step;
             }
             const uint32_t first_w = __shfl_sync(kFull, o, 8 * k + int(w));
-            v[k] = i < tot[k] ? __ldcs(a.staging + (t0 + k) * a.tile_elems + w * a.region_elems + (i - first_w))
-                              : 0u;
+            v[k] = i < tot[k] ? __ldcs(a.staging + (t0 + k) * a.tile_elems + (i - first_w) * stride + w) : 0u;
         }
 #pragma unroll
         for (int k = 0; k < kRecordTiles; ++k) {

@@ -18,12 +18,11 @@ constexpr uint32_t kMaxChunk = 65536;
 // Work decomposition of the encoder.  A tile is the unit of work of one
 // encode CTA trip: 16 KB of input (8,192 BF16 or 16,384 E5M2 elements), or the
 // chunk when chunks are smaller, so a tile never straddles a chunk (chunk
-// sizes are powers of two >= 64).  Each of the 8 consumer warps of a CTA owns
-// a contiguous region of 2 KB of the tile (32 threads x 64 bytes).
+// sizes are powers of two >= 64).  Each of the 256 consumer threads of a CTA
+// owns 64 contiguous bytes of the tile.
 constexpr uint32_t kTileBytes = 16384;
 constexpr uint32_t kEncodeWarps = 8;
 constexpr uint32_t kThreadBytes = 64;
-constexpr uint32_t kRegionBytes = 32 * kThreadBytes;
 constexpr int kHistThreads = 256;
 
 // Encoder table entry: low 4 bits = code, bit 4 = escape flag.
@@ -61,24 +60,30 @@ __host__ __device__ inline uint32_t tile_elems_for(int dtype, uint32_t chunk) {
     return chunk < full ? chunk : full;
 }
 
+// Consumer warps that hold elements of a tile: each owns 32 x 64 bytes.
+__host__ __device__ inline uint32_t staging_stride(uint32_t tile_elems, uint32_t eb) {
+    const uint32_t warp_elems = 32u * kThreadBytes / eb;
+    return tile_elems > warp_elems ? tile_elems / warp_elems : 1u;
+}
+
 // Encoder workspace: per-group escape totals (a group is kGroupTiles
 // consecutive tiles), per-(tile, consumer warp) escape counts, per-tile first
-// record indices, then one staging slot of tile_elems records per tile, in
-// which consumer warp w stages its records from element w * region_elems on;
-// a record is (in-chunk position << 8) | exponent.  Every word is written
+// record indices, then one staging slot of tile_elems records per tile; a
+// record is (in-chunk position << 8) | exponent.  Record j of consumer warp w
+// sits at slot entry j * S + w, S = staging_stride (the warps that hold
+// elements of a tile), so the tile's few records share a few sectors.  Every word is written
 // before it is read, so the workspace needs no initialisation.
 constexpr uint32_t kGroupTiles = 256;
 
 struct Workspace {
     uint64_t n_tiles, n_groups;
-    uint32_t tile_elems, region_elems;
+    uint32_t tile_elems;
     uint64_t group_off, warp_count_off, tile_first_off, staging_off, bytes;
 };
 
 __host__ __device__ inline Workspace workspace_for(uint64_t n, int dtype, uint32_t chunk) {
     Workspace W;
     W.tile_elems = tile_elems_for(dtype, chunk);
-    W.region_elems = kRegionBytes / elem_bytes(dtype);
     W.n_tiles = (n + W.tile_elems - 1u) / W.tile_elems;
     W.n_groups = (W.n_tiles + kGroupTiles - 1u) / kGroupTiles;
     W.group_off = 0;
@@ -104,7 +109,7 @@ struct EncodeArgs {
     uint64_t* out_size;
     int* error;              // device status word
     uint64_t n_tiles, n_groups;
-    uint32_t tile_elems, region_elems;
+    uint32_t tile_elems;
     uint32_t chunk_elems;
     uint64_t n_chunks;
     // Input bytes the tensor map covers (whole 128-byte rows from the start;

@@ -67,10 +67,11 @@ def test_noalloc_fp8_e5m2(splitzip_lib):
 
 
 def test_noalloc_rejects_sizes_beyond_its_scratch(splitzip_lib):
-    limit = 8_372_224  # largest n whose workspace fits 32 MiB at the default chunk size
-    for dtype in (sz.BF16, sz.FP8_E5M2):
-        assert sz.workspace_size(limit, dtype, 65536) <= sz.NOALLOC_SCRATCH_BYTES
-        assert sz.workspace_size(limit + 1, dtype, 65536) > sz.NOALLOC_SCRATCH_BYTES
+    # largest n whose workspace fits 32 MiB at the default chunk size
+    for dtype, n_max in ((sz.BF16, 8_372_224), (sz.FP8_E5M2, 8_372_224)):
+        assert sz.workspace_size(n_max, dtype, 65536) <= sz.NOALLOC_SCRATCH_BYTES
+        assert sz.workspace_size(n_max + 1, dtype, 65536) > sz.NOALLOC_SCRATCH_BYTES
+    limit = 8_372_224
     cb = sz.Codebook.make(sz.BF16, range(16))
     A = 1 << 20  # never dereferenced: the size check comes first
     st = sz.splitzip_encode_noalloc(A, limit + 1, sz.BF16, cb, 65536, A, 1 << 40, A, A, 0)
