@@ -130,6 +130,10 @@ constexpr uint32_t kDecodeSmem = kStages * kStageBytes;
 // each sub-tile is patched right after its stores, while its lines are still
 // in L2; a chunk with more escapes is patched from global memory instead.
 constexpr uint32_t kRecCap = 768;
+// Resident CTAs per SM the kernel is compiled for (register budget): BF16
+// runs fastest at 2 with ~90 registers a thread, E5M2 at 3 (measured: BF16
+// 1.18 ms at 2 vs 1.24 ms at 4; E5M2 1.50 ms at 3 vs 1.71 ms at 2).
+template <int DT> constexpr int kDecodeMinBlocks = DT == SPLITZIP_BF16 ? 2 : 3;
 constexpr uint32_t kRecBytes = 3 * kRecCap + 32;  // + room for a 16-byte window shift
 
 struct SubTile {
@@ -149,59 +153,57 @@ __device__ __forceinline__ SubTile subtile_windows(const uint8_t* nibbles, const
 }
 
 // Dense decode of one sub-tile from shared memory; results go straight to
-// global memory with 16-byte streaming stores.
+// global memory with 16-byte streaming stores.  Unit u (UE elements) of the
+// sub-tile is decoded by thread u mod 256 in round u / 256.
 template <int DT>
 __device__ __forceinline__ void decode_subtile(const uint8_t* nb, const uint8_t* sb, void* out_base, uint64_t g,
                                                uint32_t cnt, int tid, const uint16_t* lut2) {
-    if constexpr (DT == SPLITZIP_BF16) {
-        uint16_t* out = static_cast<uint16_t*>(out_base) + g;
-        const uint32_t units = (cnt + 7u) / 8u;
-#pragma unroll 4
-        for (uint32_t u = tid; u < units; u += kConsumers) {
-            const uint32_t e = 8u * u;
-            if (e + 8u <= cnt) {
+    constexpr uint32_t UE = DT == SPLITZIP_BF16 ? 8u : 16u;
+    const uint32_t units = (cnt + UE - 1u) / UE;
+    const uint32_t rounds = (units + kConsumers - 1u) / kConsumers;
+#pragma unroll 2
+    for (uint32_t k = 0; k < rounds; ++k) {
+        const uint32_t u = k * kConsumers + uint32_t(tid);
+        const uint32_t e = UE * u;
+        if (e + UE <= cnt) {
+            uint4 o;
+            if constexpr (DT == SPLITZIP_BF16) {
                 const uint32_t nib = *reinterpret_cast<const uint32_t*>(nb + e / 2);
                 const uint2 sm = *reinterpret_cast<const uint2*>(sb + e);
-                __stcs(reinterpret_cast<uint4*>(out + e), decode_unit_bf16(nib, sm, lut2));
+                o = decode_unit_bf16(nib, sm, lut2);
+                __stcs(reinterpret_cast<uint4*>(static_cast<uint16_t*>(out_base) + g + e), o);
             } else {
-                const uint32_t valid = cnt - e;
+                // 6 bytes of s3 per unit, 2-byte aligned in the stage
+                const uint16_t* s16 = reinterpret_cast<const uint16_t*>(sb + 6u * u);
+                const uint2 nib = *reinterpret_cast<const uint2*>(nb + e / 2);
+                const uint32_t s3lo = uint32_t(s16[0]) | (uint32_t(s16[1]) << 16), s3hi = s16[2];
+                o = decode_unit_e5m2(nib, s3lo, s3hi, lut2);
+                __stcs(reinterpret_cast<uint4*>(static_cast<uint8_t*>(out_base) + g + e), o);
+            }
+        } else if (e < cnt) {
+            const uint32_t valid = cnt - e;
+            uint4 o;
+            if constexpr (DT == SPLITZIP_BF16) {
                 uint32_t nib = 0;
                 uint64_t smw = 0;
                 for (uint32_t b = 0; b < (valid + 1u) / 2u; ++b) nib |= uint32_t(nb[e / 2 + b]) << (8u * b);
                 for (uint32_t b = 0; b < valid; ++b) smw |= uint64_t(sb[e + b]) << (8u * b);
-                const uint4 o = decode_unit_bf16(nib, make_uint2(uint32_t(smw), uint32_t(smw >> 32)), lut2);
-                for (uint32_t k = 0; k < valid; ++k) {
-                    const uint32_t q = k >> 1;
-                    const uint32_t w = q == 0 ? o.x : q == 1 ? o.y : q == 2 ? o.z : o.w;
-                    out[e + k] = uint16_t(w >> (16u * (k & 1u)));
-                }
-            }
-        }
-    } else {
-        uint8_t* out = static_cast<uint8_t*>(out_base) + g;
-        const uint32_t units = (cnt + 15u) / 16u;
-#pragma unroll 2
-        for (uint32_t u = tid; u < units; u += kConsumers) {
-            const uint32_t e = 16u * u;
-            // 6 bytes of s3 per unit, 2-byte aligned in the stage
-            const uint16_t* s16 = reinterpret_cast<const uint16_t*>(sb + 6u * u);
-            if (e + 16u <= cnt) {
-                const uint2 nib = *reinterpret_cast<const uint2*>(nb + e / 2);
-                const uint32_t s3lo = uint32_t(s16[0]) | (uint32_t(s16[1]) << 16), s3hi = s16[2];
-                __stcs(reinterpret_cast<uint4*>(out + e), decode_unit_e5m2(nib, s3lo, s3hi, lut2));
+                o = decode_unit_bf16(nib, make_uint2(uint32_t(smw), uint32_t(smw >> 32)), lut2);
             } else {
-                const uint32_t valid = cnt - e;
                 uint64_t nw = 0, sw = 0;
                 for (uint32_t b = 0; b < (valid + 1u) / 2u; ++b) nw |= uint64_t(nb[e / 2 + b]) << (8u * b);
                 const uint8_t* s8 = sb + 6u * u;
                 for (uint32_t b = 0; b < 3u * ((valid + 7u) / 8u); ++b) sw |= uint64_t(s8[b]) << (8u * b);
-                const uint4 o = decode_unit_e5m2(make_uint2(uint32_t(nw), uint32_t(nw >> 32)), uint32_t(sw),
-                                                 uint32_t(sw >> 32), lut2);
-                for (uint32_t k = 0; k < valid; ++k) {
-                    const uint32_t q = k >> 2;
-                    const uint32_t w = q == 0 ? o.x : q == 1 ? o.y : q == 2 ? o.z : o.w;
-                    out[e + k] = uint8_t(w >> (8u * (k & 3u)));
-                }
+                o = decode_unit_e5m2(make_uint2(uint32_t(nw), uint32_t(nw >> 32)), uint32_t(sw), uint32_t(sw >> 32),
+                                     lut2);
+            }
+            for (uint32_t b = 0; b < valid; ++b) {
+                const uint32_t q = DT == SPLITZIP_BF16 ? b >> 1 : b >> 2;
+                const uint32_t w = q == 0 ? o.x : q == 1 ? o.y : q == 2 ? o.z : o.w;
+                if constexpr (DT == SPLITZIP_BF16)
+                    static_cast<uint16_t*>(out_base)[g + e + b] = uint16_t(w >> (16u * (b & 1u)));
+                else
+                    static_cast<uint8_t*>(out_base)[g + e + b] = uint8_t(w >> (8u * (b & 3u)));
             }
         }
     }
@@ -226,7 +228,7 @@ __device__ __forceinline__ bool patch_one(void* out, uint64_t base, uint32_t len
 __device__ __forceinline__ uint32_t rec_pos(const uint8_t* r) { return uint32_t(r[0]) | (uint32_t(r[1]) << 8); }
 
 template <int DT>
-__global__ void __launch_bounds__(kBlock) decode_kernel(const DecodeArgs a) {
+__global__ void __launch_bounds__(kBlock, kDecodeMinBlocks<DT>) decode_kernel(const DecodeArgs a) {
     extern __shared__ __align__(128) uint8_t stages[];
     __shared__ __align__(8) uint64_t full_bar[kStages];
     __shared__ __align__(8) uint64_t empty_bar[kStages];
@@ -338,9 +340,10 @@ __global__ void __launch_bounds__(kBlock) decode_kernel(const DecodeArgs a) {
             // records are sorted, so this sub-tile's are the next ones with
             // position < s0 + n_sub; the counting barrier also makes the
             // sub-tile's stores visible to every consumer
+            const uint32_t done = s0 + n_sub;
             while (true) {
                 const uint32_t i = cursor + tid;
-                const bool mine = i < cnt && rec_pos(recs + 3 * i) < s0 + n_sub;
+                const bool mine = i < cnt && rec_pos(recs + 3 * i) < done;
                 const uint32_t n_in = named_barrier_popc(1, kConsumers, mine);
                 if (mine) {
                     const int64_t prev = i == 0 ? -1 : int64_t(rec_pos(recs + 3 * (i - 1)));
