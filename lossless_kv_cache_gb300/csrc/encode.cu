@@ -58,15 +58,19 @@ static_assert(kConsumers * kThreadBytes == kTileBytes, "one tile = 64 bytes per 
 // element within its group of four consecutive elements):
 //   bits 16 + 4k .. 19 + 4k  the element's code (0 when it escapes)
 //   bit  12 + k              the element's escape flag
-//   bits 3k .. 3k + 2        E5M2 only: the element's 3-bit sign|mantissa
-// The four entries of a group have disjoint bits, so their sum is the group's
-// two nibble bytes (bits 16..31, even element in the low nibble), its escape
-// mask (bits 12..15) and its 12 bits of packed sign|mantissa (bits 0..11).
+//   bits 3k .. 3k + 1        E5M2 only: the element's 2 mantissa bits
+// BF16 tables are indexed by the exponent, E5M2 tables by the byte without
+// its sign (exponent and mantissa: 128 entries, so elements that differ only
+// in sign hit the same entry instead of another bank).  The four entries of a
+// group have disjoint bits, so their sum -- plus, for E5M2, the four sign bits
+// moved to bits 3k + 2 -- is the group's two nibble bytes (bits 16..31, even
+// element in the low nibble), its escape mask (bits 12..15) and its 12 bits of
+// packed 3-bit sign|mantissa values (bits 0..11).
 __device__ __forceinline__ uint32_t table_entry(int dtype, int k, uint32_t index, const uint8_t* code) {
     uint32_t e = index, s3 = 0;
-    if (dtype != SPLITZIP_BF16) {  // index = the whole E5M2 byte
+    if (dtype != SPLITZIP_BF16) {  // index = exponent << 2 | mantissa
         e = (index >> 2) & 31u;
-        s3 = ((index >> 7) << 2) | (index & 3u);
+        s3 = index & 3u;
     }
     const uint32_t t = code[e];
     const uint32_t c = (t & kEscapeFlag) ? (1u << (12 + k)) : (uint32_t(t & 15u) << (16 + 4 * k));
@@ -85,10 +89,15 @@ __device__ __forceinline__ uint32_t group_bf16(const uint32_t* tab, uint32_t x, 
            tab_at(tab, 2, (y >> 5) & 0x3FCu) + tab_at(tab, 3, (y >> 21) & 0x3FCu);
 }
 
-// E5M2: the group of four elements in word w; the table index is the byte.
+// E5M2: the group of four elements in word w.  The sign of byte k (bit
+// 8k + 7) belongs at bit 3k + 2: the high word of (signs * 0x08421000) has it
+// there (term k is shifted by 27 - 5k), and every other product term lands on
+// a bit of its own (checked for all 16 terms: no carries), so one mask keeps
+// exactly the four signs.
 __device__ __forceinline__ uint32_t group_e5m2(const uint32_t* tab, uint32_t w) {
-    return tab_at(tab, 0, (w << 2) & 0x3FCu) + tab_at(tab, 1, (w >> 6) & 0x3FCu) +
-           tab_at(tab, 2, (w >> 14) & 0x3FCu) + tab_at(tab, 3, (w >> 22) & 0x3FCu);
+    const uint32_t signs = __umulhi(w & 0x80808080u, 0x08421000u) & 0x924u;
+    return tab_at(tab, 0, (w << 2) & 0x1FCu) + tab_at(tab, 1, (w >> 6) & 0x1FCu) +
+           tab_at(tab, 2, (w >> 14) & 0x1FCu) + tab_at(tab, 3, (w >> 22) & 0x1FCu) + signs;
 }
 
 // Stage position of byte L of a tile: the tensor-map copy stores every
