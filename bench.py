@@ -18,6 +18,7 @@ Under torchrun each rank encodes/decodes its own copy of the workload (chunks
 are independent, no data exchange): weak scaling, max time over ranks.
 """
 import argparse
+import faulthandler
 import json
 import os
 import statistics
@@ -389,8 +390,8 @@ def run_ours(args, world, rank, local):
     else:
         name, alg, ms = "decode_kernel<%s>" % tag, alg_decode, dec_ms
     achieved = alg / (ms * 1e-3) / 1e9
-    op = "encode" if enc_ms >= dec_ms else "decode"
-    traffic, traffic_src = measured_traffic(wl.name if wl.layers in (None, 32) else None, op)
+    slower = "encode" if enc_ms >= dec_ms else "decode"
+    traffic, traffic_src = measured_traffic(wl.name if wl.layers in (None, 32) else None, slower)
     roofline = {"bound": "hbm", "kernel": name, "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
                 "frac": round(achieved / hbm, 4), "peak_source": "%s hbm_gbs (copy)" % peak_kind,
                 "algorithmic_bytes_per_launch": alg, "traffic": traffic}
@@ -468,11 +469,12 @@ def run_ours(args, world, rank, local):
         "escape_rate": round(E / n, 6), "verified_bit_exact": verified,
         "per_kernel": per_kernel, "link_model": link,
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clk,
-        "gpu_launches": 4 * K,  # encode: streaming, index, records kernels; decode: one kernel
+        "gpu_launches": 5 * K,  # encode: streaming, group, index, records kernels; decode: one kernel
     }
 
 
 def main():
+    faulthandler.enable()  # a native crash prints the Python stack of every thread
     args = parse_args()
     world, rank, local = dist_setup()
     if args.impl == "reference":

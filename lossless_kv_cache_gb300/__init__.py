@@ -65,7 +65,29 @@ class Header(ctypes.Structure):
     ]
 
 
-_u64, _u32, _int, _vp = ctypes.c_uint64, ctypes.c_uint32, ctypes.c_int, ctypes.c_void_p
+class _Address(ctypes.c_void_p):
+    """A pointer argument: an integer address, None (NULL), or an object with
+    data_ptr() (a torch tensor).  Anything else -- notably a str or bytes, which
+    plain c_void_p would turn into the address of its host buffer -- is a
+    TypeError, so a wrong value never reaches a kernel as an address."""
+
+    @classmethod
+    def from_param(cls, obj):
+        if obj is None or isinstance(obj, bool):
+            if obj is None:
+                return None
+            raise TypeError("pointer argument: expected an address, got bool")
+        if isinstance(obj, int):
+            return ctypes.c_void_p(obj)
+        if isinstance(obj, ctypes.c_void_p):
+            return obj
+        if hasattr(obj, "data_ptr"):
+            return ctypes.c_void_p(obj.data_ptr())
+        raise TypeError("pointer argument: expected an integer address, None or a tensor, got %s"
+                        % type(obj).__name__)
+
+
+_u64, _u32, _int, _vp = ctypes.c_uint64, ctypes.c_uint32, ctypes.c_int, _Address
 _P_u64 = ctypes.POINTER(ctypes.c_uint64)
 
 # name -> (restype, argtypes); mirrors include/splitzip.h

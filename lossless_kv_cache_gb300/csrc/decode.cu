@@ -282,10 +282,13 @@ __global__ void __launch_bounds__(kBlock, kDecodeMinBlocks<DT>) decode_kernel(co
             const uint32_t rb = ci & 1u;
             if (ci >= 2 && !mbar_wait(&rec_empty[rb], ((ci >> 1) - 1) & 1u)) report(a.status, SPLITZIP_ERR_TIMEOUT);
             const uint64_t off = offsets[c], cnt = counts[c];
-            // only a range that lies inside the escape stream is copied; the
-            // consumers check the index entry in full
-            if (cnt > 0 && cnt <= kRecCap && cnt <= len && off <= E && cnt <= E - off) {
-                const Window w = window_of(records + 3 * off, 3 * cnt);
+            // only a range that lies inside the escape stream is copied, and
+            // only when its 16-byte-aligned window stays inside the caller's
+            // buffer (the stream ends the container unpadded); the consumers
+            // check the index entry in full
+            const Window w = window_of(records + 3 * min(off, E), 3 * min(cnt, uint64_t(kRecCap)));
+            if (cnt > 0 && cnt <= kRecCap && cnt <= len && off <= E && cnt <= E - off &&
+                w.src + w.bytes <= in + a.in_bytes) {
                 rec_offset[rb] = w.offset;
                 mbar_arrive_expect_tx(&rec_full[rb], w.bytes);
                 bulk_load(rec_buf[rb], w.src, w.bytes, &rec_full[rb]);

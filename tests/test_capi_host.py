@@ -167,3 +167,21 @@ def test_parse_header_matches_oracle(splitzip_lib):
         buf = np.ascontiguousarray(bad)
         st = sz.splitzip_parse_header(buf.ctypes.data, buf.size, sz.Header())
         assert (st == sz.OK) == (o_st == oracle.OK), name
+
+
+def test_pointer_arguments_reject_non_addresses(splitzip_lib):
+    # a str or bytes must never reach the library as an address (plain
+    # c_void_p would pass the address of the object's host buffer)
+    cb = sz.Codebook.make(sz.BF16, range(16))
+    for bad in ("encode", b"\x00" * 16, 1.5, True):
+        with pytest.raises(ctypes.ArgumentError):
+            sz.splitzip_encode(1 << 20, 8, sz.BF16, cb, 65536, bad, 1 << 20, 1 << 20, 1 << 20, 1 << 20, 1 << 20, 0)
+        with pytest.raises(ctypes.ArgumentError):
+            sz.splitzip_decode(bad, 1 << 20, 1 << 20, 8, sz.BF16, 1 << 20, 0)
+    # integers, None and objects with data_ptr() are addresses
+    class T:
+        def data_ptr(self):
+            return 1 << 20
+    assert sz._Address.from_param(None) is None
+    assert sz._Address.from_param(T()).value == 1 << 20
+    assert sz._Address.from_param(1 << 40).value == 1 << 40
