@@ -216,8 +216,7 @@ class Workload:
 
     def make(self, seed, device):
         if self.layered:
-            _, layer = self.W.layers_of(self.name)
-            return torch.cat([layer(seed, l, device) for l in range(self.layers)])
+            return self.W.make_layers(self.name, seed, self.layers, device)
         return self.W.make(self.name, seed, device)
 
     def calibration(self, device):
@@ -470,7 +469,7 @@ def run_ours(args, world, rank, local):
         "metric": METRIC, "value": round(value, 3), "unit": "GB/s", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "u16" if dtype == 0 else "u8",
-        "data": "synthetic (seeded torch CUDA generator; recipe of the workload module)",
+        "data": "synthetic (seeded torch CPU generator, rounded on the GPU; recipe of the workload module)",
         "config": wl.config(world),
         "encode_gbs": round(enc_gbs, 2), "decode_gbs": round(dec_gbs, 2),
         "encode_hbm_frac": round(alg_encode / (enc_ms * 1e-3) / 1e9 / hbm, 4),

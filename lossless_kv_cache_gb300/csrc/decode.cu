@@ -124,17 +124,23 @@ constexpr uint32_t kSub = 8192;
 constexpr uint32_t kNibCap = kSub / 2 + 32;  // + room for a 16-byte window shift
 constexpr uint32_t kSmCap = kSub + 32;
 constexpr uint32_t kStageBytes = (kNibCap + kSmCap + 127u) & ~127u;
-constexpr uint32_t kDecodeSmem = kStages * kStageBytes;
+constexpr uint32_t kRingBytes = kStages * kStageBytes;
 // A chunk's escape records are brought into shared memory with one bulk copy
-// when they fit (at most kRecCap records, 1.2 % of a 65,536-element chunk), so
-// each sub-tile is patched right after its stores, while its lines are still
-// in L2; a chunk with more escapes is patched from global memory instead.
-constexpr uint32_t kRecCap = 768;
+// when they fit (at most kRecCap records: BF16 8,192 = 12.5 % of a 65,536-element
+// chunk, E5M2 2,048 = 3.1 %, within each dtype's shared-memory budget at its
+// CTAs per SM);
+// a chunk with more escapes reads them from the escape stream instead.  Either
+// way each sub-tile is patched right after its stores, while its lines are
+// still in L2.
+template <int DT> constexpr uint32_t kRecCap = DT == SPLITZIP_BF16 ? 8192u : 2048u;
 // Resident CTAs per SM the kernel is compiled for (register budget): BF16
 // runs fastest at 2 with ~90 registers a thread, E5M2 at 3 (measured: BF16
 // 1.18 ms at 2 vs 1.24 ms at 4; E5M2 1.50 ms at 3 vs 1.71 ms at 2).
 template <int DT> constexpr int kDecodeMinBlocks = DT == SPLITZIP_BF16 ? 2 : 3;
-constexpr uint32_t kRecBytes = 3 * kRecCap + 32;  // + room for a 16-byte window shift
+// per buffer: 3 bytes a record + room for a 16-byte window shift
+template <int DT> constexpr uint32_t kRecBytes = 3 * kRecCap<DT> + 32;
+// dynamic shared memory: the sub-tile ring, then two record buffers
+template <int DT> constexpr uint32_t kDecodeSmem = kRingBytes + 2 * kRecBytes<DT>;
 
 struct SubTile {
     Window nib, sm;
@@ -211,16 +217,30 @@ __device__ __forceinline__ void decode_subtile(const uint8_t* nb, const uint8_t*
 
 // Escape-record check and patch of one element (returns false on a corrupt
 // record).  `prev` is the previous record's position in the chunk (or -1).
+// The exponent field is rewritten with two atomic reductions on the 32-bit
+// word that holds the element (AND clears the field, OR sets it; the results
+// are unused, so neither waits for memory, and one thread's two operations on
+// one address stay in order).  Other elements of the word are left as they
+// are; a word that would reach past the output's last byte (only at the very
+// end of an odd-sized output) is patched by a plain read-modify-write.
 template <int DT>
-__device__ __forceinline__ bool patch_one(void* out, uint64_t base, uint32_t len, int64_t prev, uint32_t pos,
-                                          uint32_t ex) {
+__device__ __forceinline__ bool patch_one(void* out, uint64_t n, uint64_t base, uint32_t len, int64_t prev,
+                                          uint32_t pos, uint32_t ex) {
     if (pos >= len || int64_t(pos) <= prev || ex >= (DT == SPLITZIP_BF16 ? 256u : 32u)) return false;
-    if constexpr (DT == SPLITZIP_BF16) {
-        uint16_t* o = static_cast<uint16_t*>(out) + base + pos;
-        *o = uint16_t((*o & 0x807Fu) | (ex << 7));
+    constexpr uint32_t EB = DT == SPLITZIP_BF16 ? 2u : 1u;
+    const uint64_t byte = (base + pos) * EB;
+    uint8_t* o = static_cast<uint8_t*>(out);
+    if ((byte | 3u) < n * EB) {
+        const uint32_t sh = uint32_t(byte & 3u) * 8u + (DT == SPLITZIP_BF16 ? 7u : 2u);
+        const uint32_t field = (DT == SPLITZIP_BF16 ? 0xFFu : 0x1Fu) << sh;
+        unsigned int* w = reinterpret_cast<unsigned int*>(o + (byte & ~uint64_t(3)));
+        atomicAnd(w, ~field);
+        atomicOr(w, ex << sh);
+    } else if constexpr (DT == SPLITZIP_BF16) {
+        uint16_t* e = reinterpret_cast<uint16_t*>(o + byte);
+        *e = uint16_t((*e & 0x807Fu) | (ex << 7));
     } else {
-        uint8_t* o = static_cast<uint8_t*>(out) + base + pos;
-        *o = uint8_t((*o & 0x83u) | (ex << 2));
+        o[byte] = uint8_t((o[byte] & 0x83u) | (ex << 2));
     }
     return true;
 }
@@ -234,7 +254,8 @@ __global__ void __launch_bounds__(kBlock, kDecodeMinBlocks<DT>) decode_kernel(co
     __shared__ __align__(8) uint64_t empty_bar[kStages];
     __shared__ __align__(8) uint64_t rec_full[2];
     __shared__ __align__(8) uint64_t rec_empty[2];
-    __shared__ __align__(16) uint8_t rec_buf[2][kRecBytes];
+    // record buffer b (0, 1) of the double buffer
+    auto rec_buf = [&](uint32_t b) { return stages + kRingBytes + b * kRecBytes<DT>; };
     __shared__ uint32_t rec_offset[2];  // window shift of the records in rec_buf, or kNoRecords
     __shared__ Header hdr;
     __shared__ int header_ok;
@@ -286,12 +307,12 @@ __global__ void __launch_bounds__(kBlock, kDecodeMinBlocks<DT>) decode_kernel(co
             // only when its 16-byte-aligned window stays inside the caller's
             // buffer (the stream ends the container unpadded); the consumers
             // check the index entry in full
-            const Window w = window_of(records + 3 * min(off, E), 3 * min(cnt, uint64_t(kRecCap)));
-            if (cnt > 0 && cnt <= kRecCap && cnt <= len && off <= E && cnt <= E - off &&
+            const Window w = window_of(records + 3 * min(off, E), 3 * min(cnt, uint64_t(kRecCap<DT>)));
+            if (cnt > 0 && cnt <= kRecCap<DT> && cnt <= len && off <= E && cnt <= E - off &&
                 w.src + w.bytes <= in + a.in_bytes) {
                 rec_offset[rb] = w.offset;
                 mbar_arrive_expect_tx(&rec_full[rb], w.bytes);
-                bulk_load(rec_buf[rb], w.src, w.bytes, &rec_full[rb]);
+                bulk_load(rec_buf(rb), w.src, w.bytes, &rec_full[rb]);
             } else {
                 rec_offset[rb] = cnt == 0 ? 0u : kNoRecords;
                 mbar_arrive(&rec_full[rb]);
@@ -326,10 +347,29 @@ __global__ void __launch_bounds__(kBlock, kDecodeMinBlocks<DT>) decode_kernel(co
                               (c + 1 < C || off + cnt == E);
         if (!mbar_wait(&rec_full[rb], (ci >> 1) & 1u)) report(a.status, SPLITZIP_ERR_TIMEOUT);
         const uint32_t shift = rec_offset[rb];
-        const bool in_smem = index_ok && shift != kNoRecords;  // the same in every consumer
-        const uint8_t* recs = rec_buf[rb] + (in_smem ? shift : 0u);
+        // the chunk's records: in shared memory when they fit, else read from
+        // the escape stream; either way each sub-tile is patched right after
+        // its stores (the same decision in every consumer)
+        const bool in_smem = index_ok && shift != kNoRecords;
+        const bool patch = index_ok && cnt > 0;
         uint32_t cursor = 0;  // records of this chunk already applied
         bool bad = false;
+        // records are sorted, so a sub-tile's are the next ones with position
+        // < end; the counting barrier also makes the sub-tile's stores visible
+        // to every consumer
+        auto patch_upto = [&](const uint8_t* recs, uint32_t end) {
+            while (true) {
+                const uint32_t i = cursor + tid;
+                const bool mine = i < cnt && rec_pos(recs + 3 * i) < end;
+                const uint32_t n_in = named_barrier_popc(1, kConsumers, mine);
+                if (mine) {
+                    const int64_t prev = i == 0 ? -1 : int64_t(rec_pos(recs + 3 * (i - 1)));
+                    bad |= !patch_one<DT>(a.out, a.n, base, len, prev, rec_pos(recs + 3 * i), recs[3 * i + 2]);
+                }
+                cursor += n_in;
+                if (n_in < kConsumers) break;
+            }
+        };
         for (uint32_t s0 = 0; s0 < len; s0 += sub, ++it) {
             const uint32_t stage = it % kStages, use = it / kStages;
             const uint32_t n_sub = min(sub, len - s0);
@@ -339,36 +379,15 @@ __global__ void __launch_bounds__(kBlock, kDecodeMinBlocks<DT>) decode_kernel(co
             decode_subtile<DT>(src + t.nib.offset, src + kNibCap + t.sm.offset, a.out, base + s0, n_sub, tid, lut2);
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty_bar[stage]);
-            if (!in_smem) continue;
-            // records are sorted, so this sub-tile's are the next ones with
-            // position < s0 + n_sub; the counting barrier also makes the
-            // sub-tile's stores visible to every consumer
-            const uint32_t done = s0 + n_sub;
-            while (true) {
-                const uint32_t i = cursor + tid;
-                const bool mine = i < cnt && rec_pos(recs + 3 * i) < done;
-                const uint32_t n_in = named_barrier_popc(1, kConsumers, mine);
-                if (mine) {
-                    const int64_t prev = i == 0 ? -1 : int64_t(rec_pos(recs + 3 * (i - 1)));
-                    bad |= !patch_one<DT>(a.out, base, len, prev, rec_pos(recs + 3 * i), recs[3 * i + 2]);
-                }
-                cursor += n_in;
-                if (n_in < kConsumers) break;
-            }
+            if (!patch) continue;
+            if (in_smem)
+                patch_upto(rec_buf(rb) + shift, s0 + n_sub);
+            else
+                patch_upto(records + 3 * off, s0 + n_sub);
         }
-        if (in_smem && cursor != cnt) bad = true;  // a record outside the chunk or out of order
+        if (patch && cursor != cnt) bad = true;  // a record outside the chunk or out of order
         if (bad) report(a.status, SPLITZIP_ERR_CORRUPT);
-        if (!index_ok) {
-            if (tid == 0) report(a.status, SPLITZIP_ERR_CORRUPT);
-        } else if (!in_smem && cnt > 0) {
-            // too many escapes for shared memory: patch the chunk from global memory
-            named_barrier(1, kConsumers);  // the chunk's dense stores are visible to all consumers
-            for (uint64_t i = tid; i < cnt; i += kConsumers) {
-                const uint8_t* r = records + 3 * (off + i);
-                const int64_t prev = i == 0 ? -1 : int64_t(rec_pos(r - 3));
-                if (!patch_one<DT>(a.out, base, len, prev, rec_pos(r), r[2])) report(a.status, SPLITZIP_ERR_CORRUPT);
-            }
-        }
+        if (!index_ok && tid == 0) report(a.status, SPLITZIP_ERR_CORRUPT);
         __syncwarp();
         if (lane == 0) mbar_arrive(&rec_empty[rb]);
     }
@@ -378,18 +397,20 @@ __global__ void __launch_bounds__(kBlock, kDecodeMinBlocks<DT>) decode_kernel(co
 
 cudaError_t launch_decode(const DecodeArgs& a, int grid, cudaStream_t s) {
     if (a.dtype == SPLITZIP_BF16)
-        decode_kernel<SPLITZIP_BF16><<<grid, kBlock, kDecodeSmem, s>>>(a);
+        decode_kernel<SPLITZIP_BF16><<<grid, kBlock, kDecodeSmem<SPLITZIP_BF16>, s>>>(a);
     else
-        decode_kernel<SPLITZIP_FP8_E5M2><<<grid, kBlock, kDecodeSmem, s>>>(a);
+        decode_kernel<SPLITZIP_FP8_E5M2><<<grid, kBlock, kDecodeSmem<SPLITZIP_FP8_E5M2>, s>>>(a);
     return cudaGetLastError();
 }
 
 // Also raises the kernels' dynamic shared-memory limit (once per device).
 cudaError_t occupancy_decode(int* blocks_per_sm, int dtype) {
     auto k = dtype == SPLITZIP_BF16 ? decode_kernel<SPLITZIP_BF16> : decode_kernel<SPLITZIP_FP8_E5M2>;
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kDecodeSmem));
+    const int smem =
+        int(dtype == SPLITZIP_BF16 ? kDecodeSmem<SPLITZIP_BF16> : kDecodeSmem<SPLITZIP_FP8_E5M2>);
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, k, kBlock, kDecodeSmem);
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, k, kBlock, smem);
 }
 
 }  // namespace splitzip

@@ -359,6 +359,20 @@ __global__ void __launch_bounds__(kBlock, kMinBlocks<DT>)
                 if (lane >= d) incl += y;
             }
             if (lane == 31) a.warp_counts[tile * kEncodeWarps + warp] = incl;
+            // the bits of element b of this thread, and its staged record
+            auto element_bits = [&](uint32_t b) -> uint32_t {
+                const uint32_t e = my_elem + b;  // element of the tile
+                const uint32_t B = e * EB;       // its first byte in the tile
+                if (FULL || B + EB <= in_stage)
+                    return DT == SPLITZIP_BF16 ? uint32_t(*reinterpret_cast<const uint16_t*>(st + swizzled(B)))
+                                               : uint32_t(st[swizzled(B)]);
+                return DT == SPLITZIP_BF16 ? uint32_t(reinterpret_cast<const uint16_t*>(in)[base + e])
+                                           : uint32_t(in[base + e]);
+            };
+            auto record = [&](uint32_t b, uint32_t x) -> uint32_t {
+                const uint32_t exponent = DT == SPLITZIP_BF16 ? (x >> 7) & 0xFFu : (x >> 2) & 0x1Fu;
+                return ((pos0 + my_elem + b) << 8) | exponent;
+            };
             if (cnt) {
                 uint32_t* slot = a.staging + tile * a.tile_elems + (incl - cnt) * stride + warp;
 #pragma unroll
@@ -368,21 +382,20 @@ __global__ void __launch_bounds__(kBlock, kMinBlocks<DT>)
                         m = o.mask;
                     else
                         m = o.mask[h];
+                    // two escapes per round, so their two exponent reads overlap
                     while (m) {
-                        const uint32_t b = 32u * h + uint32_t(__ffs(m) - 1);
+                        const uint32_t b0 = 32u * h + uint32_t(__ffs(m) - 1);
                         m &= m - 1u;
-                        const uint32_t e = my_elem + b;  // element of the tile
-                        const uint32_t B = e * EB;       // its first byte in the tile
-                        uint32_t x;
-                        if (FULL || B + EB <= in_stage)
-                            x = DT == SPLITZIP_BF16 ? uint32_t(*reinterpret_cast<const uint16_t*>(st + swizzled(B)))
-                                                    : uint32_t(st[swizzled(B)]);
-                        else
-                            x = DT == SPLITZIP_BF16 ? uint32_t(reinterpret_cast<const uint16_t*>(in)[base + e])
-                                                    : uint32_t(in[base + e]);
-                        const uint32_t exponent = DT == SPLITZIP_BF16 ? (x >> 7) & 0xFFu : (x >> 2) & 0x1Fu;
-                        *slot = ((pos0 + e) << 8) | exponent;
+                        const bool two = m != 0u;
+                        const uint32_t b1 = two ? 32u * h + uint32_t(__ffs(m) - 1) : b0;
+                        m &= two ? m - 1u : m;
+                        const uint32_t x0 = element_bits(b0), x1 = element_bits(b1);
+                        *slot = record(b0, x0);
                         slot += stride;
+                        if (two) {
+                            *slot = record(b1, x1);
+                            slot += stride;
+                        }
                     }
                 }
             }
@@ -534,7 +547,10 @@ __global__ void __launch_bounds__(kRecordThreads) encode_records_kernel(const En
                 if (i >= first_w) w += step;
             }
             const uint32_t first_w = __shfl_sync(kFull, o, 8 * k + int(w));
-            v[k] = i < tot[k] ? __ldcs(a.staging + (t0 + k) * a.tile_elems + (i - first_w) * stride + w) : 0u;
+            // a plain load: the 32-byte sector of record j holds the j-th record
+            // of every warp of the tile, read by other lanes in other rounds, so it
+            // must stay in L2 (an evict-first load re-read it from DRAM each time)
+            v[k] = i < tot[k] ? a.staging[(t0 + k) * a.tile_elems + (i - first_w) * stride + w] : 0u;
         }
 #pragma unroll
         for (int k = 0; k < kRecordTiles; ++k) {

@@ -12,7 +12,11 @@ tensors below stand in for them.  Layout is contiguous
 
 Every tensor is returned as raw bits: BF16 as torch.int16, E5M2 as torch.uint8.
 Per-layer generators use seed ``seed * 1000 + layer`` so a 32-layer cache can be
-produced one layer at a time.
+produced one layer at a time.  The random numbers are always drawn with the CPU
+generator (torch.Generator on the CPU, the seeds above), whatever device the
+result is for; the 32-layer caches are then moved to the device as float32 and
+rounded there (round to nearest even, no saturation: the same result as on the
+CPU), one layer at a time.
 """
 import torch
 
@@ -75,11 +79,11 @@ def kv_cache_layer_f32(seed, layer, tokens, device="cpu"):
 
 
 def kv_cache_layer_bf16(seed, layer, tokens=32768, device="cpu"):
-    return to_bf16_bits(kv_cache_layer_f32(seed, layer, tokens, device)).reshape(-1)
+    return to_bf16_bits(kv_cache_layer_f32(seed, layer, tokens).to(device)).reshape(-1)
 
 
 def kv_cache_layer_e5m2(seed, layer, tokens=65536, device="cpu"):
-    return to_e5m2_bits(kv_cache_layer_f32(seed, layer, tokens, device)).reshape(-1)
+    return to_e5m2_bits(kv_cache_layer_f32(seed, layer, tokens).to(device)).reshape(-1)
 
 
 def escape_stress(seed, chunks=64, chunk_elems=65536, sigma=3.0, device="cpu"):
@@ -144,15 +148,29 @@ def layers_of(name):
 
 
 def make(name, seed, device="cpu"):
-    """Whole tensor of a workload (raw bits, flat)."""
+    """Whole tensor of a workload (raw bits, flat), on `device`; drawn with the
+    CPU generator."""
     if name == "kv_tile_1x1024x8x128_bf16":
-        return kv_tile_k_only(seed, device=device)
+        return kv_tile_k_only(seed).to(device)
     if name == "llama_layer_2x8192x8x128_bf16":
-        return llama_layer_kv(seed, device=device)
+        return llama_layer_kv(seed).to(device)
     if name == "escape_stress_64x65536_bf16":
-        return escape_stress(seed, device=device)
+        return escape_stress(seed).to(device)
     n_layers, layer = layers_of(name)
-    return torch.cat([layer(seed, l, device) for l in range(n_layers)])
+    return make_layers(name, seed, n_layers, device)
+
+
+def make_layers(name, seed, n_layers, device="cpu"):
+    """The first n_layers layers of a 32-layer cache, filled one layer at a time."""
+    _, layer = layers_of(name)
+    first = layer(seed, 0, device)
+    out = torch.empty(n_layers * first.numel(), dtype=first.dtype, device=device)
+    out[: first.numel()].copy_(first)
+    del first
+    per = out.numel() // n_layers
+    for l in range(1, n_layers):
+        out[l * per: (l + 1) * per].copy_(layer(seed, l, device))
+    return out
 
 
 def calibration_tensor(name, device="cpu"):

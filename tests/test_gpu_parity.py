@@ -260,8 +260,8 @@ def _layout(n, dtype, chunk, E):
 
 def _full_size_check(name, sample_chunks=12):
     dtype = W.dtype_of(name)
-    n_layers, layer = W.layers_of(name)
-    x = torch.cat([layer(0, l, DEV) for l in range(n_layers)])
+    n_layers, _ = W.layers_of(name)
+    x = W.make_layers(name, 0, n_layers, DEV)
     n = x.numel()
     assert n == W.numel(name)
     cal = W.calibration_tensor(name, DEV)
