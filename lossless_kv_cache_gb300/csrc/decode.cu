@@ -122,17 +122,18 @@ constexpr int kBlock = kConsumers + 32;  // + one producer warp
 constexpr int kStages = 4;
 constexpr uint32_t kSub = 8192;
 constexpr uint32_t kNibCap = kSub / 2 + 32;  // + room for a 16-byte window shift
-constexpr uint32_t kSmCap = kSub + 32;
-constexpr uint32_t kStageBytes = (kNibCap + kSmCap + 127u) & ~127u;
-constexpr uint32_t kRingBytes = kStages * kStageBytes;
+// sign|mantissa bytes of a sub-tile: BF16 one per element, E5M2 3 per 8 elements
+template <int DT> constexpr uint32_t kSmCap = (DT == SPLITZIP_BF16 ? kSub : 3 * kSub / 8) + 32;
+template <int DT> constexpr uint32_t kStageBytes = (kNibCap + kSmCap<DT> + 127u) & ~127u;
+template <int DT> constexpr uint32_t kRingBytes = kStages * kStageBytes<DT>;
 // A chunk's escape records are brought into shared memory with one bulk copy
 // when they fit (at most kRecCap records: BF16 8,192 = 12.5 % of a 65,536-element
-// chunk, E5M2 2,048 = 3.1 %, within each dtype's shared-memory budget at its
+// chunk, E5M2 6,144 = 9.4 %, within each dtype's shared-memory budget at its
 // CTAs per SM);
 // a chunk with more escapes reads them from the escape stream instead.  Either
 // way each sub-tile is patched right after its stores, while its lines are
 // still in L2.
-template <int DT> constexpr uint32_t kRecCap = DT == SPLITZIP_BF16 ? 8192u : 2048u;
+template <int DT> constexpr uint32_t kRecCap = DT == SPLITZIP_BF16 ? 8192u : 6144u;
 // Resident CTAs per SM the kernel is compiled for (register budget): BF16
 // runs fastest at 2 with ~90 registers a thread, E5M2 at 3 (measured: BF16
 // 1.18 ms at 2 vs 1.24 ms at 4; E5M2 1.50 ms at 3 vs 1.71 ms at 2).
@@ -140,7 +141,7 @@ template <int DT> constexpr int kDecodeMinBlocks = DT == SPLITZIP_BF16 ? 2 : 3;
 // per buffer: 3 bytes a record + room for a 16-byte window shift
 template <int DT> constexpr uint32_t kRecBytes = 3 * kRecCap<DT> + 32;
 // dynamic shared memory: the sub-tile ring, then two record buffers
-template <int DT> constexpr uint32_t kDecodeSmem = kRingBytes + 2 * kRecBytes<DT>;
+template <int DT> constexpr uint32_t kDecodeSmem = kRingBytes<DT> + 2 * kRecBytes<DT>;
 
 struct SubTile {
     Window nib, sm;
@@ -255,7 +256,7 @@ __global__ void __launch_bounds__(kBlock, kDecodeMinBlocks<DT>) decode_kernel(co
     __shared__ __align__(8) uint64_t rec_full[2];
     __shared__ __align__(8) uint64_t rec_empty[2];
     // record buffer b (0, 1) of the double buffer
-    auto rec_buf = [&](uint32_t b) { return stages + kRingBytes + b * kRecBytes<DT>; };
+    auto rec_buf = [&](uint32_t b) { return stages + kRingBytes<DT> + b * kRecBytes<DT>; };
     __shared__ uint32_t rec_offset[2];  // window shift of the records in rec_buf, or kNoRecords
     __shared__ Header hdr;
     __shared__ int header_ok;
@@ -321,7 +322,7 @@ __global__ void __launch_bounds__(kBlock, kDecodeMinBlocks<DT>) decode_kernel(co
                 const uint32_t stage = it % kStages, use = it / kStages;
                 if (use > 0 && !mbar_wait(&empty_bar[stage], (use - 1) & 1u)) report(a.status, SPLITZIP_ERR_TIMEOUT);
                 const SubTile t = subtile_windows<DT>(nibbles, signmant, base + s0, min(sub, len - s0));
-                uint8_t* dst = stages + stage * kStageBytes;
+                uint8_t* dst = stages + stage * kStageBytes<DT>;
                 mbar_arrive_expect_tx(&full_bar[stage], t.nib.bytes + t.sm.bytes);
                 bulk_load(dst, t.nib.src, t.nib.bytes, &full_bar[stage]);
                 bulk_load(dst + kNibCap, t.sm.src, t.sm.bytes, &full_bar[stage]);
@@ -375,7 +376,7 @@ __global__ void __launch_bounds__(kBlock, kDecodeMinBlocks<DT>) decode_kernel(co
             const uint32_t n_sub = min(sub, len - s0);
             if (!mbar_wait(&full_bar[stage], use & 1u)) report(a.status, SPLITZIP_ERR_TIMEOUT);
             const SubTile t = subtile_windows<DT>(nibbles, signmant, base + s0, n_sub);
-            const uint8_t* src = stages + stage * kStageBytes;
+            const uint8_t* src = stages + stage * kStageBytes<DT>;
             decode_subtile<DT>(src + t.nib.offset, src + kNibCap + t.sm.offset, a.out, base + s0, n_sub, tid, lut2);
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty_bar[stage]);

@@ -18,11 +18,10 @@
 //     positions, so the sum of four entries is the group's two nibble bytes,
 //     its escape flags and (E5M2) its packed 3-bit sign|mantissa values.  The
 //     nibble and sign|mantissa streams go out with 16-byte stores; a warp scan
-//     orders the warp's escapes and the warp stages them in the tile's slot,
-//     interleaved with the other warps' (record j of warp w at j * S + w, S =
-//     the tile's warps with elements), so a tile's records share a few
-//     sectors without any synchronisation between the warps; the warp's count
-//     goes to the workspace.
+//     orders the warp's escapes, each thread writes its own contiguously into
+//     the warp's region of the tile's staging slot after those of the lower
+//     lanes, and the warp's count goes to the workspace; no synchronisation
+//     between the warps.
 //   encode_group_kernel (one CTA per group of 256 tiles): the group's total.
 //   encode_index_kernel (one CTA per group of 256 tiles): the sum of the
 //     earlier groups' totals plus a block scan of the group's tile counts give
@@ -249,7 +248,6 @@ __global__ void __launch_bounds__(kBlock, kMinBlocks<DT>)
     uint8_t* nibbles = a.out + L0.nibble_off;
     uint8_t* signmant = a.out + L0.signmant_off;
     const uint32_t my_byte = kThreadBytes * uint32_t(tid);
-    const uint32_t stride = staging_stride(a.tile_elems, EB);
     const uint32_t my_elem = my_byte / EB;  // first element of the thread in a tile
     uint32_t piece_off[4];                  // stage offsets of the thread's four 16-byte pieces
 #pragma unroll
@@ -373,8 +371,10 @@ __global__ void __launch_bounds__(kBlock, kMinBlocks<DT>)
                 const uint32_t exponent = DT == SPLITZIP_BF16 ? (x >> 7) & 0xFFu : (x >> 2) & 0x1Fu;
                 return ((pos0 + my_elem + b) << 8) | exponent;
             };
+            // the thread's escapes go contiguously into the warp's region of
+            // the tile's slot, after the escapes of the warp's lower lanes
             if (cnt) {
-                uint32_t* slot = a.staging + tile * a.tile_elems + (incl - cnt) * stride + warp;
+                uint32_t* slot = a.staging + tile * a.tile_elems + uint32_t(warp) * (TE * 32u) + (incl - cnt);
 #pragma unroll
                 for (int h = 0; h < (DT == SPLITZIP_BF16 ? 1 : 2); ++h) {
                     uint32_t m;
@@ -390,12 +390,9 @@ __global__ void __launch_bounds__(kBlock, kMinBlocks<DT>)
                         const uint32_t b1 = two ? 32u * h + uint32_t(__ffs(m) - 1) : b0;
                         m &= two ? m - 1u : m;
                         const uint32_t x0 = element_bits(b0), x1 = element_bits(b1);
-                        *slot = record(b0, x0);
-                        slot += stride;
-                        if (two) {
-                            *slot = record(b1, x1);
-                            slot += stride;
-                        }
+                        slot[0] = record(b0, x0);
+                        if (two) slot[1] = record(b1, x1);
+                        slot += two ? 2 : 1;
                     }
                 }
             }
@@ -532,7 +529,7 @@ __global__ void __launch_bounds__(kRecordThreads) encode_records_kernel(const En
     }
     const Layout L0 = layout_for(a.n, a.dtype, a.chunk_elems, 0);
     uint8_t* records = a.out + L0.escrec_off;
-    const uint32_t stride = staging_stride(a.tile_elems, elem_bytes(a.dtype));
+    const uint32_t region = 32u * kThreadBytes / elem_bytes(a.dtype);  // elements of a consumer warp's region
     const uint32_t rounds = (most + 31u) / 32u;
     for (uint32_t r = 0; r < rounds; ++r) {
         const uint32_t i = 32u * r + uint32_t(lane);
@@ -547,10 +544,10 @@ __global__ void __launch_bounds__(kRecordThreads) encode_records_kernel(const En
                 if (i >= first_w) w += step;
             }
             const uint32_t first_w = __shfl_sync(kFull, o, 8 * k + int(w));
-            // a plain load: the 32-byte sector of record j holds the j-th record
-            // of every warp of the tile, read by other lanes in other rounds, so it
-            // must stay in L2 (an evict-first load re-read it from DRAM each time)
-            v[k] = i < tot[k] ? a.staging[(t0 + k) * a.tile_elems + (i - first_w) * stride + w] : 0u;
+            // a plain load: neighbouring records are read by other lanes in other
+            // rounds, so the sector must stay in L2 (an evict-first load re-read
+            // it from DRAM each time)
+            v[k] = i < tot[k] ? a.staging[(t0 + k) * a.tile_elems + w * region + (i - first_w)] : 0u;
         }
 #pragma unroll
         for (int k = 0; k < kRecordTiles; ++k) {

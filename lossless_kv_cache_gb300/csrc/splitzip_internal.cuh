@@ -60,19 +60,11 @@ __host__ __device__ inline uint32_t tile_elems_for(int dtype, uint32_t chunk) {
     return chunk < full ? chunk : full;
 }
 
-// Consumer warps that hold elements of a tile: each owns 32 x 64 bytes.
-__host__ __device__ inline uint32_t staging_stride(uint32_t tile_elems, uint32_t eb) {
-    const uint32_t warp_elems = 32u * kThreadBytes / eb;
-    return tile_elems > warp_elems ? tile_elems / warp_elems : 1u;
-}
-
 // Encoder workspace: per-group escape totals (a group is kGroupTiles
-// consecutive tiles), per-(tile, consumer warp) escape counts, per-tile first
-// record indices, then one staging slot of tile_elems records per tile; a
-// record is (in-chunk position << 8) | exponent.  Record j of consumer warp w
-// sits at slot entry j * S + w, S = staging_stride (the warps that hold
-// elements of a tile), so the tile's few records share a few sectors.  Every word is written
-// before it is read, so the workspace needs no initialisation.
+// consecutive tiles), per-(tile, consumer warp) escape counts, then one
+// staging slot of tile_elems records per tile; a record is (in-chunk position
+// << 8) | exponent.  Consumer warp w stages its records contiguously from slot
+// element w * (2,048 bytes / element size) on (its region of the tile).
 constexpr uint32_t kGroupTiles = 256;
 
 struct Workspace {
