@@ -12,7 +12,7 @@
 //     escaped elements, making the output bit-exact.
 //
 // Persistent grid: each CTA loops over its chunks.  A producer warp streams
-// the chunks' nibble and sign|mantissa bytes into a 4-stage shared-memory ring
+// the chunks' nibble and sign|mantissa bytes into a shared-memory ring (one or two stages)
 // with bulk copies (TMA); eight consumer warps decode from shared memory and
 // write 16-byte streaming stores.  Every CTA validates the header first; each
 // chunk validates its index entry and each escape record, and errors go to the
@@ -86,31 +86,36 @@ __device__ __forceinline__ uint4 decode_unit_bf16(uint32_t nib, uint2 sm, const 
                       __byte_perm(lo1, hi1, 0x5140), __byte_perm(lo1, hi1, 0x7362));
 }
 
-// 12 bits of four packed s3 values -> one value per byte.
-__device__ __forceinline__ uint32_t unpack_s3x4(uint32_t g) {
-    const uint32_t y = (g & 0x3Fu) | ((g & 0xFC0u) << 10);       // groups of 2 at bytes 0 and 2
-    return (y & 0x00070007u) | ((y << 5) & 0x07000700u);         // one value per byte
+// E5M2: 16 elements from 16 codes (8 nibble bytes) and 48 bits of s3.  The
+// E5M2 table holds each exponent already at bits 2..6 of its byte.  For four
+// elements with s3 values v0..v3 (12 bits g, v_k = sign << 2 | mantissa at bits
+// 3k..3k+2), y = g[0:6] | g[6:12] << 16 puts v0, v1 at bits 0..5 and v2, v3
+// at bits 16..21; from there every sign and mantissa field moves left by 0, 5
+// or 10 bits to its place in the output bytes (sign bit 7, mantissa bits 0..1).
+// The fields never overlap, so the moves are multiply-adds.
+__device__ __forceinline__ uint32_t merge_e5m2(uint32_t g, uint32_t e) {
+    const uint32_t y = (g & 0xFC0u) * 1024u + (g & 0x3Fu);
+    const uint32_t t = (y & 0x00200020u) * 32u + (y & 0x001C001Cu);  // moved by 5 more, then all by 5
+    return t * 32u + ((y & 0x00030003u) | e);
 }
 
-// E5M2: 16 elements from 16 codes (8 nibble bytes) and 48 bits of s3.
-__device__ __forceinline__ uint4 decode_unit_e5m2(uint2 nib, uint32_t s3lo, uint32_t s3hi,
-                                                  const uint16_t* lut2) {
+__device__ __forceinline__ uint16_t lut_at(const uint16_t* lut2, uint32_t byte) {
+    return *reinterpret_cast<const uint16_t*>(reinterpret_cast<const uint8_t*>(lut2) + 2u * byte);
+}
+
+__device__ __forceinline__ uint4 decode_unit_e5m2(uint2 nib, uint32_t s3lo, uint32_t s3hi, const uint16_t* lut2) {
     const uint32_t nb[2] = {nib.x, nib.y};
     uint32_t e[4];
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
-        e[2 * i] = uint32_t(lut2[nb[i] & 0xFFu]) | (uint32_t(lut2[(nb[i] >> 8) & 0xFFu]) << 16);
-        e[2 * i + 1] = uint32_t(lut2[(nb[i] >> 16) & 0xFFu]) | (uint32_t(lut2[nb[i] >> 24]) << 16);
+        const uint32_t w = nb[i];
+        e[2 * i] = __byte_perm(lut_at(lut2, __byte_perm(w, 0u, 0x4440u)), lut_at(lut2, __byte_perm(w, 0u, 0x4441u)),
+                               0x5410u);
+        e[2 * i + 1] = __byte_perm(lut_at(lut2, __byte_perm(w, 0u, 0x4442u)), lut_at(lut2, w >> 24), 0x5410u);
     }
-    const uint32_t g[4] = {s3lo & 0xFFFu, (s3lo >> 12) & 0xFFFu, (s3lo >> 24) | ((s3hi & 0xFu) << 8),
-                           (s3hi >> 4) & 0xFFFu};
-    uint32_t o[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const uint32_t s = unpack_s3x4(g[i]);
-        o[i] = ((s << 5) & 0x80808080u) | ((e[i] << 2) & 0x7C7C7C7Cu) | (s & 0x03030303u);
-    }
-    return make_uint4(o[0], o[1], o[2], o[3]);
+    // only bits 0..11 of each g are used
+    return make_uint4(merge_e5m2(s3lo, e[0]), merge_e5m2(s3lo >> 12, e[1]),
+                      merge_e5m2(__funnelshift_r(s3lo, s3hi, 24), e[2]), merge_e5m2(s3hi >> 4, e[3]));
 }
 
 // Decode work: each CTA walks its chunks (c = blockIdx.x, +gridDim.x, ...)
@@ -119,29 +124,37 @@ __device__ __forceinline__ uint4 decode_unit_e5m2(uint2 nib, uint32_t s3lo, uint
 constexpr int kConsumerWarps = 8;
 constexpr int kConsumers = kConsumerWarps * 32;
 constexpr int kBlock = kConsumers + 32;  // + one producer warp
-constexpr int kStages = 4;
-constexpr uint32_t kSub = 8192;
-constexpr uint32_t kNibCap = kSub / 2 + 32;  // + room for a 16-byte window shift
+// Sub-tile size, ring depth and resident CTAs per SM, measured on the
+// 2.1 G-element BF16 and 4.3 G-element E5M2 caches: both run fastest with
+// 16,384-element sub-tiles at 3 CTAs per SM, BF16 (24 KB a sub-tile) with a
+// single stage, E5M2 (14 KB) with two; the other CTAs of the SM keep its
+// copies in flight while one decodes (BF16 1.21 ms vs 1.27 ms with four
+// 8,192-element stages at 2 CTAs; E5M2 1.44 ms vs 1.63 ms with four
+// 8,192-element stages, 1.44 ms at 32,768 elements and 2 CTAs).
+template <int DT> constexpr int kStages = DT == SPLITZIP_BF16 ? 1 : 2;
+template <int DT> constexpr uint32_t kSub = 16384u;
+template <int DT> constexpr uint32_t kNibCap = kSub<DT> / 2 + 32;  // + room for a 16-byte window shift
 // sign|mantissa bytes of a sub-tile: BF16 one per element, E5M2 3 per 8 elements
-template <int DT> constexpr uint32_t kSmCap = (DT == SPLITZIP_BF16 ? kSub : 3 * kSub / 8) + 32;
-template <int DT> constexpr uint32_t kStageBytes = (kNibCap + kSmCap<DT> + 127u) & ~127u;
-template <int DT> constexpr uint32_t kRingBytes = kStages * kStageBytes<DT>;
+template <int DT> constexpr uint32_t kSmCap = (DT == SPLITZIP_BF16 ? kSub<DT> : 3 * kSub<DT> / 8) + 32;
+template <int DT> constexpr uint32_t kStageBytes = (kNibCap<DT> + kSmCap<DT> + 127u) & ~127u;
+template <int DT> constexpr uint32_t kRingBytes = kStages<DT> * kStageBytes<DT>;
 // A chunk's escape records are brought into shared memory with one bulk copy
 // when they fit (at most kRecCap records: BF16 8,192 = 12.5 % of a 65,536-element
-// chunk, E5M2 6,144 = 9.4 %, within each dtype's shared-memory budget at its
+// chunk, E5M2 7,680 = 11.7 %, within each dtype's shared-memory budget at its
 // CTAs per SM);
 // a chunk with more escapes reads them from the escape stream instead.  Either
 // way each sub-tile is patched right after its stores, while its lines are
 // still in L2.
-template <int DT> constexpr uint32_t kRecCap = DT == SPLITZIP_BF16 ? 8192u : 6144u;
-// Resident CTAs per SM the kernel is compiled for (register budget): BF16
-// runs fastest at 2 with ~90 registers a thread, E5M2 at 3 (measured: BF16
-// 1.18 ms at 2 vs 1.24 ms at 4; E5M2 1.50 ms at 3 vs 1.71 ms at 2).
-template <int DT> constexpr int kDecodeMinBlocks = DT == SPLITZIP_BF16 ? 2 : 3;
+template <int DT> constexpr uint32_t kRecCap = DT == SPLITZIP_BF16 ? 8192u : 7680u;
+// resident CTAs per SM the kernel is compiled for (register budget)
+template <int DT> constexpr int kDecodeMinBlocks = 3;
 // per buffer: 3 bytes a record + room for a 16-byte window shift
 template <int DT> constexpr uint32_t kRecBytes = 3 * kRecCap<DT> + 32;
 // dynamic shared memory: the sub-tile ring, then two record buffers
 template <int DT> constexpr uint32_t kDecodeSmem = kRingBytes<DT> + 2 * kRecBytes<DT>;
+// the CTAs of one SM share its 228 KB (each also takes ~1 KB static + 1 KB reserved)
+static_assert(kDecodeMinBlocks<SPLITZIP_BF16> * (kDecodeSmem<SPLITZIP_BF16> + 2048) <= 228 * 1024, "smem");
+static_assert(kDecodeMinBlocks<SPLITZIP_FP8_E5M2> * (kDecodeSmem<SPLITZIP_FP8_E5M2> + 2048) <= 228 * 1024, "smem");
 
 struct SubTile {
     Window nib, sm;
@@ -251,8 +264,8 @@ __device__ __forceinline__ uint32_t rec_pos(const uint8_t* r) { return uint32_t(
 template <int DT>
 __global__ void __launch_bounds__(kBlock, kDecodeMinBlocks<DT>) decode_kernel(const DecodeArgs a) {
     extern __shared__ __align__(128) uint8_t stages[];
-    __shared__ __align__(8) uint64_t full_bar[kStages];
-    __shared__ __align__(8) uint64_t empty_bar[kStages];
+    __shared__ __align__(8) uint64_t full_bar[kStages<DT>];
+    __shared__ __align__(8) uint64_t empty_bar[kStages<DT>];
     __shared__ __align__(8) uint64_t rec_full[2];
     __shared__ __align__(8) uint64_t rec_empty[2];
     // record buffer b (0, 1) of the double buffer
@@ -260,14 +273,16 @@ __global__ void __launch_bounds__(kBlock, kDecodeMinBlocks<DT>) decode_kernel(co
     __shared__ uint32_t rec_offset[2];  // window shift of the records in rec_buf, or kNoRecords
     __shared__ Header hdr;
     __shared__ int header_ok;
-    __shared__ uint16_t lut2[256];  // nibble byte -> (exponent of low code) | (exponent of high code) << 8
+    // nibble byte -> (exponent of low code) | (exponent of high code) << 8,
+    // both shifted left by 2 for E5M2 (their place in the output byte)
+    __shared__ uint16_t lut2[256];
     constexpr uint32_t kNoRecords = 0xFFFFFFFFu;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     if (tid == 0) {
         header_ok = read_header(a, hdr);
         if (!header_ok) report(a.status, SPLITZIP_ERR_CORRUPT);
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < kStages<DT>; ++s) {
             mbar_init(&full_bar[s], 1);
             mbar_init(&empty_bar[s], kConsumerWarps);
         }
@@ -280,7 +295,7 @@ __global__ void __launch_bounds__(kBlock, kDecodeMinBlocks<DT>) decode_kernel(co
     __syncthreads();
     if (!header_ok) return;
     for (int b = tid; b < 256; b += kBlock)
-        lut2[b] = uint16_t(hdr.codebook[b & 15]) | uint16_t(hdr.codebook[b >> 4] << 8);
+        lut2[b] = uint16_t((hdr.codebook[b & 15] | (hdr.codebook[b >> 4] << 8)) << (DT == SPLITZIP_BF16 ? 0 : 2));
     __syncthreads();
 
     const uint8_t* in = a.in;
@@ -291,7 +306,7 @@ __global__ void __launch_bounds__(kBlock, kDecodeMinBlocks<DT>) decode_kernel(co
     const uint32_t* counts = reinterpret_cast<const uint32_t*>(in + L.counts_off);
     const uint8_t* records = in + L.escrec_off;  // 3 bytes each: position u16 LE, exponent
     const uint64_t chunk = hdr.chunk, C = hdr.n_chunks, E = hdr.E;
-    const uint32_t sub = uint32_t(min(uint64_t(kSub), chunk));
+    const uint32_t sub = uint32_t(min(uint64_t(kSub<DT>), chunk));
 
     if (warp == kConsumerWarps) {
         // ---- producer: per chunk its escape records (when they fit), then
@@ -319,16 +334,16 @@ __global__ void __launch_bounds__(kBlock, kDecodeMinBlocks<DT>) decode_kernel(co
                 mbar_arrive(&rec_full[rb]);
             }
             for (uint32_t s0 = 0; s0 < len; s0 += sub, ++it) {
-                const uint32_t stage = it % kStages, use = it / kStages;
+                const uint32_t stage = it % kStages<DT>, use = it / kStages<DT>;
                 if (use > 0 && !mbar_wait(&empty_bar[stage], (use - 1) & 1u)) report(a.status, SPLITZIP_ERR_TIMEOUT);
                 const SubTile t = subtile_windows<DT>(nibbles, signmant, base + s0, min(sub, len - s0));
                 uint8_t* dst = stages + stage * kStageBytes<DT>;
                 mbar_arrive_expect_tx(&full_bar[stage], t.nib.bytes + t.sm.bytes);
                 bulk_load(dst, t.nib.src, t.nib.bytes, &full_bar[stage]);
-                bulk_load(dst + kNibCap, t.sm.src, t.sm.bytes, &full_bar[stage]);
+                bulk_load(dst + kNibCap<DT>, t.sm.src, t.sm.bytes, &full_bar[stage]);
             }
         }
-        bool ok = drain_stages(full_bar, kStages, it);
+        bool ok = drain_stages(full_bar, kStages<DT>, it);
         ok &= drain_stages(rec_full, 2, ci);
         if (!ok) report(a.status, SPLITZIP_ERR_TIMEOUT);
         return;
@@ -372,12 +387,12 @@ __global__ void __launch_bounds__(kBlock, kDecodeMinBlocks<DT>) decode_kernel(co
             }
         };
         for (uint32_t s0 = 0; s0 < len; s0 += sub, ++it) {
-            const uint32_t stage = it % kStages, use = it / kStages;
+            const uint32_t stage = it % kStages<DT>, use = it / kStages<DT>;
             const uint32_t n_sub = min(sub, len - s0);
             if (!mbar_wait(&full_bar[stage], use & 1u)) report(a.status, SPLITZIP_ERR_TIMEOUT);
             const SubTile t = subtile_windows<DT>(nibbles, signmant, base + s0, n_sub);
             const uint8_t* src = stages + stage * kStageBytes<DT>;
-            decode_subtile<DT>(src + t.nib.offset, src + kNibCap + t.sm.offset, a.out, base + s0, n_sub, tid, lut2);
+            decode_subtile<DT>(src + t.nib.offset, src + kNibCap<DT> + t.sm.offset, a.out, base + s0, n_sub, tid, lut2);
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty_bar[stage]);
             if (!patch) continue;
