@@ -530,33 +530,42 @@ __global__ void __launch_bounds__(kRecordThreads) encode_records_kernel(const En
     const Layout L0 = layout_for(a.n, a.dtype, a.chunk_elems, 0);
     uint8_t* records = a.out + L0.escrec_off;
     const uint32_t region = 32u * kThreadBytes / elem_bytes(a.dtype);  // elements of a consumer warp's region
-    const uint32_t rounds = (most + 31u) / 32u;
-    for (uint32_t r = 0; r < rounds; ++r) {
-        const uint32_t i = 32u * r + uint32_t(lane);
-        uint32_t v[kRecordTiles];
+    // the staged record i of tile k (0 past the tile's count)
+    auto staged = [&](int k, uint32_t i) -> uint32_t {
+        // warp of record i: the last warp whose first record is <= i
+        uint32_t w = 0;
+#pragma unroll
+        for (uint32_t step = 4; step > 0; step >>= 1) {
+            const uint32_t first_w = __shfl_sync(kFull, o, 8 * k + int(w + step));
+            if (i >= first_w) w += step;
+        }
+        const uint32_t first_w = __shfl_sync(kFull, o, 8 * k + int(w));
+        // a plain load: neighbouring records are read by other lanes in other
+        // rounds, so the sector must stay in L2 (an evict-first load re-read
+        // it from DRAM each time)
+        return i < tot[k] ? a.staging[(t0 + k) * a.tile_elems + w * region + (i - first_w)] : 0u;
+    };
+    auto put = [&](int k, uint32_t i, uint32_t v) {
+        if (i < tot[k]) {
+            uint8_t* d = records + 3 * (f[k] + i);
+            d[0] = uint8_t(v >> 8);
+            d[1] = uint8_t(v >> 16);
+            d[2] = uint8_t(v);
+        }
+    };
+    // two rounds at a time: eight independent loads in flight per lane
+    for (uint32_t r0 = 0; r0 < most; r0 += 64u) {
+        const uint32_t i0 = r0 + uint32_t(lane), i1 = i0 + 32u;
+        uint32_t v[2 * kRecordTiles];
 #pragma unroll
         for (int k = 0; k < kRecordTiles; ++k) {
-            // warp of record i: the last warp whose first record is <= i
-            uint32_t w = 0;
-#pragma unroll
-            for (uint32_t step = 4; step > 0; step >>= 1) {
-                const uint32_t first_w = __shfl_sync(kFull, o, 8 * k + int(w + step));
-                if (i >= first_w) w += step;
-            }
-            const uint32_t first_w = __shfl_sync(kFull, o, 8 * k + int(w));
-            // a plain load: neighbouring records are read by other lanes in other
-            // rounds, so the sector must stay in L2 (an evict-first load re-read
-            // it from DRAM each time)
-            v[k] = i < tot[k] ? a.staging[(t0 + k) * a.tile_elems + w * region + (i - first_w)] : 0u;
+            v[k] = staged(k, i0);
+            v[kRecordTiles + k] = staged(k, i1);
         }
 #pragma unroll
         for (int k = 0; k < kRecordTiles; ++k) {
-            if (i < tot[k]) {
-                uint8_t* d = records + 3 * (f[k] + i);
-                d[0] = uint8_t(v[k] >> 8);
-                d[1] = uint8_t(v[k] >> 16);
-                d[2] = uint8_t(v[k]);
-            }
+            put(k, i0, v[k]);
+            put(k, i1, v[kRecordTiles + k]);
         }
     }
 }
