@@ -52,8 +52,11 @@ def parse_args():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--layers", type=int, default=32,
-                   help="32-layer workloads: encode only the first L layers (a smaller case for profiling; "
+                   help="32-layer workloads: encode only L layers (a smaller case for profiling; "
                         "not a bench line)")
+    p.add_argument("--first-layer", type=int, default=0,
+                   help="with --layers: the first of the L layers (layers 1-2 have the cache's average escape "
+                        "rate; layer 0 has the highest)")
     return p.parse_args()
 
 
@@ -90,24 +93,24 @@ def reduce_over_ranks(x, world, device, op):
 # A figure is reported only while the sources still hash to that value.
 TRAFFIC = {
     ("kv_cache_32x2x32768x8x128_bf16", "encode"): {
-        "bytes": 4337156192 + 3237539200 + 8392288 + 384 + 8405440 + 0 + 79524448 + 1891520,
+        "bytes": 4350655680 + 3342974816 + 8392000 + 384 + 8405760 + 0 + 313547840 + 64511904,
         "sources": ('encode.cu', 'tma_pipeline.cuh', 'splitzip_internal.cuh'),
-        "sha256": "f5a05b2d04bd85b74bbc730b9186b983c1454c366afb503e63f7f05092152fbc",
+        "sha256": "51410ff8433da92c8c914a6ae2b74222db3ec809ddf3ef8caca980b521eb0c44",
         "profile": "profiles/launches_kv_cache_32x2x32768x8x128_bf16.md"},
     ("kv_cache_32x2x32768x8x128_bf16", "decode"): {
-        "bytes": 3267908640 + 4248122336,
+        "bytes": 3346287680 + 4295327520,
         "sources": ('decode.cu', 'tma_pipeline.cuh', 'splitzip_internal.cuh'),
-        "sha256": "e34d3bed5aeff4d046b8a734ccdcd3fa46084be2fc8c05264a3ffdceb575cc0e",
+        "sha256": "888e96c2a7bc783449efa94952df3d46c806bfc79e79a1ea19b8382d263293b2",
         "profile": "profiles/launches_kv_cache_32x2x32768x8x128_bf16.md"},
     ("kv_cache_32x2x65536x8x128_e5m2", "encode"): {
-        "bytes": 4364481088 + 3813962784 + 8392096 + 1248 + 8406496 + 0 + 118219936 + 5934208,
+        "bytes": 4373062016 + 4038603904 + 8392032 + 0 + 8405312 + 0 + 470518944 + 177696768,
         "sources": ('encode.cu', 'tma_pipeline.cuh', 'splitzip_internal.cuh'),
-        "sha256": "f5a05b2d04bd85b74bbc730b9186b983c1454c366afb503e63f7f05092152fbc",
+        "sha256": "51410ff8433da92c8c914a6ae2b74222db3ec809ddf3ef8caca980b521eb0c44",
         "profile": "profiles/launches_kv_cache_32x2x65536x8x128_e5m2.md"},
     ("kv_cache_32x2x65536x8x128_e5m2", "decode"): {
-        "bytes": 3818561952 + 4247927424,
+        "bytes": 3994678112 + 4304559584,
         "sources": ('decode.cu', 'tma_pipeline.cuh', 'splitzip_internal.cuh'),
-        "sha256": "e34d3bed5aeff4d046b8a734ccdcd3fa46084be2fc8c05264a3ffdceb575cc0e",
+        "sha256": "888e96c2a7bc783449efa94952df3d46c806bfc79e79a1ea19b8382d263293b2",
         "profile": "profiles/launches_kv_cache_32x2x65536x8x128_e5m2.md"},
 }
 
@@ -203,7 +206,7 @@ class ClockSampler:
 class Workload:
     """One of the five workloads: raw-bit tensors and their sizes."""
 
-    def __init__(self, name, layers=32):
+    def __init__(self, name, layers=32, first_layer=0):
         from lossless_kv_cache_gb300 import workloads as W
         self.W = W
         self.name = name
@@ -211,12 +214,15 @@ class Workload:
         self.elem_bytes = W.bytes_per_element(self.dtype)
         self.layered = name in ("kv_cache_32x2x32768x8x128_bf16", "kv_cache_32x2x65536x8x128_e5m2")
         self.layers = layers if self.layered else None
+        self.first_layer = first_layer if self.layered else 0
+        if self.layered and not (0 <= first_layer and layers >= 1 and first_layer + layers <= 32):
+            raise SystemExit("--first-layer + --layers must stay within the 32 layers")
         full = W.numel(name)
         self.n = full // 32 * layers if self.layered else full
 
     def make(self, seed, device):
         if self.layered:
-            return self.W.make_layers(self.name, seed, self.layers, device)
+            return self.W.make_layers(self.name, seed, self.layers, device, first=self.first_layer)
         return self.W.make(self.name, seed, device)
 
     def calibration(self, device):
@@ -225,7 +231,8 @@ class Workload:
     def config(self, world):
         label = self.name
         if self.layered and self.layers != 32:
-            label = "%s (first %d layers only: profiling case)" % (self.name, self.layers)
+            label = "%s (layers %d-%d only: profiling case)" % (self.name, self.first_layer,
+                                                                self.first_layer + self.layers - 1)
         return {"workload": label, "elements": self.n,
                 "element_dtype": "bf16" if self.dtype == 0 else "fp8_e5m2", "chunk_elems": CHUNK,
                 "codebook": "Top-16 from the seed-1 calibration tensor"
@@ -276,7 +283,7 @@ def run_reference(args, world, rank):
     if rank != 0:
         return None
     import oracle
-    wl = Workload(args.workload, args.layers)
+    wl = Workload(args.workload, args.layers, args.first_layer)
     if wl.layered:
         _, layer = wl.W.layers_of(wl.name)
         x = layer(0, 0, "cpu").numpy()  # layer 0 of seed 0
@@ -321,7 +328,7 @@ def run_ours(args, world, rank, local):
     device = torch.device("cuda", local)
     torch.cuda.set_device(device)
     sz.lib()  # fails loudly when the CUDA library is missing
-    wl = Workload(args.workload, args.layers)
+    wl = Workload(args.workload, args.layers, args.first_layer)
     n, dtype = wl.n, wl.dtype
     raw_bytes = wl.elem_bytes * n
 

@@ -160,16 +160,17 @@ def make(name, seed, device="cpu"):
     return make_layers(name, seed, n_layers, device)
 
 
-def make_layers(name, seed, n_layers, device="cpu"):
-    """The first n_layers layers of a 32-layer cache, filled one layer at a time."""
+def make_layers(name, seed, n_layers, device="cpu", first=0):
+    """Layers first .. first + n_layers - 1 of a 32-layer cache, filled one
+    layer at a time."""
     _, layer = layers_of(name)
-    first = layer(seed, 0, device)
-    out = torch.empty(n_layers * first.numel(), dtype=first.dtype, device=device)
-    out[: first.numel()].copy_(first)
-    del first
+    head = layer(seed, first, device)
+    out = torch.empty(n_layers * head.numel(), dtype=head.dtype, device=device)
+    out[: head.numel()].copy_(head)
+    del head
     per = out.numel() // n_layers
     for l in range(1, n_layers):
-        out[l * per: (l + 1) * per].copy_(layer(seed, l, device))
+        out[l * per: (l + 1) * per].copy_(layer(seed, first + l, device))
     return out
 
 
