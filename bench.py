@@ -51,6 +51,7 @@ def parse_args():
     p.add_argument("--cpu-seconds", type=float, default=10.0, help="oracle time budget for cpu_baseline")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-transfer", action="store_true", help="skip the GPU -> host -> GPU transfer leg")
     p.add_argument("--layers", type=int, default=32,
                    help="32-layer workloads: encode only L layers (a smaller case for profiling; "
                         "not a bench line)")
@@ -514,6 +515,34 @@ def run_ours(args, world, rank, local):
                "pieces": pieces, "streams": "H2D / codec / D2H"}
         del x_host, y_host, xin, boxes, pws
 
+    # ---- transfer: GPU -> pinned host -> GPU through splitzip_transfer, the
+    # codec on both ends of the link (compressed) against the raw bytes ----
+    transfer = None
+    if not args.no_transfer:
+        if wl.layered:
+            tpieces = wl.layers
+        else:
+            tpieces = int(max(1, min(32, raw_bytes // (64 << 20))))
+        tpiece = -(-(-(-n // tpieces)) // CHUNK) * CHUNK
+        y = torch.empty_like(x)
+        res = {}
+        for compress in (True, False):
+            tb = sz.TransferBuffers(n, dtype, tpiece, compress, CHUNK, device=device)
+            sz.transfer(x, y, cb, tb)  # warm-up
+            runs = [sz.transfer(x, y, cb, tb) for _ in range(3)]
+            torch.cuda.synchronize()
+            res[compress] = (statistics.median(r[0] for r in runs), runs[0][1], bool(torch.equal(y, x)))
+            del tb
+        z_ms, z_link, z_ok = res[True]
+        r_ms, r_link, r_ok = res[False]
+        transfer = {"pieces": -(-n // tpiece), "piece_elems": tpiece, "splitzip_ms": round(z_ms, 3),
+                    "raw_ms": round(r_ms, 3), "speedup": round(r_ms / z_ms, 4),
+                    "link_bytes_each_way": {"splitzip": z_link, "raw": r_link},
+                    "raw_link_GBps_each_way": round(r_link / (r_ms * 1e-3) / 1e9, 1), "verified": z_ok and r_ok,
+                    "path": "device -> pinned host -> device copies (cudaMemcpyAsync), encode / D2H / H2D / decode "
+                            "on four streams, median of 3"}
+        del y
+
     # ---- CPU oracle on a bounded sample (rank 0 only) ----
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -537,7 +566,8 @@ def run_ours(args, world, rank, local):
         "escape_rate": round(E / n, 6), "verified_bit_exact": verified,
         "per_kernel": per_kernel, "link_model": link,
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clk,
-        "gpu_launches": 5 * K,  # encode: streaming, group, index, records kernels; decode: one kernel
+        "transfer": transfer,
+        "gpu_launches": 5 * K,  # timed steps: encode (streaming, group, index, records kernels) + decode
     }
 
 

@@ -178,9 +178,9 @@ int splitzip_encode(const void* d_in, uint64_t n, int dtype, const splitzip_code
  * the array's device address (cudaGetSymbolAddress) with that device current;
  * make that first call before any stream capture.  Every call on a device
  * shares the array, so calls whose GPU work overlaps (other streams or host
- * threads) race and must be serialised by the caller.  Each call clears the
- * part of the array that must start at zero, on its own stream, before its
- * kernel runs. */
+ * threads) race and must be serialised by the caller.  The encode writes
+ * every word of its workspace before reading it, so whatever an earlier call
+ * left in the array does no harm. */
 int splitzip_encode_noalloc(const void* d_in, uint64_t n, int dtype, const splitzip_codebook_t* cb,
                             uint32_t chunk_elems, void* d_out, uint64_t out_capacity,
                             uint64_t* d_out_size, int* d_status, cudaStream_t stream);
@@ -199,6 +199,38 @@ int splitzip_decode(const void* d_in, uint64_t in_bytes, void* d_out, uint64_t n
  * Returns SPLITZIP_ERR_CORRUPT for a malformed header or a size larger than
  * `bytes`. */
 int splitzip_parse_header(const void* h_blob, uint64_t bytes, splitzip_header_t* out);
+
+/* Scratch that splitzip_transfer needs: device bytes (with compress = 1: a
+ * ring of 4 send and 4 receive containers of one piece's maximum size, one
+ * encode workspace and 16 bytes per piece; 0 with compress = 0) and pinned
+ * host bytes (a ring of 4 staging slots, plus 16 bytes per piece when
+ * compressing).  SPLITZIP_ERR_INVALID_ARG unless n > 0 and piece_elems is a
+ * positive multiple of chunk_elems. */
+int splitzip_transfer_scratch_size(uint64_t n, int dtype, uint32_t chunk_elems, uint64_t piece_elems,
+                                   int compress, uint64_t* out_device_bytes, uint64_t* out_host_bytes);
+
+/* Move n elements from d_src to d_dst (both on the current GPU) across the
+ * GPU <-> host link, the transfer that the page speeds up (section
+ * "Results": prefill-to-decode KV transfer in disaggregated serving).  The
+ * tensor is cut into pieces of piece_elems elements (whole chunks; the last
+ * piece may be shorter).  compress = 1: each piece is encoded into its own
+ * container, exactly the container's bytes are copied device -> h_stage and
+ * back, and the received container is decoded into d_dst; compress = 0: the
+ * raw piece is copied the same way (the baseline).  Encode, the two copies
+ * and decode of different pieces overlap on four internal streams; the host
+ * reads each container's size (8 bytes copied behind its encode) while the
+ * next piece encodes.  The call starts after the work already on `stream`,
+ * makes `stream` wait for its end, and blocks until d_dst is complete.
+ * d_scratch / h_stage: at least splitzip_transfer_scratch_size's bytes,
+ * 16-byte aligned, h_stage page-locked host memory (cudaHostAlloc or
+ * cudaHostRegister; SPLITZIP_ERR_INVALID_ARG otherwise).  out_link_bytes
+ * (optional): the bytes that crossed the link in each direction;
+ * out_ms (optional): GPU time from the first to the last operation.  An
+ * encode or decode error of any piece is returned (the first one found). */
+int splitzip_transfer(const void* d_src, void* d_dst, uint64_t n, int dtype, const splitzip_codebook_t* cb,
+                      uint32_t chunk_elems, uint64_t piece_elems, int compress, void* d_scratch,
+                      uint64_t d_scratch_bytes, void* h_stage, uint64_t h_stage_bytes, uint64_t* out_link_bytes,
+                      float* out_ms, cudaStream_t stream);
 
 #ifdef __cplusplus
 }

@@ -104,6 +104,9 @@ SIGNATURES = {
                                        _vp]),
     "splitzip_decode": (_int, [_vp, _u64, _vp, _u64, _int, _vp, _vp]),
     "splitzip_parse_header": (_int, [_vp, _u64, ctypes.POINTER(Header)]),
+    "splitzip_transfer_scratch_size": (_int, [_u64, _int, _u32, _u64, _int, _P_u64, _P_u64]),
+    "splitzip_transfer": (_int, [_vp, _vp, _u64, _int, ctypes.POINTER(Codebook), _u32, _u64, _int, _vp, _u64, _vp,
+                                 _u64, _P_u64, ctypes.POINTER(ctypes.c_float), _vp]),
 }
 
 _lib = None
@@ -168,6 +171,20 @@ def splitzip_decode(d_in, in_bytes, d_out, n, dtype, d_status, stream):
 
 def splitzip_parse_header(h_blob, nbytes, out):
     return lib().splitzip_parse_header(h_blob, nbytes, ctypes.byref(out))
+
+
+def splitzip_transfer_scratch_size(n, dtype, chunk_elems, piece_elems, compress, out_device_bytes, out_host_bytes):
+    return lib().splitzip_transfer_scratch_size(n, dtype, chunk_elems, piece_elems, compress,
+                                                ctypes.byref(out_device_bytes), ctypes.byref(out_host_bytes))
+
+
+def splitzip_transfer(d_src, d_dst, n, dtype, cb, chunk_elems, piece_elems, compress, d_scratch, d_scratch_bytes,
+                      h_stage, h_stage_bytes, out_link_bytes, out_ms, stream):
+    """out_link_bytes: ctypes.c_uint64 or None; out_ms: ctypes.c_float or None."""
+    return lib().splitzip_transfer(d_src, d_dst, n, dtype, None if cb is None else ctypes.byref(cb), chunk_elems,
+                                   piece_elems, compress, d_scratch, d_scratch_bytes, h_stage, h_stage_bytes,
+                                   None if out_link_bytes is None else ctypes.byref(out_link_bytes),
+                                   None if out_ms is None else ctypes.byref(out_ms), stream)
 
 
 # ------------------------------------------------------------ size helpers
@@ -285,3 +302,34 @@ def decode(blob, n, dtype, stream=None):
     decode_into(blob, blob.numel(), out, n, dtype, status, stream)
     _check(int(status[0].item()), "splitzip_decode (device)")
     return out[:n]
+
+
+def transfer_scratch_size(n, dtype, piece_elems, compress=True, chunk_elems=DEFAULT_CHUNK_ELEMS):
+    """(device bytes, pinned host bytes) that splitzip_transfer needs."""
+    d, h = ctypes.c_uint64(0), ctypes.c_uint64(0)
+    _check(splitzip_transfer_scratch_size(n, dtype, chunk_elems, piece_elems, int(compress), d, h),
+           "splitzip_transfer_scratch_size")
+    return d.value, h.value
+
+
+class TransferBuffers:
+    """Device scratch and pinned host staging for splitzip_transfer."""
+
+    def __init__(self, n, dtype, piece_elems, compress=True, chunk_elems=DEFAULT_CHUNK_ELEMS, device="cuda"):
+        torch = _torch()
+        self.n, self.dtype, self.piece_elems = n, dtype, piece_elems
+        self.compress, self.chunk_elems = bool(compress), chunk_elems
+        d, h = transfer_scratch_size(n, dtype, piece_elems, compress, chunk_elems)
+        self.device = torch.empty(max(d, 16), dtype=torch.uint8, device=device)
+        self.host = torch.empty(max(h, 16), dtype=torch.uint8, pin_memory=True)
+
+
+def transfer(src, dst, cb, bufs, stream=None):
+    """Move device tensor src into dst across the GPU <-> host link (see
+    splitzip_transfer); returns (GPU milliseconds, bytes over the link each way)."""
+    link, ms = ctypes.c_uint64(0), ctypes.c_float(0.0)
+    _check(splitzip_transfer(src.data_ptr(), dst.data_ptr(), bufs.n, bufs.dtype, cb if bufs.compress else None,
+                             bufs.chunk_elems, bufs.piece_elems, int(bufs.compress), bufs.device.data_ptr(),
+                             bufs.device.numel(), bufs.host.data_ptr(), bufs.host.numel(), link, ms,
+                             _stream_handle(stream)), "splitzip_transfer")
+    return ms.value, link.value

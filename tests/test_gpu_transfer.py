@@ -1,0 +1,77 @@
+"""GPU: the transfer path (encode -> D2H -> H2D -> decode per piece, four
+streams) against the oracle.  The destination must equal the source bit for
+bit, the bytes that crossed the link must be the oracle's container sizes of
+the pieces, and the last container left in the host staging area must be the
+oracle's container of the last piece, byte for byte."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import lossless_kv_cache_gb300 as sz
+from lossless_kv_cache_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib(splitzip_lib):
+    assert torch.cuda.is_available()
+    return splitzip_lib
+
+
+def a16(x):
+    return (x + 15) // 16 * 16
+
+
+def bits(dtype, n, seed):
+    if dtype == sz.BF16:
+        x = W.escape_stress(seed, chunks=-(-n // 65536), chunk_elems=65536)[:n]
+        return x.numpy().view(np.uint16), x.cuda()
+    x = W.kv_cache_layer_e5m2(seed, 3, tokens=-(-n // 1024))[:n]
+    return x.numpy(), x.cuda()
+
+
+@pytest.mark.parametrize("dtype", [sz.BF16, sz.FP8_E5M2])
+@pytest.mark.parametrize("chunk,piece", [(65536, 65536), (4096, 3 * 4096)])
+def test_transfer_matches_oracle(dtype, chunk, piece):
+    n = 9 * 65536 + 12345  # ten or more pieces: the ring of four slots is reused; a ragged last piece
+    host, x = bits(dtype, n, 7)
+    exps = oracle.calibrate(oracle.histogram(host, dtype), dtype)
+    cb = sz.Codebook.make(dtype, [int(e) for e in exps])
+    for compress in (True, False):
+        y = torch.full_like(x, 0x55 if dtype == sz.FP8_E5M2 else 0x5555)
+        bufs = sz.TransferBuffers(n, dtype, piece, compress, chunk)
+        ms, link = sz.transfer(x, y, cb, bufs)
+        torch.cuda.synchronize()
+        assert torch.equal(y, x)
+        assert ms > 0
+        eb = 2 if dtype == sz.BF16 else 1
+        pieces = [(i, min(piece, n - i)) for i in range(0, n, piece)]
+        if not compress:
+            assert link == n * eb
+            continue
+        sizes = []
+        for lo, m in pieces:
+            E = int(oracle.chunk_escape_counts(host[lo:lo + m], dtype, exps, chunk).sum())
+            sizes.append(oracle.container_size(m, dtype, chunk, E))
+        assert link == sum(sizes)
+        # the last piece's container is still in its staging slot
+        lo, m = pieces[-1]
+        ref = oracle.encode(host[lo:lo + m], dtype, exps, chunk)
+        slot = (len(pieces) - 1) % 4
+        cap = a16(sz.max_compressed_size(piece, dtype, chunk))
+        got = bufs.host[slot * cap: slot * cap + ref.size].numpy()
+        assert np.array_equal(got, ref)
+
+
+def test_transfer_rejects_pageable_host_memory():
+    n, piece = 65536, 65536
+    x = torch.zeros(n, dtype=torch.int16, device="cuda")
+    d, h = sz.transfer_scratch_size(n, sz.BF16, piece, True)
+    dev = torch.empty(d, dtype=torch.uint8, device="cuda")
+    pageable = torch.empty(h + 16, dtype=torch.uint8)  # not page-locked
+    cb = sz.Codebook.make(sz.BF16, range(16))
+    st = sz.splitzip_transfer(x.data_ptr(), x.data_ptr(), n, sz.BF16, cb, 65536, piece, 1, dev.data_ptr(), d,
+                              pageable.data_ptr() + (-pageable.data_ptr()) % 16, h, None, None, 0)
+    assert st == sz.ERR_INVALID_ARG
