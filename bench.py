@@ -52,6 +52,7 @@ def parse_args():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-transfer", action="store_true", help="skip the GPU -> host -> GPU transfer leg")
+    p.add_argument("--no-online", action="store_true", help="skip the online-calibration leg")
     p.add_argument("--layers", type=int, default=32,
                    help="32-layer workloads: encode only L layers (a smaller case for profiling; "
                         "not a bench line)")
@@ -543,6 +544,48 @@ def run_ours(args, world, rank, local):
                             "on four streams, median of 3"}
         del y
 
+    # ---- online calibration: histogram + Top-16 on the device, then the
+    # encode that reads that codebook, against the offline codebook's encode ----
+    online = None
+    if not args.no_online:
+        hist_d = torch.empty(256, dtype=torch.int64, device=device)
+        cb_d = torch.empty(32, dtype=torch.uint8, device=device)
+
+        def online_step(ev=None):
+            if ev is not None:
+                ev[0].record(stream)
+            check(sz.splitzip_calibrate_device(xp, n, dtype, hist_d.data_ptr(), cb_d.data_ptr(), h), "calibrate")
+            if ev is not None:
+                ev[1].record(stream)
+            check(sz.splitzip_encode_device_codebook(xp, n, dtype, cb_d.data_ptr(), CHUNK, op, cap, wp, ws,
+                                                     bufs.size.data_ptr(), bufs.status.data_ptr(), h), "encode")
+            if ev is not None:
+                ev[2].record(stream)
+
+        for _ in range(2):
+            online_step()
+        torch.cuda.synchronize()
+        oevs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(10)]
+        for ev in oevs:
+            if flush is not None:
+                flush.fill_(1)
+            online_step(ev)
+        torch.cuda.synchronize()
+        cal_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in oevs)
+        oenc_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in oevs)
+        on_ok = int(bufs.status[0]) == sz.OK
+        on_size = int(bufs.size[0])
+        on_E = int(bufs.out[24:32].cpu().numpy().view(np.uint64)[0])
+        check(sz.splitzip_decode(op, cap, out.data_ptr(), n, dtype, dstatus.data_ptr(), h), "decode")
+        torch.cuda.synchronize()
+        on_ok = on_ok and int(dstatus[0]) == sz.OK and bool(torch.equal(out, x))
+        online = {"calibrate_ms": round(cal_ms, 4), "encode_ms": round(oenc_ms, 4),
+                  "total_ms": round(cal_ms + oenc_ms, 4), "offline_encode_ms": round(enc_ms, 4),
+                  "slowdown_vs_offline": round((cal_ms + oenc_ms) / enc_ms, 4),
+                  "escape_rate": round(on_E / n, 6), "ratio": round(raw_bytes / on_size, 5),
+                  "codebook": [int(v) for v in cb_d[1:17].cpu().tolist()], "verified": on_ok,
+                  "what": "per-tensor codebook calibrated on the device from the encoded tensor itself"}
+
     # ---- CPU oracle on a bounded sample (rank 0 only) ----
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -566,7 +609,7 @@ def run_ours(args, world, rank, local):
         "escape_rate": round(E / n, 6), "verified_bit_exact": verified,
         "per_kernel": per_kernel, "link_model": link,
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clk,
-        "transfer": transfer,
+        "transfer": transfer, "online_calibration": online,
         "gpu_launches": 5 * K,  # timed steps: encode (streaming, group, index, records kernels) + decode
     }
 

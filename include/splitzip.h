@@ -159,6 +159,28 @@ int splitzip_encode(const void* d_in, uint64_t n, int dtype, const splitzip_code
                     uint32_t chunk_elems, void* d_out, uint64_t out_capacity, void* d_ws,
                     uint64_t ws_bytes, uint64_t* d_out_size, int* d_status, cudaStream_t stream);
 
+/* Online calibration, all on the device and stream-ordered (no host
+ * synchronisation): the exponent histogram of d_x into d_hist256 (as
+ * splitzip_exponent_histogram), then its Top-16 codebook (Method, "Top-16
+ * exponent coding"; count descending, exponent ascending on ties, as
+ * splitzip_calibrate) into the device struct *d_cb.  The page calibrates
+ * offline to avoid exactly this pass (section "Method: SplitZip", and Results,
+ * "Ablations: Calibration"); this entry point measures what it costs.
+ * d_hist256: device, 256 u64, 16-byte aligned; d_cb: device splitzip_codebook_t. */
+int splitzip_calibrate_device(const void* d_x, uint64_t n, int dtype, uint64_t* d_hist256,
+                              splitzip_codebook_t* d_cb, cudaStream_t stream);
+
+/* splitzip_encode with the codebook in device memory (d_cb, e.g. written by
+ * splitzip_calibrate_device), so that calibrate and encode can follow each
+ * other on a stream without the host.  The GPU checks the codebook (its
+ * dtype field, exponents in range and distinct) and writes
+ * SPLITZIP_ERR_INVALID_ARG to *d_status for a bad one (output unspecified).
+ * Everything else as splitzip_encode; the output is byte-identical to
+ * splitzip_encode's with the same codebook on the host. */
+int splitzip_encode_device_codebook(const void* d_in, uint64_t n, int dtype, const splitzip_codebook_t* d_cb,
+                                    uint32_t chunk_elems, void* d_out, uint64_t out_capacity, void* d_ws,
+                                    uint64_t ws_bytes, uint64_t* d_out_size, int* d_status, cudaStream_t stream);
+
 /* Size of the device array that splitzip_encode_noalloc uses as scratch. */
 #define SPLITZIP_NOALLOC_SCRATCH_BYTES (32ull << 20)
 

@@ -104,6 +104,8 @@ SIGNATURES = {
                                        _vp]),
     "splitzip_decode": (_int, [_vp, _u64, _vp, _u64, _int, _vp, _vp]),
     "splitzip_parse_header": (_int, [_vp, _u64, ctypes.POINTER(Header)]),
+    "splitzip_calibrate_device": (_int, [_vp, _u64, _int, _vp, _vp, _vp]),
+    "splitzip_encode_device_codebook": (_int, [_vp, _u64, _int, _vp, _u32, _vp, _u64, _vp, _u64, _vp, _vp, _vp]),
     "splitzip_transfer_scratch_size": (_int, [_u64, _int, _u32, _u64, _int, _P_u64, _P_u64]),
     "splitzip_transfer": (_int, [_vp, _vp, _u64, _int, ctypes.POINTER(Codebook), _u32, _u64, _int, _vp, _u64, _vp,
                                  _u64, _P_u64, ctypes.POINTER(ctypes.c_float), _vp]),
@@ -171,6 +173,16 @@ def splitzip_decode(d_in, in_bytes, d_out, n, dtype, d_status, stream):
 
 def splitzip_parse_header(h_blob, nbytes, out):
     return lib().splitzip_parse_header(h_blob, nbytes, ctypes.byref(out))
+
+
+def splitzip_calibrate_device(d_x, n, dtype, d_hist256, d_cb, stream):
+    return lib().splitzip_calibrate_device(d_x, n, dtype, d_hist256, d_cb, stream)
+
+
+def splitzip_encode_device_codebook(d_in, n, dtype, d_cb, chunk_elems, d_out, out_capacity, d_ws, ws_bytes,
+                                    d_out_size, d_status, stream):
+    return lib().splitzip_encode_device_codebook(d_in, n, dtype, d_cb, chunk_elems, d_out, out_capacity, d_ws,
+                                                 ws_bytes, d_out_size, d_status, stream)
 
 
 def splitzip_transfer_scratch_size(n, dtype, chunk_elems, piece_elems, compress, out_device_bytes, out_host_bytes):
@@ -333,3 +345,23 @@ def transfer(src, dst, cb, bufs, stream=None):
                              bufs.device.numel(), bufs.host.data_ptr(), bufs.host.numel(), link, ms,
                              _stream_handle(stream)), "splitzip_transfer")
     return ms.value, link.value
+
+
+def calibrate_device(x, dtype, hist=None, cb=None, stream=None):
+    """Online calibration on the device (no host synchronisation): returns
+    (histogram, codebook) as device tensors (256 int64; 17 uint8 laid out as
+    splitzip_codebook_t: dtype, then the 16 exponents)."""
+    torch = _torch()
+    hist = torch.empty(256, dtype=torch.int64, device=x.device) if hist is None else hist
+    cb = torch.empty(32, dtype=torch.uint8, device=x.device) if cb is None else cb
+    _check(splitzip_calibrate_device(x.data_ptr(), x.numel(), dtype, hist.data_ptr(), cb.data_ptr(),
+                                     _stream_handle(stream)), "splitzip_calibrate_device")
+    return hist, cb
+
+
+def encode_into_device_codebook(x, d_cb, bufs, stream=None):
+    """encode_into with the codebook in device memory (see calibrate_device)."""
+    _check(splitzip_encode_device_codebook(x.data_ptr(), x.numel(), bufs.dtype, d_cb.data_ptr(), bufs.chunk_elems,
+                                           bufs.out.data_ptr(), bufs.capacity, bufs.ws.data_ptr(), bufs.ws_bytes,
+                                           bufs.size.data_ptr(), bufs.status.data_ptr(), _stream_handle(stream)),
+           "splitzip_encode_device_codebook")

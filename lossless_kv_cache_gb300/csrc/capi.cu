@@ -89,12 +89,14 @@ int grid_for(uint64_t work_items, int sms, int blocks_per_sm) {
 }
 
 // Argument checks of splitzip_encode; fills the kernel arguments.
+// cb is a host codebook (checked here) or, with device_cb, the device address
+// of one (checked by the kernel).
 int prepare_encode(const void* d_in, uint64_t n, int dtype, const splitzip_codebook_t* cb, uint32_t chunk,
                    void* d_out, uint64_t out_capacity, void* d_ws, uint64_t ws_bytes, uint64_t* d_out_size,
-                   int* d_status, EncodeArgs* a, Workspace* W) {
+                   int* d_status, EncodeArgs* a, Workspace* W, bool device_cb = false) {
     int st = check_geometry(n, dtype, chunk);
     if (st != SPLITZIP_OK) return st;
-    if ((st = check_codebook(cb, dtype)) != SPLITZIP_OK) return st;
+    if (device_cb ? !cb : (st = check_codebook(cb, dtype)) != SPLITZIP_OK) return device_cb ? SPLITZIP_ERR_INVALID_ARG : st;
     if (n > 0 && (!d_in || !aligned(d_in, 16))) return SPLITZIP_ERR_INVALID_ARG;
     if (!d_out || !aligned(d_out, 16)) return SPLITZIP_ERR_INVALID_ARG;
     if (!d_out_size || !aligned(d_out_size, 8) || !d_status || !aligned(d_status, 4))
@@ -120,7 +122,13 @@ int prepare_encode(const void* d_in, uint64_t n, int dtype, const splitzip_codeb
     a->chunk_elems = chunk;
     a->n_chunks = layout_for(n, dtype, chunk, 0).n_chunks;
     a->dtype = dtype;
-    std::memcpy(a->codebook, cb->exps, 16);
+    if (device_cb) {
+        std::memset(a->codebook, 0, 16);
+        a->dev_codebook = reinterpret_cast<const uint8_t*>(cb);
+    } else {
+        std::memcpy(a->codebook, cb->exps, 16);
+        a->dev_codebook = nullptr;
+    }
     a->tensor_bytes = 0;
     a->box_bytes = 0;
     return SPLITZIP_OK;
@@ -258,13 +266,15 @@ int splitzip_exponent_histogram(const void* d_x, uint64_t n, int dtype, uint64_t
                : SPLITZIP_ERR_CUDA;
 }
 
-int splitzip_encode(const void* d_in, uint64_t n, int dtype, const splitzip_codebook_t* cb, uint32_t chunk_elems,
-                    void* d_out, uint64_t out_capacity, void* d_ws, uint64_t ws_bytes, uint64_t* d_out_size,
-                    int* d_status, cudaStream_t stream) {
+namespace {
+
+int encode_call(const void* d_in, uint64_t n, int dtype, const splitzip_codebook_t* cb, uint32_t chunk_elems,
+                void* d_out, uint64_t out_capacity, void* d_ws, uint64_t ws_bytes, uint64_t* d_out_size,
+                int* d_status, cudaStream_t stream, bool device_cb) {
     EncodeArgs a;
     Workspace W;
     int st = prepare_encode(d_in, n, dtype, cb, chunk_elems, d_out, out_capacity, d_ws, ws_bytes, d_out_size,
-                            d_status, &a, &W);
+                            d_status, &a, &W, device_cb);
     if (st != SPLITZIP_OK) return st;
     DeviceState d;
     if ((st = device_state(&d)) != SPLITZIP_OK) return st;
@@ -272,7 +282,8 @@ int splitzip_encode(const void* d_in, uint64_t n, int dtype, const splitzip_code
     if ((st = make_input_map(d_in, dtype, &a, &map)) != SPLITZIP_OK) return st;
     EncodeLut lut;
     std::memset(lut.code, kEscapeFlag, sizeof(lut.code));
-    for (int k = 0; k < 16; ++k) lut.code[cb->exps[k]] = uint8_t(k);
+    if (!device_cb)
+        for (int k = 0; k < 16; ++k) lut.code[cb->exps[k]] = uint8_t(k);
     // errors are recorded into the status word with compare-and-swap
     if (cudaMemsetAsync(d_status, 0, sizeof(int), stream) != cudaSuccess) {
         cudaGetLastError();
@@ -280,6 +291,33 @@ int splitzip_encode(const void* d_in, uint64_t n, int dtype, const splitzip_code
     }
     const int grid = grid_for(a.n_tiles, d.sms, d.encode_bpsm[dtype]);
     return launch_encode(a, lut, map, grid, stream) == cudaSuccess ? SPLITZIP_OK : SPLITZIP_ERR_CUDA;
+}
+
+}  // namespace
+
+int splitzip_encode(const void* d_in, uint64_t n, int dtype, const splitzip_codebook_t* cb, uint32_t chunk_elems,
+                    void* d_out, uint64_t out_capacity, void* d_ws, uint64_t ws_bytes, uint64_t* d_out_size,
+                    int* d_status, cudaStream_t stream) {
+    return encode_call(d_in, n, dtype, cb, chunk_elems, d_out, out_capacity, d_ws, ws_bytes, d_out_size, d_status,
+                       stream, false);
+}
+
+int splitzip_encode_device_codebook(const void* d_in, uint64_t n, int dtype, const splitzip_codebook_t* d_cb,
+                                    uint32_t chunk_elems, void* d_out, uint64_t out_capacity, void* d_ws,
+                                    uint64_t ws_bytes, uint64_t* d_out_size, int* d_status, cudaStream_t stream) {
+    return encode_call(d_in, n, dtype, d_cb, chunk_elems, d_out, out_capacity, d_ws, ws_bytes, d_out_size, d_status,
+                       stream, true);
+}
+
+int splitzip_calibrate_device(const void* d_x, uint64_t n, int dtype, uint64_t* d_hist256,
+                              splitzip_codebook_t* d_cb, cudaStream_t stream) {
+    if (!d_cb) return SPLITZIP_ERR_INVALID_ARG;
+    const int st = splitzip_exponent_histogram(d_x, n, dtype, d_hist256, stream);
+    if (st != SPLITZIP_OK) return st;
+    return launch_codebook(reinterpret_cast<const unsigned long long*>(d_hist256), dtype,
+                           reinterpret_cast<uint8_t*>(d_cb), stream) == cudaSuccess
+               ? SPLITZIP_OK
+               : SPLITZIP_ERR_CUDA;
 }
 
 int splitzip_decode(const void* d_in, uint64_t in_bytes, void* d_out, uint64_t n, int dtype, int* d_status,

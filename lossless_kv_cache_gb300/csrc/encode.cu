@@ -115,7 +115,7 @@ __device__ __forceinline__ uint4 load_partial(const uint8_t* p, uint32_t nbytes)
 
 // Header fields known before any tile is encoded (E is written at the end),
 // and the zero padding between sections, whose places depend only on n.
-__device__ void write_header_and_padding(const EncodeArgs& a) {
+__device__ void write_header_and_padding(const EncodeArgs& a, const uint8_t* codebook) {
     uint8_t* h = a.out;
     uint32_t* h32 = reinterpret_cast<uint32_t*>(h);
     h32[0] = kMagic;
@@ -126,8 +126,8 @@ __device__ void write_header_and_padding(const EncodeArgs& a) {
     uint32_t cb[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i)
-        cb[i] = uint32_t(a.codebook[4 * i]) | (uint32_t(a.codebook[4 * i + 1]) << 8) |
-                (uint32_t(a.codebook[4 * i + 2]) << 16) | (uint32_t(a.codebook[4 * i + 3]) << 24);
+        cb[i] = uint32_t(codebook[4 * i]) | (uint32_t(codebook[4 * i + 1]) << 8) |
+                (uint32_t(codebook[4 * i + 2]) << 16) | (uint32_t(codebook[4 * i + 3]) << 24);
     reinterpret_cast<uint4*>(h)[2] = make_uint4(cb[0], cb[1], cb[2], cb[3]);
     reinterpret_cast<uint4*>(h)[3] = make_uint4(0u, 0u, 0u, 0u);
     const Layout L = layout_for(a.n, a.dtype, a.chunk_elems, 0);
@@ -206,18 +206,41 @@ __global__ void __launch_bounds__(kBlock, kMinBlocks<DT>)
     __shared__ __align__(8) uint64_t full_bar[kStages];
     __shared__ __align__(8) uint64_t empty_bar[kStages];
     __shared__ __align__(16) uint32_t tab[4 * 256];
+    __shared__ uint8_t code_s[256];  // exponent -> code | kEscapeFlag
+    __shared__ uint8_t cb_s[16];     // code -> exponent (the header's codebook)
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     // the ring starts on a 1024-byte boundary of the shared window
     uint8_t* ring = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-    for (int i = tid; i < 4 * 256; i += kBlock) tab[i] = table_entry(DT, i >> 8, uint32_t(i & 255), lut.code);
+    if (a.dev_codebook) {
+        // a codebook in device memory (online calibration): checked here, on
+        // the GPU (its dtype, every exponent in range, all distinct); a bad
+        // one is reported and leaves the output unspecified
+        for (int i = tid; i < 256; i += kBlock) code_s[i] = kEscapeFlag;
+        if (tid < 16) cb_s[tid] = a.dev_codebook[1 + tid];
+        __syncthreads();
+        if (tid == 0) {
+            bool ok = a.dev_codebook[0] == uint8_t(a.dtype);
+            for (int k = 0; k < 16; ++k) {
+                const uint32_t e = cb_s[k];
+                ok &= e < (DT == SPLITZIP_BF16 ? 256u : 32u) && code_s[e] == kEscapeFlag;
+                code_s[e] = uint8_t(k);
+            }
+            if (!ok) report(a.error, SPLITZIP_ERR_INVALID_ARG);
+        }
+    } else {
+        for (int i = tid; i < 256; i += kBlock) code_s[i] = lut.code[i];
+        if (tid < 16) cb_s[tid] = a.codebook[tid];
+    }
+    __syncthreads();
+    for (int i = tid; i < 4 * 256; i += kBlock) tab[i] = table_entry(DT, i >> 8, uint32_t(i & 255), code_s);
     if (tid == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&full_bar[s], 1);
             mbar_init(&empty_bar[s], kConsumerWarps);
         }
         mbar_init_fence();
-        if (blockIdx.x == 0) write_header_and_padding(a);
+        if (blockIdx.x == 0) write_header_and_padding(a, cb_s);
     }
     __syncthreads();
 

@@ -1,4 +1,4 @@
-// Exponent histogram for offline codebook calibration (sm_103a).
+// Exponent histogram and Top-16 codebook for calibration (sm_103a).
 //
 // "SplitZip: Ultra Fast Lossless KV Compression for Disaggregated LLM
 // Serving", Results, "Ablations: Calibration": one codebook calibrated
@@ -63,7 +63,31 @@ histogram_kernel(const uint8_t* x, uint64_t n, unsigned long long* hist) {
     }
 }
 
+// Top-16 of the histogram (Method, "Top-16 exponent coding"): bin t's rank
+// is the number of bins with a larger count, or an equal count and a smaller
+// exponent -- the order of a stable sort by descending count -- and the bins
+// of rank < 16 are the codebook, code = rank.  Exponents that never occur
+// fill the remaining codes in ascending order.
+__global__ void __launch_bounds__(256) codebook_kernel(const unsigned long long* hist, int dtype, uint8_t* cb) {
+    __shared__ unsigned long long h[256];
+    const int t = threadIdx.x;
+    const int bins = dtype == SPLITZIP_BF16 ? 256 : 32;
+    h[t] = t < bins ? hist[t] : 0ull;
+    __syncthreads();
+    if (t < bins) {
+        int rank = 0;
+        for (int j = 0; j < bins; ++j) rank += (h[j] > h[t]) || (h[j] == h[t] && j < t);
+        if (rank < 16) cb[1 + rank] = uint8_t(t);
+    }
+    if (t == 0) cb[0] = uint8_t(dtype);
+}
+
 }  // namespace
+
+cudaError_t launch_codebook(const unsigned long long* hist, int dtype, uint8_t* cb, cudaStream_t s) {
+    codebook_kernel<<<1, 256, 0, s>>>(hist, dtype, cb);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_histogram(const void* x, uint64_t n, int dtype, unsigned long long* hist, int grid,
                              cudaStream_t s) {

@@ -110,6 +110,9 @@ struct EncodeArgs {
     uint32_t box_bytes;
     int dtype;
     uint8_t codebook[16];
+    // a splitzip_codebook_t in device memory (dtype byte, then the 16
+    // exponents) that replaces codebook[] and the host-built table, or null
+    const uint8_t* dev_codebook;
 };
 
 struct DecodeArgs {
@@ -126,6 +129,9 @@ struct DecodeArgs {
 cudaError_t launch_encode(const EncodeArgs& a, const EncodeLut& lut, const CUtensorMap& map, int grid,
                           cudaStream_t s);
 cudaError_t launch_decode(const DecodeArgs& a, int grid, cudaStream_t s);
+// One CTA: the Top-16 codebook of a device histogram into a device
+// splitzip_codebook_t (count descending, exponent ascending on ties).
+cudaError_t launch_codebook(const unsigned long long* hist, int dtype, uint8_t* cb, cudaStream_t s);
 cudaError_t launch_histogram(const void* x, uint64_t n, int dtype, unsigned long long* hist, int grid,
                              cudaStream_t s);
 

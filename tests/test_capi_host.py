@@ -185,3 +185,16 @@ def test_pointer_arguments_reject_non_addresses(splitzip_lib):
     assert sz._Address.from_param(None) is None
     assert sz._Address.from_param(T()).value == 1 << 20
     assert sz._Address.from_param(1 << 40).value == 1 << 40
+
+
+def test_online_calibration_argument_errors(splitzip_lib):
+    A = 1 << 20  # fake device addresses: every call below fails before the GPU
+    assert sz.splitzip_calibrate_device(A, 100, sz.BF16, A, None, 0) == sz.ERR_INVALID_ARG      # no codebook
+    assert sz.splitzip_calibrate_device(A, 100, 7, A, A, 0) == sz.ERR_INVALID_ARG               # dtype
+    assert sz.splitzip_calibrate_device(A, 100, sz.BF16, A + 8, A, 0) == sz.ERR_INVALID_ARG     # misaligned
+    ws = sz.workspace_size(1000, sz.BF16, 64)
+    cap = sz.max_compressed_size(1000, sz.BF16, 64)
+    f = sz.splitzip_encode_device_codebook
+    assert f(A, 1000, sz.BF16, None, 64, A, cap, A, ws, A, A, 0) == sz.ERR_INVALID_ARG          # no codebook
+    assert f(A, 1000, sz.BF16, A, 96, A, cap, A, ws, A, A, 0) == sz.ERR_INVALID_ARG             # chunk
+    assert f(A, 1000, sz.BF16, A, 64, A, cap - 1, A, ws, A, A, 0) == sz.ERR_CAPACITY            # output
