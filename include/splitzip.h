@@ -217,6 +217,34 @@ int splitzip_encode_noalloc(const void* d_in, uint64_t n, int dtype, const split
 int splitzip_decode(const void* d_in, uint64_t in_bytes, void* d_out, uint64_t n, int dtype,
                     int* d_status, cudaStream_t stream);
 
+/* Paged KV cache (serving engines keep a cache in fixed-size pages of a pool,
+ * listed per request in a page table; a transfer gathers them on the sending
+ * side and scatters them on the receiving one).  d_pool holds pool_pages
+ * pages of page_elems elements each (page_elems a power of two); d_pages
+ * (device int32, n_pages entries) lists the pages of the tensor in order.
+ * splitzip_encode_paged encodes the n_pages * page_elems elements of those
+ * pages, gathered by the encoder's tensor-map copies straight from the pool:
+ * the container is byte-identical to splitzip_encode of the gathered tensor.
+ * page_elems must be a multiple of the encoder's tile (8,192 BF16 or 16,384
+ * E5M2 elements, or chunk_elems when that is smaller).  The workspace and
+ * output sizes are those of n = n_pages * page_elems elements.  A page index
+ * outside [0, pool_pages) is reported in *d_status as
+ * SPLITZIP_ERR_INVALID_ARG (and never read). */
+int splitzip_encode_paged(const void* d_pool, uint64_t pool_pages, const int32_t* d_pages, uint64_t n_pages,
+                          uint64_t page_elems, int dtype, const splitzip_codebook_t* cb, uint32_t chunk_elems,
+                          void* d_out, uint64_t out_capacity, void* d_ws, uint64_t ws_bytes, uint64_t* d_out_size,
+                          int* d_status, cudaStream_t stream);
+
+/* Decode a container of n_pages * page_elems elements into the pages listed
+ * in d_pages of the pool d_pool (element g goes to element g mod page_elems
+ * of page d_pages[g / page_elems]); every other byte of the pool is left as
+ * it is.  page_elems: a power of two >= 16.  Checks as splitzip_decode; a
+ * page index outside the pool is reported (SPLITZIP_ERR_INVALID_ARG in
+ * *d_status) and never written. */
+int splitzip_decode_paged(const void* d_in, uint64_t in_bytes, void* d_pool, uint64_t pool_pages,
+                          const int32_t* d_pages, uint64_t n_pages, uint64_t page_elems, int dtype, int* d_status,
+                          cudaStream_t stream);
+
 /* Parse and check a container header held in host memory (bytes >= 64).
  * Returns SPLITZIP_ERR_CORRUPT for a malformed header or a size larger than
  * `bytes`. */

@@ -105,6 +105,9 @@ SIGNATURES = {
     "splitzip_decode": (_int, [_vp, _u64, _vp, _u64, _int, _vp, _vp]),
     "splitzip_parse_header": (_int, [_vp, _u64, ctypes.POINTER(Header)]),
     "splitzip_calibrate_device": (_int, [_vp, _u64, _int, _vp, _vp, _vp]),
+    "splitzip_encode_paged": (_int, [_vp, _u64, _vp, _u64, _u64, _int, ctypes.POINTER(Codebook), _u32, _vp, _u64, _vp,
+                                     _u64, _vp, _vp, _vp]),
+    "splitzip_decode_paged": (_int, [_vp, _u64, _vp, _u64, _vp, _u64, _u64, _int, _vp, _vp]),
     "splitzip_encode_device_codebook": (_int, [_vp, _u64, _int, _vp, _u32, _vp, _u64, _vp, _u64, _vp, _vp, _vp]),
     "splitzip_transfer_scratch_size": (_int, [_u64, _int, _u32, _u64, _int, _P_u64, _P_u64]),
     "splitzip_transfer": (_int, [_vp, _vp, _u64, _int, ctypes.POINTER(Codebook), _u32, _u64, _int, _vp, _u64, _vp,
@@ -173,6 +176,17 @@ def splitzip_decode(d_in, in_bytes, d_out, n, dtype, d_status, stream):
 
 def splitzip_parse_header(h_blob, nbytes, out):
     return lib().splitzip_parse_header(h_blob, nbytes, ctypes.byref(out))
+
+
+def splitzip_encode_paged(d_pool, pool_pages, d_pages, n_pages, page_elems, dtype, cb, chunk_elems, d_out,
+                          out_capacity, d_ws, ws_bytes, d_out_size, d_status, stream):
+    return lib().splitzip_encode_paged(d_pool, pool_pages, d_pages, n_pages, page_elems, dtype, ctypes.byref(cb),
+                                       chunk_elems, d_out, out_capacity, d_ws, ws_bytes, d_out_size, d_status, stream)
+
+
+def splitzip_decode_paged(d_in, in_bytes, d_pool, pool_pages, d_pages, n_pages, page_elems, dtype, d_status, stream):
+    return lib().splitzip_decode_paged(d_in, in_bytes, d_pool, pool_pages, d_pages, n_pages, page_elems, dtype,
+                                       d_status, stream)
 
 
 def splitzip_calibrate_device(d_x, n, dtype, d_hist256, d_cb, stream):
@@ -365,3 +379,19 @@ def encode_into_device_codebook(x, d_cb, bufs, stream=None):
                                            bufs.out.data_ptr(), bufs.capacity, bufs.ws.data_ptr(), bufs.ws_bytes,
                                            bufs.size.data_ptr(), bufs.status.data_ptr(), _stream_handle(stream)),
            "splitzip_encode_device_codebook")
+
+
+def encode_paged_into(pool, pages, page_elems, cb, bufs, stream=None):
+    """Encode the pages `pages` (device int32 tensor) of `pool` (a device tensor
+    of whole pages, raw bits) into `bufs` (sized for len(pages) * page_elems)."""
+    _check(splitzip_encode_paged(pool.data_ptr(), pool.numel() // page_elems, pages.data_ptr(), pages.numel(),
+                                 page_elems, bufs.dtype, cb, bufs.chunk_elems, bufs.out.data_ptr(), bufs.capacity,
+                                 bufs.ws.data_ptr(), bufs.ws_bytes, bufs.size.data_ptr(), bufs.status.data_ptr(),
+                                 _stream_handle(stream)), "splitzip_encode_paged")
+
+
+def decode_paged_into(blob, in_bytes, pool, pages, page_elems, dtype, status, stream=None):
+    """Decode a container into the pages `pages` of `pool`."""
+    _check(splitzip_decode_paged(blob.data_ptr(), in_bytes, pool.data_ptr(), pool.numel() // page_elems,
+                                 pages.data_ptr(), pages.numel(), page_elems, dtype, status.data_ptr(),
+                                 _stream_handle(stream)), "splitzip_decode_paged")

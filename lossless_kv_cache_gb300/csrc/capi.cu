@@ -159,10 +159,10 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 // 64 bytes) fits in one row and is copied unswizzled.  Row coordinates are
 // 32-bit signed, so at most 2^31 - 256 rows are mapped; bytes past them are
 // also read directly.
-int make_input_map(const void* d_in, int dtype, EncodeArgs* a, CUtensorMap* map) {
+int make_input_map(const void* d_in, int dtype, EncodeArgs* a, CUtensorMap* map, uint64_t in_bytes) {
     std::memset(map, 0, sizeof(*map));
     const uint64_t eb = elem_bytes(dtype);
-    const uint64_t rows = std::min<uint64_t>(a->n * eb / 128u, (uint64_t(1) << 31) - 256u);
+    const uint64_t rows = std::min<uint64_t>(in_bytes / 128u, (uint64_t(1) << 31) - 256u);
     if (rows == 0) return SPLITZIP_OK;  // every byte is read directly
     PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
     if (!encode) return SPLITZIP_ERR_CUDA;
@@ -268,18 +268,36 @@ int splitzip_exponent_histogram(const void* d_x, uint64_t n, int dtype, uint64_t
 
 namespace {
 
+// Paged input for encode_call: the pool and its page list (null: contiguous).
+struct PagedInput {
+    const int32_t* pages = nullptr;
+    uint64_t pool_pages = 0, page_elems = 0;
+};
+
 int encode_call(const void* d_in, uint64_t n, int dtype, const splitzip_codebook_t* cb, uint32_t chunk_elems,
                 void* d_out, uint64_t out_capacity, void* d_ws, uint64_t ws_bytes, uint64_t* d_out_size,
-                int* d_status, cudaStream_t stream, bool device_cb) {
+                int* d_status, cudaStream_t stream, bool device_cb, const PagedInput& paged = PagedInput()) {
     EncodeArgs a;
     Workspace W;
     int st = prepare_encode(d_in, n, dtype, cb, chunk_elems, d_out, out_capacity, d_ws, ws_bytes, d_out_size,
                             d_status, &a, &W, device_cb);
     if (st != SPLITZIP_OK) return st;
+    const uint64_t eb = elem_bytes(dtype);
+    a.pages = paged.pages;
+    a.pool_pages = paged.pool_pages;
+    a.page_tile_shift = 0;
+    if (paged.pages) {
+        const uint64_t tiles_per_page = paged.page_elems / a.tile_elems;
+        while ((uint64_t(1) << a.page_tile_shift) < tiles_per_page) ++a.page_tile_shift;
+        // the tensor map must reach every byte of the pool
+        if (paged.pool_pages * paged.page_elems * eb > ((uint64_t(1) << 31) - 256u) * 128u)
+            return SPLITZIP_ERR_UNSUPPORTED;
+    }
     DeviceState d;
     if ((st = device_state(&d)) != SPLITZIP_OK) return st;
     CUtensorMap map;
-    if ((st = make_input_map(d_in, dtype, &a, &map)) != SPLITZIP_OK) return st;
+    const uint64_t mapped = paged.pages ? paged.pool_pages * paged.page_elems * eb : n * eb;
+    if ((st = make_input_map(d_in, dtype, &a, &map, mapped)) != SPLITZIP_OK) return st;
     EncodeLut lut;
     std::memset(lut.code, kEscapeFlag, sizeof(lut.code));
     if (!device_cb)
@@ -320,8 +338,10 @@ int splitzip_calibrate_device(const void* d_x, uint64_t n, int dtype, uint64_t* 
                : SPLITZIP_ERR_CUDA;
 }
 
-int splitzip_decode(const void* d_in, uint64_t in_bytes, void* d_out, uint64_t n, int dtype, int* d_status,
-                    cudaStream_t stream) {
+namespace {
+
+int decode_call(const void* d_in, uint64_t in_bytes, void* d_out, uint64_t n, int dtype, int* d_status,
+                cudaStream_t stream, const int32_t* pages, uint64_t pool_pages, uint32_t page_shift) {
     if (!valid_dtype(dtype) || !d_in || !aligned(d_in, 16) || !d_status || !aligned(d_status, 4))
         return SPLITZIP_ERR_INVALID_ARG;
     if (n > 0 && (!d_out || !aligned(d_out, 16))) return SPLITZIP_ERR_INVALID_ARG;
@@ -341,8 +361,54 @@ int splitzip_decode(const void* d_in, uint64_t in_bytes, void* d_out, uint64_t n
     a.n = n;
     a.dtype = dtype;
     a.status = d_status;
+    a.pages = pages;
+    a.pool_pages = pool_pages;
+    a.page_shift = page_shift;
     const int grid = grid_for((n + kMinChunk - 1) / kMinChunk, d.sms, d.decode_bpsm[dtype]);
     return launch_decode(a, grid, stream) == cudaSuccess ? SPLITZIP_OK : SPLITZIP_ERR_CUDA;
+}
+
+bool pow2(uint64_t x) { return x != 0 && (x & (x - 1)) == 0; }
+
+uint32_t log2_of(uint64_t x) {
+    uint32_t k = 0;
+    while ((uint64_t(1) << k) < x) ++k;
+    return k;
+}
+
+}  // namespace
+
+int splitzip_decode(const void* d_in, uint64_t in_bytes, void* d_out, uint64_t n, int dtype, int* d_status,
+                    cudaStream_t stream) {
+    return decode_call(d_in, in_bytes, d_out, n, dtype, d_status, stream, nullptr, 0, 0);
+}
+
+int splitzip_encode_paged(const void* d_pool, uint64_t pool_pages, const int32_t* d_pages, uint64_t n_pages,
+                          uint64_t page_elems, int dtype, const splitzip_codebook_t* cb, uint32_t chunk_elems,
+                          void* d_out, uint64_t out_capacity, void* d_ws, uint64_t ws_bytes, uint64_t* d_out_size,
+                          int* d_status, cudaStream_t stream) {
+    if (!valid_dtype(dtype) || !valid_chunk(chunk_elems)) return SPLITZIP_ERR_INVALID_ARG;
+    if (!d_pages || !aligned(d_pages, 4) || n_pages == 0 || pool_pages == 0 || !pow2(page_elems) ||
+        page_elems % tile_elems_for(dtype, chunk_elems) != 0)
+        return SPLITZIP_ERR_INVALID_ARG;
+    if (n_pages > kMaxElems / page_elems || pool_pages > kMaxElems / page_elems) return SPLITZIP_ERR_UNSUPPORTED;
+    PagedInput paged;
+    paged.pages = d_pages;
+    paged.pool_pages = pool_pages;
+    paged.page_elems = page_elems;
+    return encode_call(d_pool, n_pages * page_elems, dtype, cb, chunk_elems, d_out, out_capacity, d_ws, ws_bytes,
+                       d_out_size, d_status, stream, false, paged);
+}
+
+int splitzip_decode_paged(const void* d_in, uint64_t in_bytes, void* d_pool, uint64_t pool_pages,
+                          const int32_t* d_pages, uint64_t n_pages, uint64_t page_elems, int dtype, int* d_status,
+                          cudaStream_t stream) {
+    if (!valid_dtype(dtype) || !d_pages || !aligned(d_pages, 4) || n_pages == 0 || pool_pages == 0 ||
+        !pow2(page_elems) || page_elems < 16)
+        return SPLITZIP_ERR_INVALID_ARG;
+    if (n_pages > kMaxElems / page_elems || pool_pages > kMaxElems / page_elems) return SPLITZIP_ERR_UNSUPPORTED;
+    return decode_call(d_in, in_bytes, d_pool, n_pages * page_elems, dtype, d_status, stream, d_pages, pool_pages,
+                       log2_of(page_elems));
 }
 
 int splitzip_parse_header(const void* h_blob, uint64_t bytes, splitzip_header_t* out) {

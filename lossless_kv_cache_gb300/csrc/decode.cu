@@ -175,9 +175,39 @@ __device__ __forceinline__ SubTile subtile_windows(const uint8_t* nibbles, const
 // Dense decode of one sub-tile from shared memory; results go straight to
 // global memory with 16-byte streaming stores.  Unit u (UE elements) of the
 // sub-tile is decoded by thread u mod 256 in round u / 256.
-template <int DT>
-__device__ __forceinline__ void decode_subtile(const uint8_t* nb, const uint8_t* sb, void* out_base, uint64_t g,
-                                               uint32_t cnt, int tid, const uint16_t* lut2) {
+// Where element g of the tensor is written: itself (contiguous output) or,
+// with paged output, element g mod 2^shift of pool page pages[g >> shift].
+// A page index outside the pool is reported and its elements are not
+// written.  The 16-byte units and the 4-byte words the decoder writes never
+// straddle a page (pages hold a power of two >= 16 elements).
+template <bool PAGED>
+struct OutMap {
+    uint8_t* base;
+    uint64_t limit;  // bytes of the output (tensor or pool)
+    const int32_t* pages;
+    uint64_t pool_pages;
+    uint32_t shift;
+    int* status;
+    __device__ __forceinline__ bool at(uint64_t g, uint32_t eb, uint64_t& off) const {
+        if constexpr (!PAGED) {
+            off = g * eb;
+            return true;
+        } else {
+            const int64_t p = pages[g >> shift];
+            if (p < 0 || uint64_t(p) >= pool_pages) {
+                atomicCAS(status, SPLITZIP_OK, SPLITZIP_ERR_INVALID_ARG);
+                return false;
+            }
+            off = ((uint64_t(p) << shift) | (g & ((uint64_t(1) << shift) - 1u))) * eb;
+            return true;
+        }
+    }
+};
+
+template <int DT, bool PAGED>
+__device__ __forceinline__ void decode_subtile(const uint8_t* nb, const uint8_t* sb, const OutMap<PAGED>& om,
+                                               uint64_t g, uint32_t cnt, int tid, const uint16_t* lut2) {
+    constexpr uint32_t EB = DT == SPLITZIP_BF16 ? 2u : 1u;
     constexpr uint32_t UE = DT == SPLITZIP_BF16 ? 8u : 16u;
     const uint32_t units = (cnt + UE - 1u) / UE;
     const uint32_t rounds = (units + kConsumers - 1u) / kConsumers;
@@ -191,15 +221,15 @@ __device__ __forceinline__ void decode_subtile(const uint8_t* nb, const uint8_t*
                 const uint32_t nib = *reinterpret_cast<const uint32_t*>(nb + e / 2);
                 const uint2 sm = *reinterpret_cast<const uint2*>(sb + e);
                 o = decode_unit_bf16(nib, sm, lut2);
-                __stcs(reinterpret_cast<uint4*>(static_cast<uint16_t*>(out_base) + g + e), o);
             } else {
                 // 6 bytes of s3 per unit, 2-byte aligned in the stage
                 const uint16_t* s16 = reinterpret_cast<const uint16_t*>(sb + 6u * u);
                 const uint2 nib = *reinterpret_cast<const uint2*>(nb + e / 2);
                 const uint32_t s3lo = uint32_t(s16[0]) | (uint32_t(s16[1]) << 16), s3hi = s16[2];
                 o = decode_unit_e5m2(nib, s3lo, s3hi, lut2);
-                __stcs(reinterpret_cast<uint4*>(static_cast<uint8_t*>(out_base) + g + e), o);
             }
+            uint64_t off;
+            if (om.at(g + e, EB, off)) __stcs(reinterpret_cast<uint4*>(om.base + off), o);
         } else if (e < cnt) {
             const uint32_t valid = cnt - e;
             uint4 o;
@@ -217,13 +247,16 @@ __device__ __forceinline__ void decode_subtile(const uint8_t* nb, const uint8_t*
                 o = decode_unit_e5m2(make_uint2(uint32_t(nw), uint32_t(nw >> 32)), uint32_t(sw), uint32_t(sw >> 32),
                                      lut2);
             }
-            for (uint32_t b = 0; b < valid; ++b) {
-                const uint32_t q = DT == SPLITZIP_BF16 ? b >> 1 : b >> 2;
-                const uint32_t w = q == 0 ? o.x : q == 1 ? o.y : q == 2 ? o.z : o.w;
-                if constexpr (DT == SPLITZIP_BF16)
-                    static_cast<uint16_t*>(out_base)[g + e + b] = uint16_t(w >> (16u * (b & 1u)));
-                else
-                    static_cast<uint8_t*>(out_base)[g + e + b] = uint8_t(w >> (8u * (b & 3u)));
+            uint64_t off;
+            if (om.at(g + e, EB, off)) {
+                for (uint32_t b = 0; b < valid; ++b) {
+                    const uint32_t q = DT == SPLITZIP_BF16 ? b >> 1 : b >> 2;
+                    const uint32_t w = q == 0 ? o.x : q == 1 ? o.y : q == 2 ? o.z : o.w;
+                    if constexpr (DT == SPLITZIP_BF16)
+                        reinterpret_cast<uint16_t*>(om.base + off)[b] = uint16_t(w >> (16u * (b & 1u)));
+                    else
+                        (om.base + off)[b] = uint8_t(w >> (8u * (b & 3u)));
+                }
             }
         }
     }
@@ -237,14 +270,15 @@ __device__ __forceinline__ void decode_subtile(const uint8_t* nb, const uint8_t*
 // one address stay in order).  Other elements of the word are left as they
 // are; a word that would reach past the output's last byte (only at the very
 // end of an odd-sized output) is patched by a plain read-modify-write.
-template <int DT>
-__device__ __forceinline__ bool patch_one(void* out, uint64_t n, uint64_t base, uint32_t len, int64_t prev,
+template <int DT, bool PAGED>
+__device__ __forceinline__ bool patch_one(const OutMap<PAGED>& om, uint64_t base, uint32_t len, int64_t prev,
                                           uint32_t pos, uint32_t ex) {
     if (pos >= len || int64_t(pos) <= prev || ex >= (DT == SPLITZIP_BF16 ? 256u : 32u)) return false;
     constexpr uint32_t EB = DT == SPLITZIP_BF16 ? 2u : 1u;
-    const uint64_t byte = (base + pos) * EB;
-    uint8_t* o = static_cast<uint8_t*>(out);
-    if ((byte | 3u) < n * EB) {
+    uint64_t byte;
+    if (!om.at(base + pos, EB, byte)) return true;  // (reported: a page outside the pool)
+    uint8_t* o = om.base;
+    if ((byte | 3u) < om.limit) {
         const uint32_t sh = uint32_t(byte & 3u) * 8u + (DT == SPLITZIP_BF16 ? 7u : 2u);
         const uint32_t field = (DT == SPLITZIP_BF16 ? 0xFFu : 0x1Fu) << sh;
         unsigned int* w = reinterpret_cast<unsigned int*>(o + (byte & ~uint64_t(3)));
@@ -261,7 +295,7 @@ __device__ __forceinline__ bool patch_one(void* out, uint64_t n, uint64_t base, 
 
 __device__ __forceinline__ uint32_t rec_pos(const uint8_t* r) { return uint32_t(r[0]) | (uint32_t(r[1]) << 8); }
 
-template <int DT>
+template <int DT, bool PAGED>
 __global__ void __launch_bounds__(kBlock, kDecodeMinBlocks<DT>) decode_kernel(const DecodeArgs a) {
     extern __shared__ __align__(128) uint8_t stages[];
     __shared__ __align__(8) uint64_t full_bar[kStages<DT>];
@@ -306,6 +340,10 @@ __global__ void __launch_bounds__(kBlock, kDecodeMinBlocks<DT>) decode_kernel(co
     const uint32_t* counts = reinterpret_cast<const uint32_t*>(in + L.counts_off);
     const uint8_t* records = in + L.escrec_off;  // 3 bytes each: position u16 LE, exponent
     const uint64_t chunk = hdr.chunk, C = hdr.n_chunks, E = hdr.E;
+    const uint32_t EBo = DT == SPLITZIP_BF16 ? 2u : 1u;
+    const OutMap<PAGED> om{static_cast<uint8_t*>(a.out),
+                           PAGED ? (a.pool_pages << a.page_shift) * EBo : a.n * EBo,
+                           a.pages, a.pool_pages, a.page_shift, a.status};
     const uint32_t sub = uint32_t(min(uint64_t(kSub<DT>), chunk));
 
     if (warp == kConsumerWarps) {
@@ -380,7 +418,7 @@ __global__ void __launch_bounds__(kBlock, kDecodeMinBlocks<DT>) decode_kernel(co
                 const uint32_t n_in = named_barrier_popc(1, kConsumers, mine);
                 if (mine) {
                     const int64_t prev = i == 0 ? -1 : int64_t(rec_pos(recs + 3 * (i - 1)));
-                    bad |= !patch_one<DT>(a.out, a.n, base, len, prev, rec_pos(recs + 3 * i), recs[3 * i + 2]);
+                    bad |= !patch_one<DT, PAGED>(om, base, len, prev, rec_pos(recs + 3 * i), recs[3 * i + 2]);
                 }
                 cursor += n_in;
                 if (n_in < kConsumers) break;
@@ -392,7 +430,8 @@ __global__ void __launch_bounds__(kBlock, kDecodeMinBlocks<DT>) decode_kernel(co
             if (!mbar_wait(&full_bar[stage], use & 1u)) report(a.status, SPLITZIP_ERR_TIMEOUT);
             const SubTile t = subtile_windows<DT>(nibbles, signmant, base + s0, n_sub);
             const uint8_t* src = stages + stage * kStageBytes<DT>;
-            decode_subtile<DT>(src + t.nib.offset, src + kNibCap<DT> + t.sm.offset, a.out, base + s0, n_sub, tid, lut2);
+            decode_subtile<DT, PAGED>(src + t.nib.offset, src + kNibCap<DT> + t.sm.offset, om, base + s0, n_sub, tid,
+                                      lut2);
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty_bar[stage]);
             if (!patch) continue;
@@ -412,19 +451,31 @@ __global__ void __launch_bounds__(kBlock, kDecodeMinBlocks<DT>) decode_kernel(co
 }  // namespace
 
 cudaError_t launch_decode(const DecodeArgs& a, int grid, cudaStream_t s) {
-    if (a.dtype == SPLITZIP_BF16)
-        decode_kernel<SPLITZIP_BF16><<<grid, kBlock, kDecodeSmem<SPLITZIP_BF16>, s>>>(a);
-    else
-        decode_kernel<SPLITZIP_FP8_E5M2><<<grid, kBlock, kDecodeSmem<SPLITZIP_FP8_E5M2>, s>>>(a);
+    const bool paged = a.pages != nullptr;
+    if (a.dtype == SPLITZIP_BF16) {
+        if (paged)
+            decode_kernel<SPLITZIP_BF16, true><<<grid, kBlock, kDecodeSmem<SPLITZIP_BF16>, s>>>(a);
+        else
+            decode_kernel<SPLITZIP_BF16, false><<<grid, kBlock, kDecodeSmem<SPLITZIP_BF16>, s>>>(a);
+    } else {
+        if (paged)
+            decode_kernel<SPLITZIP_FP8_E5M2, true><<<grid, kBlock, kDecodeSmem<SPLITZIP_FP8_E5M2>, s>>>(a);
+        else
+            decode_kernel<SPLITZIP_FP8_E5M2, false><<<grid, kBlock, kDecodeSmem<SPLITZIP_FP8_E5M2>, s>>>(a);
+    }
     return cudaGetLastError();
 }
 
-// Also raises the kernels' dynamic shared-memory limit (once per device).
+// Also raises the kernels' dynamic shared-memory limit (once per device, for
+// the contiguous and the paged instances); the occupancy is the contiguous
+// instance's.
 cudaError_t occupancy_decode(int* blocks_per_sm, int dtype) {
-    auto k = dtype == SPLITZIP_BF16 ? decode_kernel<SPLITZIP_BF16> : decode_kernel<SPLITZIP_FP8_E5M2>;
-    const int smem =
-        int(dtype == SPLITZIP_BF16 ? kDecodeSmem<SPLITZIP_BF16> : kDecodeSmem<SPLITZIP_FP8_E5M2>);
+    const bool bf16 = dtype == SPLITZIP_BF16;
+    auto k = bf16 ? decode_kernel<SPLITZIP_BF16, false> : decode_kernel<SPLITZIP_FP8_E5M2, false>;
+    auto kp = bf16 ? decode_kernel<SPLITZIP_BF16, true> : decode_kernel<SPLITZIP_FP8_E5M2, true>;
+    const int smem = int(bf16 ? kDecodeSmem<SPLITZIP_BF16> : kDecodeSmem<SPLITZIP_FP8_E5M2>);
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(kp, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, k, kBlock, smem);
 }

@@ -249,11 +249,26 @@ __global__ void __launch_bounds__(kBlock, kMinBlocks<DT>)
     if (warp == kConsumerWarps) {
         // ---- producer: stream the CTA's tiles (blockIdx.x + k * gridDim.x) ----
         if (lane != 0) return;
+        // the pool tile that holds tile t (paged input; a page index outside
+        // the pool is reported and read as page 0, inside the pool)
+        auto source_tile = [&](uint64_t t) -> uint64_t {
+            if (!a.pages) return t;
+            int64_t p = a.pages[t >> a.page_tile_shift];
+            if (p < 0 || uint64_t(p) >= a.pool_pages) {
+                report(a.error, SPLITZIP_ERR_INVALID_ARG);
+                p = 0;
+            }
+            return (uint64_t(p) << a.page_tile_shift) | (t & ((uint64_t(1) << a.page_tile_shift) - 1u));
+        };
         uint32_t it = 0;
+        uint64_t src_next = blockIdx.x < a.n_tiles ? source_tile(blockIdx.x) : 0;
         for (uint64_t t = blockIdx.x; t < a.n_tiles; t += gridDim.x, ++it) {
             const uint32_t stage = it % kStages, use = it / kStages;
+            const uint64_t src = src_next;
+            // the next tile's page lookup is issued before this stage's wait
+            if (t + gridDim.x < a.n_tiles) src_next = source_tile(t + gridDim.x);
             if (use > 0 && !mbar_wait(&empty_bar[stage], (use - 1) & 1u)) report(a.error, SPLITZIP_ERR_TIMEOUT);
-            const uint64_t tb = t * tile_bytes;
+            const uint64_t tb = src * tile_bytes;
             if (tb < a.tensor_bytes) {
                 mbar_arrive_expect_tx(&full_bar[stage], a.box_bytes);
                 tensor_load_2d(ring + stage * kStageBytes, &map, int32_t((tb & 127u) / EB), int32_t(tb >> 7),
@@ -286,9 +301,11 @@ __global__ void __launch_bounds__(kBlock, kMinBlocks<DT>)
         const uint64_t rem = a.n - base;
         const uint32_t len = rem < a.tile_elems ? uint32_t(rem) : a.tile_elems;
         const uint64_t tb = base * EB;
-        // bytes of this tile that the tensor-map copy delivered
+        // bytes of this tile that the tensor-map copy delivered (paged input:
+        // whole tiles inside the mapped pool, every time)
         const uint32_t in_stage =
-            tb >= a.tensor_bytes ? 0u : uint32_t(min(uint64_t(tile_bytes), a.tensor_bytes - tb));
+            a.pages ? tile_bytes
+                    : (tb >= a.tensor_bytes ? 0u : uint32_t(min(uint64_t(tile_bytes), a.tensor_bytes - tb)));
         const uint32_t pos0 = uint32_t(base & (a.chunk_elems - 1u));  // in-chunk position of element 0
         const uint8_t* st = ring + stage * kStageBytes;
 

@@ -113,6 +113,12 @@ struct EncodeArgs {
     // a splitzip_codebook_t in device memory (dtype byte, then the 16
     // exponents) that replaces codebook[] and the host-built table, or null
     const uint8_t* dev_codebook;
+    // paged input (null: `in` is the tensor): `in` is a pool of pool_pages
+    // pages of 2^page_tile_shift tiles each, and tile t of the tensor is tile
+    // t mod 2^page_tile_shift of pool page pages[t >> page_tile_shift]
+    const int32_t* pages;
+    uint64_t pool_pages;
+    uint32_t page_tile_shift;
 };
 
 struct DecodeArgs {
@@ -122,6 +128,12 @@ struct DecodeArgs {
     uint64_t n;
     int dtype;
     int* status;
+    // paged output (null: `out` is the tensor): `out` is a pool of pool_pages
+    // pages of 2^page_shift elements, and element g goes to element
+    // g mod 2^page_shift of pool page pages[g >> page_shift]
+    const int32_t* pages;
+    uint64_t pool_pages;
+    uint32_t page_shift;
 };
 
 // Launchers (encode.cu, decode.cu, histogram.cu).  Each returns the result of

@@ -198,3 +198,34 @@ def test_online_calibration_argument_errors(splitzip_lib):
     assert f(A, 1000, sz.BF16, None, 64, A, cap, A, ws, A, A, 0) == sz.ERR_INVALID_ARG          # no codebook
     assert f(A, 1000, sz.BF16, A, 96, A, cap, A, ws, A, A, 0) == sz.ERR_INVALID_ARG             # chunk
     assert f(A, 1000, sz.BF16, A, 64, A, cap - 1, A, ws, A, A, 0) == sz.ERR_CAPACITY            # output
+
+
+def test_paged_argument_errors(splitzip_lib):
+    A = 1 << 20  # fake device addresses: every call below fails before the GPU
+    cb = sz.Codebook.make(sz.BF16, range(16))
+    n_pages, page = 4, 16384
+    cap = sz.max_compressed_size(n_pages * page, sz.BF16, 65536)
+    ws = sz.workspace_size(n_pages * page, sz.BF16, 65536)
+    f = sz.splitzip_encode_paged
+    ok = (A, 8, A, n_pages, page, sz.BF16, cb, 65536, A, cap, A, ws, A, A, 0)
+
+    def call(**kw):
+        args = list(ok)
+        names = ["pool", "pool_pages", "pages", "n_pages", "page_elems", "dtype", "cb", "chunk", "out", "cap", "ws",
+                 "ws_bytes", "size", "status", "stream"]
+        for k, v in kw.items():
+            args[names.index(k)] = v
+        return f(*args)
+
+    assert call(page_elems=3 * 8192) == sz.ERR_INVALID_ARG      # not a power of two
+    assert call(page_elems=4096) == sz.ERR_INVALID_ARG          # smaller than a BF16 tile at chunk 65,536
+    assert call(pages=None) == sz.ERR_INVALID_ARG
+    assert call(pages=A + 2) == sz.ERR_INVALID_ARG              # misaligned page table
+    assert call(n_pages=0) == sz.ERR_INVALID_ARG
+    assert call(pool_pages=0) == sz.ERR_INVALID_ARG
+    assert call(cap=cap - 1) == sz.ERR_CAPACITY
+    d = sz.splitzip_decode_paged
+    assert d(A, 1 << 20, A, 8, A, 4, 24, sz.BF16, A, 0) == sz.ERR_INVALID_ARG   # not a power of two
+    assert d(A, 1 << 20, A, 8, A, 4, 8, sz.BF16, A, 0) == sz.ERR_INVALID_ARG    # fewer than 16 elements
+    assert d(A, 1 << 20, A, 8, None, 4, 4096, sz.BF16, A, 0) == sz.ERR_INVALID_ARG
+    assert d(A, 1 << 20, A, 0, A, 4, 4096, sz.BF16, A, 0) == sz.ERR_INVALID_ARG
