@@ -53,6 +53,7 @@ def parse_args():
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-transfer", action="store_true", help="skip the GPU -> host -> GPU transfer leg")
     p.add_argument("--no-online", action="store_true", help="skip the online-calibration leg")
+    p.add_argument("--no-paged", action="store_true", help="skip the paged-KV leg")
     p.add_argument("--layers", type=int, default=32,
                    help="32-layer workloads: encode only L layers (a smaller case for profiling; "
                         "not a bench line)")
@@ -586,6 +587,51 @@ def run_ours(args, world, rank, local):
                   "codebook": [int(v) for v in cb_d[1:17].cpu().tolist()], "verified": on_ok,
                   "what": "per-tensor codebook calibrated on the device from the encoded tensor itself"}
 
+    # ---- paged KV: the workload as a pool of 16,384-element pages (16 tokens
+    # x 8 heads x 128 of one layer's K or V), encoded from a shuffled page
+    # table and decoded into another shuffled one ----
+    paged = None
+    page_elems = 16384
+    if not args.no_paged and n % page_elems == 0 and n // page_elems >= 2:
+        pool_pages = n // page_elems
+        g = torch.Generator()
+        g.manual_seed(11)
+        src_pages = torch.randperm(pool_pages, generator=g).to(torch.int32).to(device)
+        dst_pages = torch.randperm(pool_pages, generator=g).to(torch.int32).to(device)
+
+        def paged_step(ev=None):
+            if ev is not None:
+                ev[0].record(stream)
+            check(sz.splitzip_encode_paged(xp, pool_pages, src_pages.data_ptr(), pool_pages, page_elems, dtype, cb,
+                                           CHUNK, op, cap, wp, ws, bufs.size.data_ptr(), bufs.status.data_ptr(), h),
+                  "encode_paged")
+            if ev is not None:
+                ev[1].record(stream)
+            check(sz.splitzip_decode_paged(op, cap, out.data_ptr(), pool_pages, dst_pages.data_ptr(), pool_pages,
+                                           page_elems, dtype, dstatus.data_ptr(), h), "decode_paged")
+            if ev is not None:
+                ev[2].record(stream)
+
+        for _ in range(2):
+            paged_step()
+        torch.cuda.synchronize()
+        pevs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(10)]
+        for ev in pevs:
+            if flush is not None:
+                flush.fill_(2)
+            paged_step(ev)
+        torch.cuda.synchronize()
+        penc = statistics.mean(e[0].elapsed_time(e[1]) for e in pevs)
+        pdec = statistics.mean(e[1].elapsed_time(e[2]) for e in pevs)
+        p_ok = int(bufs.status[0]) == sz.OK and int(dstatus[0]) == sz.OK and bool(torch.equal(
+            out.view(pool_pages, page_elems)[dst_pages.long()], x.view(pool_pages, page_elems)[src_pages.long()]))
+        paged = {"page_elems": page_elems, "pages": pool_pages, "page_tables": "two seeded random permutations",
+                 "encode_ms": round(penc, 4), "decode_ms": round(pdec, 4),
+                 "encode_gbs": round(raw_bytes / (penc * 1e-3) / 1e9, 2),
+                 "decode_gbs": round(raw_bytes / (pdec * 1e-3) / 1e9, 2),
+                 "vs_contiguous": {"encode": round(enc_ms / penc, 4), "decode": round(dec_ms / pdec, 4)},
+                 "verified": p_ok}
+
     # ---- CPU oracle on a bounded sample (rank 0 only) ----
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -609,7 +655,7 @@ def run_ours(args, world, rank, local):
         "escape_rate": round(E / n, 6), "verified_bit_exact": verified,
         "per_kernel": per_kernel, "link_model": link,
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clk,
-        "transfer": transfer, "online_calibration": online,
+        "transfer": transfer, "online_calibration": online, "paged": paged,
         "gpu_launches": 5 * K,  # timed steps: encode (streaming, group, index, records kernels) + decode
     }
 

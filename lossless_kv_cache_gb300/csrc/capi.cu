@@ -298,6 +298,7 @@ int encode_call(const void* d_in, uint64_t n, int dtype, const splitzip_codebook
     CUtensorMap map;
     const uint64_t mapped = paged.pages ? paged.pool_pages * paged.page_elems * eb : n * eb;
     if ((st = make_input_map(d_in, dtype, &a, &map, mapped)) != SPLITZIP_OK) return st;
+    a.staged_bytes = paged.pages ? ~uint64_t(0) : a.tensor_bytes;
     EncodeLut lut;
     std::memset(lut.code, kEscapeFlag, sizeof(lut.code));
     if (!device_cb)

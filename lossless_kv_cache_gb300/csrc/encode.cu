@@ -302,10 +302,10 @@ __global__ void __launch_bounds__(kBlock, kMinBlocks<DT>)
         const uint32_t len = rem < a.tile_elems ? uint32_t(rem) : a.tile_elems;
         const uint64_t tb = base * EB;
         // bytes of this tile that the tensor-map copy delivered (paged input:
-        // whole tiles inside the mapped pool, every time)
+        // whole tiles inside the mapped pool, every time: staged_bytes is
+        // unbounded there)
         const uint32_t in_stage =
-            a.pages ? tile_bytes
-                    : (tb >= a.tensor_bytes ? 0u : uint32_t(min(uint64_t(tile_bytes), a.tensor_bytes - tb)));
+            tb >= a.staged_bytes ? 0u : uint32_t(min(uint64_t(tile_bytes), a.staged_bytes - tb));
         const uint32_t pos0 = uint32_t(base & (a.chunk_elems - 1u));  // in-chunk position of element 0
         const uint8_t* st = ring + stage * kStageBytes;
 

@@ -108,6 +108,9 @@ struct EncodeArgs {
     // 0 = no tensor map) and the bytes one tensor-map load delivers.
     uint64_t tensor_bytes;
     uint32_t box_bytes;
+    // tensor bytes (from the start) whose tiles arrive through the tensor map:
+    // tensor_bytes, or every byte with paged input
+    uint64_t staged_bytes;
     int dtype;
     uint8_t codebook[16];
     // a splitzip_codebook_t in device memory (dtype byte, then the 16
