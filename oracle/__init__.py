@@ -51,6 +51,12 @@ def lib():
         L.oracle_decode.argtypes = [vp, u64, vp, u64, i32]
         L.oracle_parse_header.restype = i32
         L.oracle_parse_header.argtypes = [vp, u64, ctypes.POINTER(Header)]
+        L.oracle_variant_size.restype = u64
+        L.oracle_variant_size.argtypes = [u64, i32, u32, i32, u64]
+        L.oracle_encode_variant.restype = i32
+        L.oracle_encode_variant.argtypes = [vp, u64, i32, vp, u32, i32, vp, u64, ctypes.POINTER(u64)]
+        L.oracle_decode_variant.restype = i32
+        L.oracle_decode_variant.argtypes = [vp, u64, vp, u64, i32]
         _lib = L
     return _lib
 
@@ -138,3 +144,49 @@ def parse_header(blob):
     h = Header()
     st = lib().oracle_parse_header(_ptr(blob), blob.size, ctypes.byref(h))
     return st, h
+
+
+# ---------------------------------------------------------------- ablation variants
+# (Results, "Ablation Studies"): 1 = Top-8 with 3-bit codes, 2 = Top-15 with a
+# sentinel code; 0 = the main format.  See READINGS V1-V3 in splitzip_oracle.c.
+TOP16, TOP8, TOP15_SENTINEL = 0, 1, 2
+
+
+def variant_codebook(codebook16, variant):
+    """The variant's codebook: the first k exponents of the Top-16 order (the
+    same selection stopped at k), the remaining bytes zero."""
+    k = {TOP16: 16, TOP8: 8, TOP15_SENTINEL: 15}[variant]
+    cb = np.zeros(16, dtype=np.uint8)
+    cb[:k] = np.asarray(codebook16, dtype=np.uint8)[:k]
+    return cb
+
+
+def variant_size(n, dtype, chunk_elems, variant, total_escapes):
+    return int(lib().oracle_variant_size(n, dtype, chunk_elems, variant, total_escapes))
+
+
+def encode_variant(x, dtype, codebook, chunk_elems, variant):
+    x = _check_bits(x, dtype)
+    cb = np.ascontiguousarray(codebook, dtype=np.uint8)
+    cap = variant_size(x.size, dtype, chunk_elems, variant, x.size)
+    out = np.zeros(max(cap, 1), dtype=np.uint8)
+    size = ctypes.c_uint64(0)
+    st = lib().oracle_encode_variant(_ptr(x), x.size, dtype, _ptr(cb), chunk_elems, variant, _ptr(out), cap,
+                                     ctypes.byref(size))
+    if st != OK:
+        raise ValueError("oracle_encode_variant status %d" % st)
+    return out[: size.value].copy()
+
+
+def decode_variant_status(blob, n, dtype):
+    blob = np.ascontiguousarray(blob, dtype=np.uint8)
+    out = np.zeros(n, dtype=np.uint16 if dtype == BF16 else np.uint8)
+    st = lib().oracle_decode_variant(_ptr(blob), blob.size, _ptr(out), n, dtype)
+    return st, out
+
+
+def decode_variant(blob, n, dtype):
+    st, out = decode_variant_status(blob, n, dtype)
+    if st != OK:
+        raise ValueError("oracle_decode_variant status %d" % st)
+    return out

@@ -396,3 +396,241 @@ int oracle_decode(const uint8_t* blob, uint64_t bytes, void* out, uint64_t n, in
     }
     return OR_OK;
 }
+
+/* ======================= ablation variants ==================================
+ * Results, "Ablation Studies" (and Method, the design choice of Top-16 over
+ * Top-15): the page compares Top-16 with Top-8 (fewer exponents, 3-bit codes:
+ * lower coverage, more escapes, less efficient packing) and with Top-15 plus a
+ * sentinel (one code marks an escape; escape positions are not stored but found
+ * from the sentinels: less metadata, irregular decoding).  It gives no format
+ * for either; the plainest forms of what it describes:
+ *
+ *   READING V1  both keep the main container's header, index and sign|mantissa
+ *               stream; header byte 7 (reserved 0 in the main format) names the
+ *               variant: 1 = Top-8, 2 = Top-15 + sentinel (0 = the main format).
+ *   READING V2  Top-8: the 8 most frequent exponents (R1 order) get codes 0..7,
+ *               packed 3 bits per element, LSB-first (as R7), 3 bytes per 8
+ *               elements, zero-padded; escapes exactly as the main format (code
+ *               0, 3-byte (position, exponent) records).  Codebook bytes 8..15
+ *               are zero.
+ *   READING V3  Top-15 + sentinel: the 15 most frequent exponents get codes
+ *               0..14; an escaped element stores code 15 (the sentinel) in the
+ *               nibble stream; the escape stream holds only the escaped
+ *               elements' exponents, one byte each, chunk-major in element
+ *               order (the index still gives each chunk's offset and count).
+ *               Codebook byte 15 is zero.
+ */
+
+static unsigned variant_codes(int variant) { return variant == 1 ? 8u : variant == 2 ? 15u : 16u; }
+
+static layout_t layout_variant(uint64_t n, int dtype, uint32_t chunk, int variant, uint64_t E) {
+    layout_t L;
+    L.n_chunks = (n + chunk - 1u) / chunk;
+    L.index_off = OR_HEADER_BYTES;
+    L.counts_off = L.index_off + 8u * L.n_chunks;
+    L.nib_off = align16(L.counts_off + 4u * L.n_chunks);
+    uint64_t code_bytes = variant == 1 ? 3u * ((n + 7u) / 8u) : (n + 1u) / 2u;
+    L.sm_off = L.nib_off + align16(code_bytes);
+    L.rec_off = L.sm_off + align16(sm_stream_bytes(dtype, n));
+    L.size = L.rec_off + (variant == 2 ? 1u : 3u) * E;
+    return L;
+}
+
+uint64_t oracle_variant_size(uint64_t n, int dtype, uint32_t chunk, int variant, uint64_t total_escapes) {
+    return layout_variant(n, dtype, chunk, variant, total_escapes).size;
+}
+
+/* the first k entries distinct and in range, the rest zero */
+static int valid_variant_codebook(const uint8_t* cb16, int dtype, int variant) {
+    unsigned k = variant_codes(variant), bins = exponent_bins(dtype);
+    for (unsigned a = 0; a < 16; a++) {
+        if (a >= k) {
+            if (cb16[a] != 0) return 0;
+            continue;
+        }
+        if (cb16[a] >= bins) return 0;
+        for (unsigned b = a + 1; b < k; b++)
+            if (cb16[a] == cb16[b]) return 0;
+    }
+    return 1;
+}
+
+static int code_of_k(const uint8_t* cb16, unsigned k, unsigned e) {
+    for (unsigned c = 0; c < k; c++)
+        if (cb16[c] == e) return (int)c;
+    return -1;
+}
+
+/* Encode with one of the variants (V1-V3); variant 0 is the main format.  Same
+ * steps as oracle_encode: count the escapes per chunk, place the sections,
+ * then per element the code (or the escape), the sign|mantissa bits and the
+ * escape entry. */
+int oracle_encode_variant(const void* x, uint64_t n, int dtype, const uint8_t* cb16, uint32_t chunk, int variant,
+                          uint8_t* out, uint64_t capacity, uint64_t* out_size) {
+    if ((n && !x) || !cb16 || !out || !out_size || (dtype != OR_BF16 && dtype != OR_E5M2) ||
+        variant < 0 || variant > 2 || !valid_chunk(chunk) || !valid_variant_codebook(cb16, dtype, variant))
+        return OR_INVALID;
+    unsigned k = variant_codes(variant);
+    uint64_t C = (n + chunk - 1u) / chunk;
+    if (C > 0xFFFFFFFFull) return OR_INVALID;
+    uint32_t* counts = (uint32_t*)calloc(C ? C : 1, sizeof(uint32_t));
+    if (!counts) return OR_CAPACITY;
+    for (uint64_t i = 0; i < n; i++)
+        if (code_of_k(cb16, k, exponent_of(dtype, read_element(x, dtype, i))) < 0) counts[i / chunk]++;
+    uint64_t E = 0;
+    for (uint64_t c = 0; c < C; c++) E += counts[c];
+    layout_t L = layout_variant(n, dtype, chunk, variant, E);
+    if (L.size > capacity) {
+        free(counts);
+        return OR_CAPACITY;
+    }
+    memset(out, 0, L.size);
+    put_u32(out + 0, OR_MAGIC);
+    put_u16(out + 4, OR_VERSION);
+    out[6] = (uint8_t)dtype;
+    out[7] = (uint8_t)variant;
+    put_u64(out + 8, n);
+    put_u32(out + 16, chunk);
+    put_u32(out + 20, (uint32_t)C);
+    put_u64(out + 24, E);
+    for (int c = 0; c < 16; c++) out[32 + c] = cb16[c];
+    uint64_t running = 0;
+    for (uint64_t c = 0; c < C; c++) {
+        put_u64(out + L.index_off + 8u * c, running);
+        put_u32(out + L.counts_off + 4u * c, counts[c]);
+        running += counts[c];
+    }
+    uint64_t next_escape = 0;
+    for (uint64_t i = 0; i < n; i++) {
+        unsigned v = read_element(x, dtype, i);
+        unsigned e = exponent_of(dtype, v);
+        unsigned sm = sign_mantissa_of(dtype, v);
+        int code = code_of_k(cb16, k, e);
+        if (code < 0) {
+            if (variant == 2) {
+                out[L.rec_off + next_escape] = (uint8_t)e;  /* V3: the exponent only */
+                code = 15;
+            } else {
+                put_u16(out + L.rec_off + 3u * next_escape, (uint16_t)(i % chunk));
+                out[L.rec_off + 3u * next_escape + 2u] = (uint8_t)e;
+                code = 0;
+            }
+            next_escape++;
+        }
+        if (variant == 1) {
+            for (unsigned b = 0; b < 3; b++) {
+                if (((unsigned)code >> b) & 1u) {
+                    uint64_t bit = 3u * i + b;
+                    out[L.nib_off + bit / 8] |= (uint8_t)(1u << (bit % 8));
+                }
+            }
+        } else {
+            out[L.nib_off + i / 2] |= (uint8_t)((unsigned)code << (4u * (unsigned)(i % 2)));
+        }
+        if (dtype == OR_BF16) {
+            out[L.sm_off + i] = (uint8_t)sm;
+        } else {
+            for (unsigned b = 0; b < 3; b++) {
+                if ((sm >> b) & 1u) {
+                    uint64_t bit = 3u * i + b;
+                    out[L.sm_off + bit / 8] |= (uint8_t)(1u << (bit % 8));
+                }
+            }
+        }
+    }
+    free(counts);
+    *out_size = L.size;
+    return OR_OK;
+}
+
+/* Decode a container of any variant (byte 7).  Header and index checks as
+ * oracle_decode; dense path per element; then the correction: explicit records
+ * (variants 0, 1) as oracle_decode, or, for the sentinel variant, each element
+ * with code 15 takes the next exponent of its chunk's escape bytes, and the
+ * chunk must hold exactly as many sentinels as its count says. */
+int oracle_decode_variant(const uint8_t* blob, uint64_t bytes, void* out, uint64_t n, int dtype) {
+    if (!blob || (n && !out) || (dtype != OR_BF16 && dtype != OR_E5M2)) return OR_INVALID;
+    if (bytes < OR_HEADER_BYTES) return OR_CORRUPT;
+    if (get_u32(blob) != OR_MAGIC || get_u16(blob + 4) != OR_VERSION) return OR_CORRUPT;
+    if (blob[6] != (uint8_t)dtype || blob[7] > 2) return OR_CORRUPT;
+    for (int b = 48; b < 64; b++)
+        if (blob[b] != 0) return OR_CORRUPT;
+    int variant = blob[7];
+    uint64_t hn = get_u64(blob + 8), E = get_u64(blob + 24);
+    uint32_t chunk = get_u32(blob + 16), C = get_u32(blob + 20);
+    const uint8_t* cb = blob + 32;
+    if (hn != n || !valid_chunk(chunk) || (n + chunk - 1u) / chunk != C || E > n) return OR_CORRUPT;
+    if (!valid_variant_codebook(cb, dtype, variant)) return OR_CORRUPT;
+    layout_t L = layout_variant(n, dtype, chunk, variant, E);
+    if (L.size > bytes) return OR_CORRUPT;
+    uint64_t running = 0;
+    for (uint64_t c = 0; c < C; c++) {
+        uint64_t off = get_u64(blob + L.index_off + 8u * c);
+        uint64_t cnt = get_u32(blob + L.counts_off + 4u * c);
+        uint64_t len = (c + 1 < C) ? chunk : n - c * chunk;
+        if (off != running || cnt > len) return OR_CORRUPT;
+        running += cnt;
+    }
+    if (running != E) return OR_CORRUPT;
+
+    uint64_t sentinels = 0, chunk_start = 0;  /* variant 2: escapes of the current chunk so far */
+    for (uint64_t i = 0; i < n; i++) {
+        if (i % chunk == 0) {
+            if (i > 0 && variant == 2 && sentinels != get_u32(blob + L.counts_off + 4u * (i / chunk - 1)))
+                return OR_CORRUPT;
+            sentinels = 0;
+            chunk_start = get_u64(blob + L.index_off + 8u * (i / chunk));
+        }
+        unsigned code = 0;
+        if (variant == 1) {
+            for (unsigned b = 0; b < 3; b++) {
+                uint64_t bit = 3u * i + b;
+                code |= ((blob[L.nib_off + bit / 8] >> (bit % 8)) & 1u) << b;
+            }
+        } else {
+            code = (blob[L.nib_off + i / 2] >> (4u * (unsigned)(i % 2))) & 0xFu;
+        }
+        unsigned e;
+        if (variant == 2 && code == 15) {
+            uint64_t cnt = get_u32(blob + L.counts_off + 4u * (i / chunk));
+            if (sentinels >= cnt) return OR_CORRUPT;
+            e = blob[L.rec_off + chunk_start + sentinels];
+            if (e >= exponent_bins(dtype)) return OR_CORRUPT;
+            sentinels++;
+        } else {
+            e = cb[code];
+        }
+        unsigned sm;
+        if (dtype == OR_BF16) {
+            sm = blob[L.sm_off + i];
+        } else {
+            sm = 0;
+            for (unsigned b = 0; b < 3; b++) {
+                uint64_t bit = 3u * i + b;
+                sm |= ((blob[L.sm_off + bit / 8] >> (bit % 8)) & 1u) << b;
+            }
+        }
+        write_element(out, dtype, i, join_fields(dtype, sm, e));
+    }
+    if (variant == 2) {
+        if (n > 0 && sentinels != get_u32(blob + L.counts_off + 4u * (C - 1))) return OR_CORRUPT;
+        return OR_OK;
+    }
+    for (uint64_t c = 0; c < C; c++) {
+        uint64_t off = get_u64(blob + L.index_off + 8u * c);
+        uint64_t cnt = get_u32(blob + L.counts_off + 4u * c);
+        uint64_t len = (c + 1 < C) ? chunk : n - c * chunk;
+        for (uint64_t j = 0; j < cnt; j++) {
+            const uint8_t* rec = blob + L.rec_off + 3u * (off + j);
+            uint64_t pos = get_u16(rec);
+            unsigned e = rec[2];
+            if (pos >= len) return OR_CORRUPT;
+            if (j > 0 && pos <= get_u16(rec - 3)) return OR_CORRUPT;
+            if (e >= exponent_bins(dtype)) return OR_CORRUPT;
+            uint64_t i = c * chunk + pos;
+            unsigned v = read_element(out, dtype, i);
+            write_element(out, dtype, i, join_fields(dtype, sign_mantissa_of(dtype, v), e));
+        }
+    }
+    return OR_OK;
+}
