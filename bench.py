@@ -54,6 +54,7 @@ def parse_args():
     p.add_argument("--no-transfer", action="store_true", help="skip the GPU -> host -> GPU transfer leg")
     p.add_argument("--no-online", action="store_true", help="skip the online-calibration leg")
     p.add_argument("--no-paged", action="store_true", help="skip the paged-KV leg")
+    p.add_argument("--no-ablation", action="store_true", help="skip the Top-8 / Top-15 + sentinel leg")
     p.add_argument("--layers", type=int, default=32,
                    help="32-layer workloads: encode only L layers (a smaller case for profiling; "
                         "not a bench line)")
@@ -632,6 +633,51 @@ def run_ours(args, world, rank, local):
                  "vs_contiguous": {"encode": round(enc_ms / penc, 4), "decode": round(dec_ms / pdec, 4)},
                  "verified": p_ok}
 
+    # ---- ablation formats: Top-16 / Top-8 / Top-15 + sentinel through one
+    # plain kernel family (their differences are the formats'), next to the
+    # production Top-16 kernels ----
+    ablation = None
+    if not args.no_ablation:
+        ablation = {"kernels": "one plain kernel family for the three formats (no TMA ring); "
+                               "production Top-16 decode: %.4f ms" % dec_ms}
+        for variant, label in ((sz.ABL_TOP16, "top16"), (sz.ABL_TOP8, "top8"), (sz.ABL_TOP15_SENTINEL, "top15_sentinel")):
+            vcb = sz.ablation_codebook(cb, variant)
+            acap = sz.ablation_max_size(n, dtype, variant, CHUNK)
+
+            def abl_step(ev=None):
+                if ev is not None:
+                    ev[0].record(stream)
+                check(sz.splitzip_ablation_encode(xp, n, dtype, vcb, CHUNK, variant, op, acap, bufs.size.data_ptr(),
+                                                  bufs.status.data_ptr(), h), "ablation encode")
+                if ev is not None:
+                    ev[1].record(stream)
+                check(sz.splitzip_ablation_decode(op, acap, out.data_ptr(), n, dtype, variant, dstatus.data_ptr(),
+                                                  h), "ablation decode")
+                if ev is not None:
+                    ev[2].record(stream)
+
+            abl_step()
+            torch.cuda.synchronize()
+            aevs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(5)]
+            for ev in aevs:
+                if flush is not None:
+                    flush.fill_(3)
+                abl_step(ev)
+            torch.cuda.synchronize()
+            aenc = statistics.mean(e[0].elapsed_time(e[1]) for e in aevs)
+            adec = statistics.mean(e[1].elapsed_time(e[2]) for e in aevs)
+            asize = int(bufs.size[0])
+            aE = int(bufs.out[24:32].cpu().numpy().view(np.uint64)[0])
+            a_ok = int(bufs.status[0]) == sz.OK and int(dstatus[0]) == sz.OK and bool(torch.equal(out, x))
+            ablation[label] = {"encode_ms": round(aenc, 4), "decode_ms": round(adec, 4),
+                               "encode_gbs": round(raw_bytes / (aenc * 1e-3) / 1e9, 1),
+                               "decode_gbs": round(raw_bytes / (adec * 1e-3) / 1e9, 1),
+                               "escape_rate": round(aE / n, 6), "ratio": round(raw_bytes / asize, 5),
+                               "verified": a_ok}
+        for label in ("top8", "top15_sentinel"):
+            ablation[label]["decode_slowdown_vs_top16"] = round(ablation[label]["decode_ms"] /
+                                                                ablation["top16"]["decode_ms"], 3)
+
     # ---- CPU oracle on a bounded sample (rank 0 only) ----
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -655,7 +701,7 @@ def run_ours(args, world, rank, local):
         "escape_rate": round(E / n, 6), "verified_bit_exact": verified,
         "per_kernel": per_kernel, "link_model": link,
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clk,
-        "transfer": transfer, "online_calibration": online, "paged": paged,
+        "transfer": transfer, "online_calibration": online, "paged": paged, "ablation": ablation,
         "gpu_launches": 5 * K,  # timed steps: encode (streaming, group, index, records kernels) + decode
     }
 

@@ -245,6 +245,29 @@ int splitzip_decode_paged(const void* d_in, uint64_t in_bytes, void* d_pool, uin
                           const int32_t* d_pages, uint64_t n_pages, uint64_t page_elems, int dtype, int* d_status,
                           cudaStream_t stream);
 
+/* The page's ablation formats (section "Results", "Ablation Studies"):
+ * variant 1 = Top-8 (8 coded exponents, 3-bit codes packed LSB-first, 3 bytes
+ * per 8 elements; escapes as 3-byte (position, exponent) records), variant 2 =
+ * Top-15 + sentinel (15 coded exponents; code 15 marks an escape; the escape
+ * stream holds one exponent byte per escape, positions found from the
+ * sentinels), variant 0 = Top-16 (the main format, byte-identical to
+ * splitzip_encode's container).  Header, index and sign|mantissa stream as the
+ * main format; header byte 7 = the variant.  These entry points run one plain
+ * kernel family for all three (the production Top-16 kernels are
+ * splitzip_encode / splitzip_decode), so their measured speeds differ by the
+ * formats alone.  The codebook holds the variant's k = 16, 8 or 15 exponents
+ * (the first k of the Top-16 order), distinct and in range, then zeros.
+ * splitzip_ablation_max_size: the container size with every element
+ * escaping.  Encode: no workspace (the counts go to the container's index);
+ * three kernels.  Decode: the header, index and escapes are checked like
+ * splitzip_decode's; errors go to *d_status. */
+int splitzip_ablation_max_size(uint64_t n, int dtype, uint32_t chunk_elems, int variant, uint64_t* out_bytes);
+int splitzip_ablation_encode(const void* d_in, uint64_t n, int dtype, const splitzip_codebook_t* cb,
+                             uint32_t chunk_elems, int variant, void* d_out, uint64_t out_capacity,
+                             uint64_t* d_out_size, int* d_status, cudaStream_t stream);
+int splitzip_ablation_decode(const void* d_in, uint64_t in_bytes, void* d_out, uint64_t n, int dtype, int variant,
+                             int* d_status, cudaStream_t stream);
+
 /* Parse and check a container header held in host memory (bytes >= 64).
  * Returns SPLITZIP_ERR_CORRUPT for a malformed header or a size larger than
  * `bytes`. */

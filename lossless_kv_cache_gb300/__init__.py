@@ -105,6 +105,10 @@ SIGNATURES = {
     "splitzip_decode": (_int, [_vp, _u64, _vp, _u64, _int, _vp, _vp]),
     "splitzip_parse_header": (_int, [_vp, _u64, ctypes.POINTER(Header)]),
     "splitzip_calibrate_device": (_int, [_vp, _u64, _int, _vp, _vp, _vp]),
+    "splitzip_ablation_max_size": (_int, [_u64, _int, _u32, _int, _P_u64]),
+    "splitzip_ablation_encode": (_int, [_vp, _u64, _int, ctypes.POINTER(Codebook), _u32, _int, _vp, _u64, _vp, _vp,
+                                        _vp]),
+    "splitzip_ablation_decode": (_int, [_vp, _u64, _vp, _u64, _int, _int, _vp, _vp]),
     "splitzip_encode_paged": (_int, [_vp, _u64, _vp, _u64, _u64, _int, ctypes.POINTER(Codebook), _u32, _vp, _u64, _vp,
                                      _u64, _vp, _vp, _vp]),
     "splitzip_decode_paged": (_int, [_vp, _u64, _vp, _u64, _vp, _u64, _u64, _int, _vp, _vp]),
@@ -187,6 +191,20 @@ def splitzip_encode_paged(d_pool, pool_pages, d_pages, n_pages, page_elems, dtyp
 def splitzip_decode_paged(d_in, in_bytes, d_pool, pool_pages, d_pages, n_pages, page_elems, dtype, d_status, stream):
     return lib().splitzip_decode_paged(d_in, in_bytes, d_pool, pool_pages, d_pages, n_pages, page_elems, dtype,
                                        d_status, stream)
+
+
+def splitzip_ablation_max_size(n, dtype, chunk_elems, variant, out_bytes):
+    return lib().splitzip_ablation_max_size(n, dtype, chunk_elems, variant, ctypes.byref(out_bytes))
+
+
+def splitzip_ablation_encode(d_in, n, dtype, cb, chunk_elems, variant, d_out, out_capacity, d_out_size, d_status,
+                             stream):
+    return lib().splitzip_ablation_encode(d_in, n, dtype, ctypes.byref(cb), chunk_elems, variant, d_out,
+                                          out_capacity, d_out_size, d_status, stream)
+
+
+def splitzip_ablation_decode(d_in, in_bytes, d_out, n, dtype, variant, d_status, stream):
+    return lib().splitzip_ablation_decode(d_in, in_bytes, d_out, n, dtype, variant, d_status, stream)
 
 
 def splitzip_calibrate_device(d_x, n, dtype, d_hist256, d_cb, stream):
@@ -395,3 +413,47 @@ def decode_paged_into(blob, in_bytes, pool, pages, page_elems, dtype, status, st
     _check(splitzip_decode_paged(blob.data_ptr(), in_bytes, pool.data_ptr(), pool.numel() // page_elems,
                                  pages.data_ptr(), pages.numel(), page_elems, dtype, status.data_ptr(),
                                  _stream_handle(stream)), "splitzip_decode_paged")
+
+
+# ablation formats (see splitzip_ablation_encode): 0 = Top-16, 1 = Top-8, 2 = Top-15 + sentinel
+ABL_TOP16, ABL_TOP8, ABL_TOP15_SENTINEL = 0, 1, 2
+ABL_CODES = {ABL_TOP16: 16, ABL_TOP8: 8, ABL_TOP15_SENTINEL: 15}
+
+
+def ablation_codebook(cb16, variant):
+    """The variant's codebook: the first k exponents of a Top-16 codebook, then zeros."""
+    k = ABL_CODES[variant]
+    vals = list(cb16.values())[:k]
+    c = Codebook()
+    c.dtype = cb16.dtype
+    for i in range(16):
+        c.exps[i] = vals[i] if i < k else 0
+    return c
+
+
+def ablation_max_size(n, dtype, variant, chunk_elems=DEFAULT_CHUNK_ELEMS):
+    return _size_call(splitzip_ablation_max_size, n, dtype, chunk_elems, variant)
+
+
+def ablation_encode(x, cb, dtype, variant, chunk_elems=DEFAULT_CHUNK_ELEMS, stream=None):
+    """Encode device tensor x in an ablation format; returns the container
+    (uint8 device tensor of its exact size).  Synchronises."""
+    torch = _torch()
+    cap = ablation_max_size(x.numel(), dtype, variant, chunk_elems)
+    out = torch.empty(max(cap, 16), dtype=torch.uint8, device=x.device)
+    size = torch.zeros(2, dtype=torch.int64, device=x.device)
+    status = torch.zeros(4, dtype=torch.int32, device=x.device)
+    _check(splitzip_ablation_encode(x.data_ptr(), x.numel(), dtype, cb, chunk_elems, variant, out.data_ptr(), cap,
+                                    size.data_ptr(), status.data_ptr(), _stream_handle(stream)),
+           "splitzip_ablation_encode")
+    _check(int(status[0].item()), "splitzip_ablation_encode (device)")
+    return out[: int(size[0].item())]
+
+
+def ablation_decode_status(blob, n, dtype, variant, stream=None):
+    torch = _torch()
+    out = torch.empty(max(n, 1), dtype=_bits_dtype(dtype), device=blob.device)
+    status = torch.full((4,), -1, dtype=torch.int32, device=blob.device)
+    _check(splitzip_ablation_decode(blob.data_ptr(), blob.numel(), out.data_ptr() if n else 0, n, dtype, variant,
+                                    status.data_ptr(), _stream_handle(stream)), "splitzip_ablation_decode")
+    return int(status[0].item()), out[:n]

@@ -229,3 +229,24 @@ def test_paged_argument_errors(splitzip_lib):
     assert d(A, 1 << 20, A, 8, A, 4, 8, sz.BF16, A, 0) == sz.ERR_INVALID_ARG    # fewer than 16 elements
     assert d(A, 1 << 20, A, 8, None, 4, 4096, sz.BF16, A, 0) == sz.ERR_INVALID_ARG
     assert d(A, 1 << 20, A, 0, A, 4, 4096, sz.BF16, A, 0) == sz.ERR_INVALID_ARG
+
+
+def test_ablation_argument_errors(splitzip_lib):
+    A = 1 << 20  # fake device addresses: every call below fails before the GPU
+    out = ctypes.c_uint64(0)
+    assert sz.splitzip_ablation_max_size(100, sz.BF16, 64, 3, out) == sz.ERR_INVALID_ARG
+    assert sz.splitzip_ablation_max_size(100, sz.BF16, 96, 1, out) == sz.ERR_INVALID_ARG
+    assert sz.splitzip_ablation_max_size(100, sz.BF16, 64, 1, out) == sz.OK
+    # two chunks: 64 + 2 * 12 -> 96; 3 * 13 code bytes -> 48; 100 sign|mantissa bytes -> 112; 300 escape bytes
+    assert out.value == 96 + 48 + 112 + 300
+    cap = sz.ablation_max_size(1000, sz.BF16, 1, 64)
+    f = sz.splitzip_ablation_encode
+    good = sz.Codebook.make(sz.BF16, list(range(8)) + [0] * 8)
+    assert f(A, 1000, sz.BF16, good, 64, 1, A, cap - 1, A, A, 0) == sz.ERR_CAPACITY
+    tail = sz.Codebook.make(sz.BF16, list(range(8)) + [0] * 7 + [9])           # byte 15 must be zero
+    assert f(A, 1000, sz.BF16, tail, 64, 1, A, cap, A, A, 0) == sz.ERR_INVALID_ARG
+    dup = sz.Codebook.make(sz.BF16, [3, 3] + list(range(4, 10)) + [0] * 8)       # duplicate exponent
+    assert f(A, 1000, sz.BF16, dup, 64, 1, A, cap, A, A, 0) == sz.ERR_INVALID_ARG
+    assert f(A, 1000, sz.FP8_E5M2, good, 64, 1, A, cap, A, A, 0) == sz.ERR_INVALID_ARG  # other dtype
+    assert sz.splitzip_ablation_decode(A, 1 << 20, A, 10, sz.BF16, 5, A, 0) == sz.ERR_INVALID_ARG
+    assert sz.splitzip_ablation_decode(A, 63, A, 10, sz.BF16, 1, A, 0) == sz.ERR_CORRUPT
