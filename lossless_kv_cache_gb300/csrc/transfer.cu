@@ -10,9 +10,13 @@
 // decoded into the destination.  Four internal streams (encode, D2H, H2D,
 // decode) and per-slot events let the four stages of different pieces run at
 // the same time; kRing slots of device and host buffers are reused in turn.
-// The host learns each container's size from an 8-byte copy behind its
-// encode and enqueues that piece's copies while the next piece encodes, the
-// way a sender must know a message's length before posting it.
+// The host learns each container's size from a record that a one-thread
+// kernel behind its encode stores into the pinned staging memory (mapped into
+// the device's address space), and enqueues that piece's copies while the
+// next piece encodes, the way a sender must know a message's length before
+// posting it.  (A copy of the record would queue on the copy engine behind
+// the previous piece's link copy, so the size would arrive only after that
+// copy drained and the link would idle while the host enqueued the next.)
 #include <cstring>
 #include <vector>
 
@@ -35,6 +39,14 @@ struct PieceInfo {
     int dec_status;
 };
 static_assert(sizeof(PieceInfo) == 16, "16-byte piece records");
+
+// Piece record (size, encode status) -> pinned host memory, in stream order.
+__global__ void publish_info_kernel(const PieceInfo* src, PieceInfo* host_dst) {
+    volatile PieceInfo* d = host_dst;
+    d->size = src->size;
+    d->enc_status = src->enc_status;
+    __threadfence_system();
+}
 
 struct Plan {
     uint64_t pieces, piece_elems, cap;        // cap: one piece's container capacity
@@ -97,13 +109,18 @@ struct Streams {
     }
 };
 
-bool is_pinned_host(const void* p) {
+// Page-locked host memory; *mapped = its address in the device's address
+// space, or null if it has none.
+bool is_pinned_host(const void* p, void** mapped) {
     cudaPointerAttributes attr;
+    *mapped = nullptr;
     if (cudaPointerGetAttributes(&attr, p) != cudaSuccess) {
         cudaGetLastError();
         return false;
     }
-    return attr.type == cudaMemoryTypeHost;
+    if (attr.type != cudaMemoryTypeHost) return false;
+    *mapped = attr.devicePointer;
+    return true;
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -135,7 +152,8 @@ extern "C" int splitzip_transfer(const void* d_src, void* d_dst, uint64_t n, int
         return SPLITZIP_ERR_INVALID_ARG;
     if (compress && (!cb || !d_scratch || !aligned16(d_scratch))) return SPLITZIP_ERR_INVALID_ARG;
     if (d_scratch_bytes < p.device_bytes || h_stage_bytes < p.host_bytes) return SPLITZIP_ERR_CAPACITY;
-    if (!is_pinned_host(h_stage)) return SPLITZIP_ERR_INVALID_ARG;  // the link copies need page-locked memory
+    void* h_stage_mapped = nullptr;  // the link copies need page-locked memory
+    if (!is_pinned_host(h_stage, &h_stage_mapped)) return SPLITZIP_ERR_INVALID_ARG;
 
     Streams S;
     if (!S.ok) {
@@ -149,6 +167,11 @@ extern "C" int splitzip_transfer(const void* d_src, void* d_dst, uint64_t n, int
     uint8_t* host = static_cast<uint8_t*>(h_stage);
     PieceInfo* dinfo = compress ? reinterpret_cast<PieceInfo*>(dev + p.info_off) : nullptr;
     PieceInfo* hinfo = compress ? reinterpret_cast<PieceInfo*>(host + p.hinfo_off) : nullptr;
+    // the same records as the device sees them (null: copy them instead)
+    PieceInfo* hinfo_mapped =
+        compress && h_stage_mapped
+            ? reinterpret_cast<PieceInfo*>(static_cast<uint8_t*>(h_stage_mapped) + p.hinfo_off)
+            : nullptr;
     cudaStream_t s_enc = S.s[0], s_d2h = S.s[1], s_h2d = S.s[2], s_dec = S.s[3];
     bool cuda_ok = true;
     auto ok = [&](cudaError_t e) { cuda_ok &= e == cudaSuccess; };
@@ -209,7 +232,12 @@ extern "C" int splitzip_transfer(const void* d_src, void* d_dst, uint64_t n, int
                                  dev + p.send_off + k * p.cap, p.cap, dev + p.ws_off, p.ws_bytes, &dinfo[i].size,
                                  &dinfo[i].enc_status, s_enc);
             if (st != SPLITZIP_OK) break;
-            ok(cudaMemcpyAsync(&hinfo[i], &dinfo[i], 12, cudaMemcpyDeviceToHost, s_enc));  // size + status
+            if (hinfo_mapped) {
+                publish_info_kernel<<<1, 1, 0, s_enc>>>(&dinfo[i], &hinfo_mapped[i]);
+                ok(cudaGetLastError());
+            } else {
+                ok(cudaMemcpyAsync(&hinfo[i], &dinfo[i], 12, cudaMemcpyDeviceToHost, s_enc));  // size + status
+            }
             ok(cudaEventRecord(S.info[k], s_enc));
             if (!cuda_ok) st = SPLITZIP_ERR_CUDA;
             // piece i encodes while the host places piece i - 1 on the link
