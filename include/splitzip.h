@@ -274,11 +274,14 @@ int splitzip_ablation_decode(const void* d_in, uint64_t in_bytes, void* d_out, u
 int splitzip_parse_header(const void* h_blob, uint64_t bytes, splitzip_header_t* out);
 
 /* Scratch that splitzip_transfer needs: device bytes (with compress = 1: a
- * ring of 4 send and 4 receive containers of one piece's maximum size, one
- * encode workspace and 16 bytes per piece; 0 with compress = 0) and pinned
- * host bytes (a ring of 4 staging slots, plus 16 bytes per piece when
- * compressing).  SPLITZIP_ERR_INVALID_ARG unless n > 0 and piece_elems is a
- * positive multiple of chunk_elems. */
+ * ring of 4 send and 4 receive slots, each one piece's maximum container
+ * size, one encode workspace and 16 bytes per piece; 0 with compress = 0) and
+ * pinned host bytes (a ring of 4 staging slots, each a maximum container or,
+ * with compress = 0, a raw piece, plus 16 bytes per piece when compressing).
+ * Slots are rounded up to A = 2 MiB (64 KiB when a slot is under 2 MiB) and
+ * each area has A - 16 bytes more, so that a 16-byte-aligned base can be
+ * moved up to the next multiple of A.  SPLITZIP_ERR_INVALID_ARG unless n > 0
+ * and piece_elems is a positive multiple of chunk_elems. */
 int splitzip_transfer_scratch_size(uint64_t n, int dtype, uint32_t chunk_elems, uint64_t piece_elems,
                                    int compress, uint64_t* out_device_bytes, uint64_t* out_host_bytes);
 
@@ -291,8 +294,9 @@ int splitzip_transfer_scratch_size(uint64_t n, int dtype, uint32_t chunk_elems, 
  * back, and the received container is decoded into d_dst; compress = 0: the
  * raw piece is copied the same way (the baseline).  Encode, the two copies
  * and decode of different pieces overlap on four internal streams; the host
- * reads each container's size (8 bytes copied behind its encode) while the
- * next piece encodes.  The call starts after the work already on `stream`,
+ * reads each container's size, which a one-thread kernel behind its encode
+ * stores into h_stage through the device's mapping of it (a 12-byte copy
+ * where h_stage has no device mapping), while the next piece encodes.  The call starts after the work already on `stream`,
  * makes `stream` wait for its end, and blocks until d_dst is complete.
  * d_scratch / h_stage: at least splitzip_transfer_scratch_size's bytes,
  * 16-byte aligned, h_stage page-locked host memory (cudaHostAlloc or

@@ -10,6 +10,10 @@
 // decoded into the destination.  Four internal streams (encode, D2H, H2D,
 // decode) and per-slot events let the four stages of different pieces run at
 // the same time; kRing slots of device and host buffers are reused in turn.
+// Slots start on 2 MiB boundaries (64 KiB for slots under 2 MiB): with slots
+// at the 16-byte-aligned stride of a container's maximum size, the link copies
+// of every other slot ran ~30 % slower (BF16 cache, one-layer pieces: 23.2-27.5
+// ms per transfer against 20.6-21.4 ms with aligned slots).
 // The host learns each container's size from a record that a one-thread
 // kernel behind its encode stores into the pinned staging memory (mapped into
 // the device's address space), and enqueues that piece's copies while the
@@ -30,6 +34,13 @@ namespace {
 constexpr int kRing = 4;  // pieces in flight
 
 uint64_t a16(uint64_t x) { return (x + 15u) & ~uint64_t(15); }
+uint64_t align_up(uint64_t x, uint64_t a) { return (x + a - 1u) / a * a; }
+
+// Slot alignment for slots of `bytes`.
+uint64_t slot_align(uint64_t bytes) {
+    constexpr uint64_t kLarge = uint64_t(2) << 20, kSmall = uint64_t(64) << 10;
+    return bytes >= kLarge ? kLarge : kSmall;
+}
 
 // Per-piece record in device scratch and its copy in host staging: the
 // container size written by the encode, the encode and decode status words.
@@ -49,7 +60,8 @@ __global__ void publish_info_kernel(const PieceInfo* src, PieceInfo* host_dst) {
 }
 
 struct Plan {
-    uint64_t pieces, piece_elems, cap;        // cap: one piece's container capacity
+    uint64_t pieces, piece_elems, cap;        // cap: one slot (a piece's container capacity, aligned)
+    uint64_t align;                           // slot alignment; scratch bases are rounded up to it
     uint64_t ws_bytes;                        // one encode workspace
     uint64_t send_off, recv_off, ws_off, info_off, device_bytes;
     uint64_t stage_off, hinfo_off, host_bytes;
@@ -65,17 +77,20 @@ int plan_for(uint64_t n, int dtype, uint32_t chunk, uint64_t piece_elems, int co
     p->piece_elems = piece_elems;
     p->pieces = (n + piece_elems - 1) / piece_elems;
     // raw pieces cross the link as they are
-    p->cap = a16(compress ? cap : piece_elems * eb);
+    const uint64_t slot = compress ? cap : piece_elems * eb;
+    p->align = slot_align(slot);
+    p->cap = align_up(slot, p->align);
     p->ws_bytes = compress ? a16(ws) : 0;
     const uint64_t ring = std::min<uint64_t>(kRing, p->pieces);
     p->send_off = 0;
     p->recv_off = compress ? ring * p->cap : 0;
     p->ws_off = p->recv_off + (compress ? ring * p->cap : 0);
     p->info_off = p->ws_off + p->ws_bytes;
-    p->device_bytes = compress ? p->info_off + sizeof(PieceInfo) * p->pieces : 0;
+    // + room to round a 16-byte-aligned base up to the slot alignment
+    p->device_bytes = compress ? (p->align - 16u) + p->info_off + sizeof(PieceInfo) * p->pieces : 0;
     p->stage_off = 0;
     p->hinfo_off = ring * p->cap;
-    p->host_bytes = p->hinfo_off + (compress ? sizeof(PieceInfo) * p->pieces : 0);
+    p->host_bytes = (p->align - 16u) + p->hinfo_off + (compress ? sizeof(PieceInfo) * p->pieces : 0);
     return SPLITZIP_OK;
 }
 
@@ -163,14 +178,20 @@ extern "C" int splitzip_transfer(const void* d_src, void* d_dst, uint64_t n, int
     const uint64_t eb = dtype == SPLITZIP_BF16 ? 2u : 1u;
     const uint8_t* src = static_cast<const uint8_t*>(d_src);
     uint8_t* dst = static_cast<uint8_t*>(d_dst);
-    uint8_t* dev = static_cast<uint8_t*>(d_scratch);
-    uint8_t* host = static_cast<uint8_t*>(h_stage);
+    // both scratch areas start at the slot alignment
+    auto aligned_base = [&](void* b) {
+        const uintptr_t u = reinterpret_cast<uintptr_t>(b);
+        return reinterpret_cast<uint8_t*>(align_up(u, p.align));
+    };
+    uint8_t* dev = compress ? aligned_base(d_scratch) : nullptr;
+    uint8_t* host = aligned_base(h_stage);
+    const uint64_t host_pad = uint64_t(host - static_cast<uint8_t*>(h_stage));
     PieceInfo* dinfo = compress ? reinterpret_cast<PieceInfo*>(dev + p.info_off) : nullptr;
     PieceInfo* hinfo = compress ? reinterpret_cast<PieceInfo*>(host + p.hinfo_off) : nullptr;
     // the same records as the device sees them (null: copy them instead)
     PieceInfo* hinfo_mapped =
         compress && h_stage_mapped
-            ? reinterpret_cast<PieceInfo*>(static_cast<uint8_t*>(h_stage_mapped) + p.hinfo_off)
+            ? reinterpret_cast<PieceInfo*>(static_cast<uint8_t*>(h_stage_mapped) + host_pad + p.hinfo_off)
             : nullptr;
     cudaStream_t s_enc = S.s[0], s_d2h = S.s[1], s_h2d = S.s[2], s_dec = S.s[3];
     bool cuda_ok = true;

@@ -20,8 +20,11 @@ def _lib(splitzip_lib):
     return splitzip_lib
 
 
-def a16(x):
-    return (x + 15) // 16 * 16
+def slot_layout(x):
+    """(slot stride, alignment) of the transfer's staging ring: slots and the
+    area's base on 2 MiB boundaries, 64 KiB ones for slots under 2 MiB."""
+    a = 2 << 20 if x >= 2 << 20 else 64 << 10
+    return -(-x // a) * a, a
 
 
 def bits(dtype, n, seed):
@@ -59,9 +62,10 @@ def test_transfer_matches_oracle(dtype, chunk, piece):
         # the last piece's container is still in its staging slot
         lo, m = pieces[-1]
         ref = oracle.encode(host[lo:lo + m], dtype, exps, chunk)
-        slot = (len(pieces) - 1) % 4
-        cap = a16(sz.max_compressed_size(piece, dtype, chunk))
-        got = bufs.host[slot * cap: slot * cap + ref.size].numpy()
+        k = (len(pieces) - 1) % 4
+        cap, a = slot_layout(sz.max_compressed_size(piece, dtype, chunk))
+        base = -bufs.host.data_ptr() % a  # the ring starts at the next multiple of a
+        got = bufs.host[base + k * cap: base + k * cap + ref.size].numpy()
         assert np.array_equal(got, ref)
 
 

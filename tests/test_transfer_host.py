@@ -11,20 +11,31 @@ def a16(x):
     return (x + 15) // 16 * 16
 
 
+def slot(x):
+    """(slot stride, alignment): 2 MiB slots from 2 MiB on, 64 KiB below."""
+    a = 2 << 20 if x >= 2 << 20 else 64 << 10
+    return -(-x // a) * a, a
+
+
 def test_transfer_scratch_sizes(splitzip_lib):
     for dtype, eb in ((sz.BF16, 2), (sz.FP8_E5M2, 1)):
-        for n, piece in ((10 * 65536 + 5, 65536), (3 * 65536, 2 * 65536), (65536, 65536), (1, 4096)):
+        for n, piece in ((10 * 65536 + 5, 65536), (3 * 65536, 2 * 65536), (65536, 65536), (1, 4096),
+                         (3 << 20, 1 << 20), (5 << 21, 1 << 21)):
             chunk = 65536 if piece % 65536 == 0 else 4096
             pieces = -(-n // piece)
             ring = min(4, pieces)
-            cap = a16(sz.max_compressed_size(piece, dtype, chunk))
+            cap, a = slot(sz.max_compressed_size(piece, dtype, chunk))
             ws = a16(sz.workspace_size(piece, dtype, chunk))
             d, h = sz.transfer_scratch_size(n, dtype, piece, True, chunk)
-            assert d == 2 * ring * cap + ws + 16 * pieces
-            assert h == ring * cap + 16 * pieces
+            assert d == (a - 16) + 2 * ring * cap + ws + 16 * pieces
+            assert h == (a - 16) + ring * cap + 16 * pieces
             d, h = sz.transfer_scratch_size(n, dtype, piece, False, chunk)
+            raw, a = slot(piece * eb)
             assert d == 0
-            assert h == ring * a16(piece * eb)
+            assert h == (a - 16) + ring * raw
+    # both alignments occur above
+    assert slot(sz.max_compressed_size(1 << 20, sz.FP8_E5M2, 65536))[1] == 2 << 20
+    assert slot(sz.max_compressed_size(65536, sz.BF16, 65536))[1] == 64 << 10
 
 
 def test_transfer_argument_errors(splitzip_lib):
