@@ -6,7 +6,6 @@ baseline leg of ``bench.py`` may use it; the product package never does.
 Arrays are numpy arrays of raw bits: BF16 as ``uint16``, FP8-E5M2 as ``uint8``.
 """
 import ctypes
-import os
 
 import numpy as np
 

@@ -83,3 +83,14 @@ def test_cpu_baseline_helper_on_host_bits():
     gbs, done, secs, distinct, block = bench.oracle_throughput(x, 0, cb, 0.01, 4)
     assert block == 2 * bench.CHUNK and distinct == x.numel() and done % distinct == 0
     assert gbs > 0 and secs > 0
+
+
+def test_reference_arm_runs_on_rank_0_only():
+    import sys
+    old = sys.argv
+    sys.argv = ["bench.py", "--impl", "reference", "--workload", "escape_stress_64x65536_bf16"]
+    try:
+        args = bench.parse_args()
+    finally:
+        sys.argv = old
+    assert bench.run_reference(args, 2, 1) is None  # rank 1 of 2: no work, no line
