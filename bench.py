@@ -9,8 +9,11 @@ the headline line).
 Prints one JSON line.  `value` is the round-trip throughput in GB/s of
 uncompressed bytes (bytes of the tensor / (encode + decode time)); encode and
 decode throughputs, the compression ratio, the escape rate and the derived
-link-transfer model are reported beside it.  `--impl reference` times the CPU
-oracle on a bounded sample of the same workload instead.
+link-transfer model are reported beside it, with the end-to-end figure from
+pinned host memory, the transfer path, online calibration, paged KV and the
+ablation formats.  `cpu_baseline` and `--impl reference` time the CPU oracle
+as it stands on a bounded sample of the same workload, in independent
+containers on every host core (the single-thread figure beside it).
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                        [--workload NAME] [--layers L]
