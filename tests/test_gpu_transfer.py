@@ -3,6 +3,8 @@ streams) against the oracle.  The destination must equal the source bit for
 bit, the bytes that crossed the link must be the oracle's container sizes of
 the pieces, and the last container left in the host staging area must be the
 oracle's container of the last piece, byte for byte."""
+import ctypes
+
 import numpy as np
 import pytest
 import torch
@@ -79,3 +81,31 @@ def test_transfer_rejects_pageable_host_memory():
     st = sz.splitzip_transfer(x.data_ptr(), x.data_ptr(), n, sz.BF16, cb, 65536, piece, 1, dev.data_ptr(), d,
                               pageable.data_ptr() + (-pageable.data_ptr()) % 16, h, None, None, 0)
     assert st == sz.ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("compress", [True, False])
+def test_transfer_with_bases_off_the_slot_alignment(compress):
+    # 16-byte-aligned bases 16 bytes past an allocation (so off the slot
+    # alignment, the worst case for the call's rounding up) and exactly the
+    # scratch sizes reported: the output is exact and not a byte outside the
+    # areas passed in is written
+    n, piece = 5 * 65536 + 7, 65536
+    host, x = bits(sz.BF16, n, 11)
+    exps = oracle.calibrate(oracle.histogram(host, sz.BF16), sz.BF16)
+    cb = sz.Codebook.make(sz.BF16, [int(e) for e in exps])
+    d, h = sz.transfer_scratch_size(n, sz.BF16, piece, compress)
+    pad = 16
+    dev = torch.full((d + 2 * pad + 16,), 0xA7, dtype=torch.uint8, device="cuda")
+    hst = torch.full((h + 2 * pad + 16,), 0x5C, dtype=torch.uint8).pin_memory()
+    assert dev.data_ptr() % 16 == 0 and hst.data_ptr() % 16 == 0
+    y = torch.zeros_like(x)
+    link, ms = ctypes.c_uint64(0), ctypes.c_float(0.0)
+    st = sz.splitzip_transfer(x.data_ptr(), y.data_ptr(), n, sz.BF16, cb if compress else None, 65536, piece,
+                              int(compress), dev.data_ptr() + pad if compress else 0, d if compress else 0,
+                              hst.data_ptr() + pad, h, link, ms, torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    assert st == sz.OK
+    assert torch.equal(y, x)
+    dv, hv = dev.cpu(), hst
+    assert bool((dv[:pad] == 0xA7).all()) and bool((dv[pad + d:] == 0xA7).all())
+    assert bool((hv[:pad] == 0x5C).all()) and bool((hv[pad + h:] == 0x5C).all())
