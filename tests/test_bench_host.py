@@ -94,3 +94,14 @@ def test_reference_arm_runs_on_rank_0_only():
     finally:
         sys.argv = old
     assert bench.run_reference(args, 2, 1) is None  # rank 1 of 2: no work, no line
+
+
+def test_traffic_table_agrees_with_its_profiles():
+    # the per-operation DRAM traffic that each launch-list profile prints (MB,
+    # one decimal) is the figure the bench line reports
+    for (workload, op), t in bench.TRAFFIC.items():
+        with open(os.path.join(bench.ROOT, t["profile"])) as f:
+            rows = [line.split("|") for line in f if line.startswith("| %s" % op)]
+        assert len(rows) == 1, (workload, op)
+        printed = float(rows[0][3].strip().split()[0].replace(",", ""))
+        assert printed == round(t["bytes"] / 1e6, 1), (workload, op, printed, t["bytes"])
