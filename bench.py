@@ -60,6 +60,9 @@ def parse_args():
     p.add_argument("--no-online", action="store_true", help="skip the online-calibration leg")
     p.add_argument("--no-paged", action="store_true", help="skip the paged-KV leg")
     p.add_argument("--no-ablation", action="store_true", help="skip the Top-8 / Top-15 + sentinel leg")
+    p.add_argument("--no-workloads", action="store_true",
+                   help="skip the per-workload object (the other four workloads, timed after the headline)")
+    p.add_argument("--workload-steps", type=int, default=20, help="timed steps per workload of that object")
     p.add_argument("--layers", type=int, default=32,
                    help="32-layer workloads: encode only L layers (a smaller case for profiling; "
                         "not a bench line)")
@@ -259,6 +262,75 @@ class Workload:
         streams = (n + 1) // 2 + (n if self.dtype == 0 else 3 * (-(-n // 8)))
         moved = n * self.elem_bytes + streams + 3 * E + 12 * C
         return moved, moved
+
+
+# ---------------------------------------------------- other workloads
+
+def measure_workload(name, steps, warmup, device, hbm):
+    """Encode + decode of one workload (seed 0, codebook from its calibration
+    tensor), timed like the headline: CUDA events around each call on the
+    launching stream, W untimed warm-up steps, a 512 MB L2 flush before every
+    step when the input fits in L2; the round trip is checked bit for bit."""
+    import lossless_kv_cache_gb300 as sz
+    wl = Workload(name)
+    n, dtype = wl.n, wl.dtype
+    raw = wl.elem_bytes * n
+    x = wl.make(0, device)
+    cb, _ = sz.calibrate(wl.calibration(device), dtype)
+    bufs = sz.EncodeBuffers(n, dtype, CHUNK, device=device)
+    out = torch.empty(n, dtype=x.dtype, device=device)
+    dstatus = torch.zeros(4, dtype=torch.int32, device=device)
+    stream = torch.cuda.current_stream()
+    h = stream.cuda_stream
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=device) if raw <= L2_BYTES else None
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        st = sz.splitzip_encode(x.data_ptr(), n, dtype, cb, CHUNK, bufs.out.data_ptr(), bufs.capacity,
+                                bufs.ws.data_ptr(), bufs.ws_bytes, bufs.size.data_ptr(), bufs.status.data_ptr(), h)
+        if st != sz.OK:
+            raise sz.SplitZipError(st, "encode")
+        if ev is not None:
+            ev[1].record(stream)
+        st = sz.splitzip_decode(bufs.out.data_ptr(), bufs.capacity, out.data_ptr(), n, dtype, dstatus.data_ptr(), h)
+        if st != sz.OK:
+            raise sz.SplitZipError(st, "decode")
+        if ev is not None:
+            ev[2].record(stream)
+
+    for _ in range(max(warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    out.fill_(0)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    for ev in evs:
+        if flush is not None:
+            flush.fill_(7)
+        step(ev)
+    torch.cuda.synchronize()
+    ok = int(bufs.status[0]) == sz.OK and int(dstatus[0]) == sz.OK and bool(torch.equal(out, x))
+    enc = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
+    dec = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
+    size = int(bufs.size[0])
+    E = int(bufs.out[24:32].cpu().numpy().view(np.uint64)[0])
+    alg, _ = wl.algorithmic_bytes(E)
+    link = {}
+    for L in LINKS_GBS:
+        t_plain = raw / (L * 1e9)
+        link["%d_GBps" % int(L)] = round(t_plain / ((enc + dec) * 1e-3 + size / (L * 1e9)), 4)
+    res = {"elements": n, "element_dtype": "bf16" if dtype == 0 else "fp8_e5m2", "steps": steps,
+           "encode_ms": round(enc, 5), "decode_ms": round(dec, 5),
+           "encode_gbs": round(raw / (enc * 1e-3) / 1e9, 2), "decode_gbs": round(raw / (dec * 1e-3) / 1e9, 2),
+           "round_trip_gbs": round(raw / ((enc + dec) * 1e-3) / 1e9, 2),
+           "encode_hbm_frac": round(alg / (enc * 1e-3) / 1e9 / hbm, 4),
+           "decode_hbm_frac": round(alg / (dec * 1e-3) / 1e9 / hbm, 4),
+           "ratio": round(raw / size, 5), "escape_rate": round(E / n, 6),
+           "link_model_speedup": link, "verified": ok,
+           "l2": "flushed (512 MB write) before every step" if flush is not None else "inputs larger than L2"}
+    del x, bufs, out, flush
+    torch.cuda.empty_cache()
+    return res
 
 
 # --------------------------------------------------------- CPU oracle
@@ -739,6 +811,17 @@ def run_ours(args, world, rank, local):
                                  "sample": "%d elements in %.1f s: passes over the first %d elements, %s" % (
                                      elems1, secs1, distinct1, what % block1)}}
 
+    # ---- the other workloads (one line carries all five), timed after the
+    # headline's buffers are released ----
+    workloads = None
+    if not args.no_workloads and wl.name == DEFAULT_WORKLOAD and wl.layers == 32:
+        del x, out, bufs
+        torch.cuda.empty_cache()
+        workloads = {}
+        for other in ("kv_tile_1x1024x8x128_bf16", "llama_layer_2x8192x8x128_bf16",
+                      "escape_stress_64x65536_bf16", "kv_cache_32x2x65536x8x128_e5m2"):
+            workloads[other] = measure_workload(other, args.workload_steps, args.warmup, device, hbm)
+
     if rank != 0:
         return None
     return {
@@ -755,6 +838,7 @@ def run_ours(args, world, rank, local):
         "per_kernel": per_kernel, "link_model": link,
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clk,
         "transfer": transfer, "online_calibration": online, "paged": paged, "ablation": ablation,
+        "workloads": workloads,
         "gpu_launches": 5 * K,  # timed steps: encode (streaming, group, index, records kernels) + decode
     }
 

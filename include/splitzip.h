@@ -119,9 +119,12 @@ int splitzip_exponent_histogram(const void* d_x, uint64_t n, int dtype, uint64_t
  * coding": the 16 most frequent exponents get the 4-bit codes).  Ties go to
  * the smaller exponent; unseen exponents fill the remaining codes in
  * ascending order; code 0 is the most frequent exponent.
- * hist256: host array, or device array when hist_is_device != 0 (then the
- * call copies it to the host and synchronises the current device's default
- * stream).  FP8-E5M2 histograms with counts in bins >= 32 are rejected. */
+ * hist256: host array, or device array on the current device when
+ * hist_is_device != 0: the call then blocks in cudaDeviceSynchronize() until
+ * all work queued on every stream of the device has finished (so a histogram
+ * that splitzip_exponent_histogram enqueued on any stream, non-blocking
+ * streams included, is complete) and copies the 256 counts to the host.
+ * FP8-E5M2 histograms with counts in bins >= 32 are rejected. */
 int splitzip_calibrate(const uint64_t* hist256, int hist_is_device, int dtype,
                        splitzip_codebook_t* out_cb);
 
@@ -196,9 +199,11 @@ int splitzip_encode_device_codebook(const void* d_in, uint64_t n, int dtype, con
  * default chunk size, for either dtype); larger n returns SPLITZIP_ERR_CAPACITY before any GPU
  * work.  The call allocates nothing: the caller still passes input, output,
  * d_out_size and d_status exactly as for splitzip_encode, and the output is
- * byte-identical to splitzip_encode's.  The first call on each device looks up
- * the array's device address (cudaGetSymbolAddress) with that device current;
- * make that first call before any stream capture.  Every call on a device
+ * byte-identical to splitzip_encode's.  Every call looks up the array's
+ * device address on the current device (cudaGetSymbolAddress), so an address
+ * from before a device reset is never reused; the first call on a device also
+ * loads the library's device code there, so make that first call before any
+ * stream capture.  Every call on a device
  * shares the array, so calls whose GPU work overlaps (other streams or host
  * threads) race and must be serialised by the caller.  The encode writes
  * every word of its workspace before reading it, so whatever an earlier call
@@ -308,6 +313,22 @@ int splitzip_transfer(const void* d_src, void* d_dst, uint64_t n, int dtype, con
                       uint32_t chunk_elems, uint64_t piece_elems, int compress, void* d_scratch,
                       uint64_t d_scratch_bytes, void* h_stage, uint64_t h_stage_bytes, uint64_t* out_link_bytes,
                       float* out_ms, cudaStream_t stream);
+
+/* Self-test of the bounded device wait.  Every wait of the encode and
+ * decode kernels on a bulk-copy barrier gives up after a bounded number of SM
+ * cycles (about one second), records SPLITZIP_ERR_TIMEOUT in the status word
+ * and lets the kernel finish, so that a failed copy cannot hang the GPU; in a
+ * healthy run that path never executes.  This call runs it on purpose with no
+ * copy in flight: one warp waits, limit_cycles SM cycles at most, on an
+ * mbarrier that nothing arrives on, then reports exactly as the streaming
+ * kernels do.  The page has no counterpart (the codec never waits on data).
+ * limit_cycles: 1 .. 2e9.  d_status: device int, cleared by the call, then
+ * SPLITZIP_ERR_TIMEOUT (the expected outcome; a control wait on a completed
+ * barrier must also succeed, else the status is the same and d_cycles[1] is
+ * -1).  d_cycles (optional, device, 2 x int64): cycles the giving-up wait
+ * took, and cycles the control wait took. */
+int splitzip_selftest_bounded_wait(uint64_t limit_cycles, int* d_status, long long* d_cycles,
+                                   cudaStream_t stream);
 
 #ifdef __cplusplus
 }

@@ -116,6 +116,7 @@ SIGNATURES = {
     "splitzip_transfer_scratch_size": (_int, [_u64, _int, _u32, _u64, _int, _P_u64, _P_u64]),
     "splitzip_transfer": (_int, [_vp, _vp, _u64, _int, ctypes.POINTER(Codebook), _u32, _u64, _int, _vp, _u64, _vp,
                                  _u64, _P_u64, ctypes.POINTER(ctypes.c_float), _vp]),
+    "splitzip_selftest_bounded_wait": (_int, [_u64, _vp, _vp, _vp]),
 }
 
 _lib = None
@@ -229,6 +230,10 @@ def splitzip_transfer(d_src, d_dst, n, dtype, cb, chunk_elems, piece_elems, comp
                                    piece_elems, compress, d_scratch, d_scratch_bytes, h_stage, h_stage_bytes,
                                    None if out_link_bytes is None else ctypes.byref(out_link_bytes),
                                    None if out_ms is None else ctypes.byref(out_ms), stream)
+
+
+def splitzip_selftest_bounded_wait(limit_cycles, d_status, d_cycles, stream):
+    return lib().splitzip_selftest_bounded_wait(limit_cycles, d_status, d_cycles, stream)
 
 
 # ------------------------------------------------------------ size helpers

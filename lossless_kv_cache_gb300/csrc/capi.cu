@@ -225,7 +225,12 @@ int splitzip_calibrate(const uint64_t* hist256, int hist_is_device, int dtype, s
     if (!hist256 || !out_cb || !valid_dtype(dtype)) return SPLITZIP_ERR_INVALID_ARG;
     uint64_t h[256];
     if (hist_is_device) {
-        if (cudaMemcpy(h, hist256, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess) {
+        // A histogram enqueued on any stream of the device (non-blocking
+        // streams and per-thread default streams included) is complete after a
+        // device-wide synchronisation; a plain cudaMemcpy would order only
+        // against the legacy default stream.
+        if (cudaDeviceSynchronize() != cudaSuccess ||
+            cudaMemcpy(h, hist256, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess) {
             cudaGetLastError();
             return SPLITZIP_ERR_CUDA;
         }

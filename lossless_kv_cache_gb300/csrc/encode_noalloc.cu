@@ -14,38 +14,26 @@
 // or several host threads) race on it and must be serialised by the caller.
 // splitzip_encode writes every word of its workspace before reading it, so
 // the contents left by an earlier call do no harm.
-#include <mutex>
-
 #include "splitzip_internal.cuh"
 
 namespace {
 
 static __device__ __align__(256) uint8_t g_noalloc_scratch[SPLITZIP_NOALLOC_SCRATCH_BYTES];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_scratch_mutex;
-void* g_scratch_address[kMaxDevices];
-
 // Device address of the scratch array on the current device.  In host code
 // the symbol g_noalloc_scratch is only a host-side stand-in, so the address is
-// asked from the runtime once per device, with that device current.
+// asked from the runtime, with the device current, on every call: once the
+// module is loaded this is a table lookup, and an address taken before a
+// device reset (after which the module can load at another address) is never
+// reused.  The first call on a device loads the module, so it should come
+// before any stream capture.
 int scratch_address(void** out) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) {
         cudaGetLastError();
         return SPLITZIP_ERR_CUDA;
     }
-    if (dev < 0 || dev >= kMaxDevices) return SPLITZIP_ERR_UNSUPPORTED;
-    std::lock_guard<std::mutex> lock(g_scratch_mutex);
-    if (g_scratch_address[dev] == nullptr) {
-        void* p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) {
-            cudaGetLastError();
-            return SPLITZIP_ERR_CUDA;
-        }
-        g_scratch_address[dev] = p;
-    }
-    *out = g_scratch_address[dev];
+    *out = p;
     return SPLITZIP_OK;
 }
 

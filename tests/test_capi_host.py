@@ -250,3 +250,13 @@ def test_ablation_argument_errors(splitzip_lib):
     assert f(A, 1000, sz.FP8_E5M2, good, 64, 1, A, cap, A, A, 0) == sz.ERR_INVALID_ARG  # other dtype
     assert sz.splitzip_ablation_decode(A, 1 << 20, A, 10, sz.BF16, 5, A, 0) == sz.ERR_INVALID_ARG
     assert sz.splitzip_ablation_decode(A, 63, A, 10, sz.BF16, 1, A, 0) == sz.ERR_CORRUPT
+
+
+def test_selftest_argument_errors(splitzip_lib):
+    # the bounded-wait self-test checks its arguments before any CUDA call
+    A = 1 << 20  # never dereferenced: the checks come first
+    assert sz.splitzip_selftest_bounded_wait(0, A, None, 0) == sz.ERR_INVALID_ARG
+    assert sz.splitzip_selftest_bounded_wait(3_000_000_000, A, None, 0) == sz.ERR_INVALID_ARG
+    assert sz.splitzip_selftest_bounded_wait(100, None, None, 0) == sz.ERR_INVALID_ARG
+    assert sz.splitzip_selftest_bounded_wait(100, A + 2, None, 0) == sz.ERR_INVALID_ARG
+    assert sz.splitzip_selftest_bounded_wait(100, A, A + 4, 0) == sz.ERR_INVALID_ARG

@@ -75,3 +75,32 @@ def test_bad_device_codebook_is_reported(dtype, bad):
     sz.encode_into_device_codebook(x, dcb, bufs)
     torch.cuda.synchronize()
     assert int(bufs.status[0]) == sz.ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("dtype", [sz.BF16, sz.FP8_E5M2])
+def test_calibrate_reads_device_histogram_from_a_nonblocking_stream(dtype):
+    """splitzip_exponent_histogram on a torch side stream (non-blocking), kept
+    busy first so the histogram is still pending when the host returns, then
+    splitzip_calibrate(d_hist, hist_is_device=1) straight away with no host
+    synchronisation in between: the call must wait for the histogram."""
+    x = W.escape_stress(7, chunks=16) if dtype == sz.BF16 else W.kv_cache_layer_e5m2(6, 2, tokens=2048)
+    ref = oracle.calibrate(oracle.histogram(host_bits(x, dtype), dtype), dtype)
+    xd = x.to("cuda")
+    hist = torch.empty(256, dtype=torch.int64, device="cuda")
+    # a stale histogram whose codebook differs from the true one
+    stale = np.zeros(256, dtype=np.int64)
+    stale[:32] = np.arange(32, 0, -1) * 1000
+    hist.copy_(torch.from_numpy(stale))
+    torch.cuda.synchronize()
+    side = torch.cuda.Stream()
+    busy = torch.empty(1 << 28, dtype=torch.uint8, device="cuda")
+    with torch.cuda.stream(side):
+        for i in range(40):  # ~10 GB of writes queued ahead of the histogram
+            busy.fill_(i)
+        assert sz.splitzip_exponent_histogram(xd.data_ptr(), xd.numel(), dtype, hist.data_ptr(),
+                                              side.cuda_stream) == sz.OK
+    cb = sz.Codebook()
+    assert sz.splitzip_calibrate(hist.data_ptr(), 1, dtype, cb) == sz.OK
+    np.testing.assert_array_equal(np.array(cb.values(), np.uint8), ref)
+    assert cb.dtype == dtype
+    side.synchronize()

@@ -2,12 +2,14 @@
 
 Integer/bit work, so the bar is byte equality of the container and bit
 equality of the decoded tensor (tolerance 0).  Small and medium workloads are
-compared whole; the two 4.3 GB workloads are compared on sampled chunks (the
-oracle encodes each sampled chunk on its own; a chunk's sections do not depend
-on other chunks) plus properties that hold at any size: the index is the
-prefix of the counts, E equals the exponent mass outside the codebook
-(counted by torch.bincount, not by this library), the size formula, and
-decode(encode(x)) == x.
+compared whole; the two 4.3 GB workloads are compared chunk by chunk, every
+chunk (the oracle encodes blocks of whole chunks on host threads; a chunk's
+sections do not depend on other chunks), with the header and padding bytes
+checked against the layout formula, plus properties that hold at any size:
+the index is the prefix of the counts, E equals the exponent mass outside the
+codebook (counted by torch.bincount, not by this library), the size formula,
+and decode(encode(x)) == x; an oracle-built container of one whole layer is
+decoded on the GPU.
 """
 import numpy as np
 import pytest
@@ -247,7 +249,7 @@ def test_chunk_aligned_shards_match_single_container():
     np.testing.assert_array_equal(rw[3 * E0:], parts[1][hp[1].escrec_off: hp[1].size])
 
 
-# ------------------------------------------- the 4.3 GB workloads, sampled
+# ------------------------------------------- the 4.3 GB workloads, whole
 
 def _layout(n, dtype, chunk, E):
     C = -(-n // chunk)
@@ -255,10 +257,59 @@ def _layout(n, dtype, chunk, E):
     sm = nib + a16((n + 1) // 2)
     sm_bytes = n if dtype == 0 else 3 * (-(-n // 8))
     rec = sm + a16(sm_bytes)
-    return dict(C=C, index=64, counts=64 + 8 * C, nib=nib, sm=sm, rec=rec, size=rec + 3 * E)
+    return dict(C=C, index=64, counts=64 + 8 * C, index_end=64 + 12 * C, nib=nib, sm=sm, sm_bytes=sm_bytes,
+                rec=rec, size=rec + 3 * E)
 
 
-def _full_size_check(name, sample_chunks=12):
+def _expected_header(n, dtype, chunk, C, E, cb):
+    h = np.zeros(64, np.uint8)
+    h[0:4] = np.frombuffer(np.uint32(0x50495A53).tobytes(), np.uint8)
+    h[4:6] = (1, 0)
+    h[6] = dtype
+    h[8:16] = np.frombuffer(np.uint64(n).tobytes(), np.uint8)
+    h[16:20] = np.frombuffer(np.uint32(chunk).tobytes(), np.uint8)
+    h[20:24] = np.frombuffer(np.uint32(C).tobytes(), np.uint8)
+    h[24:32] = np.frombuffer(np.uint64(E).tobytes(), np.uint8)
+    h[32:48] = cb
+    return h
+
+
+def _compare_all_chunks(hb, xh, dtype, cb, chunk, L, off, cnt, block_chunks=16):
+    """Every chunk of the GPU container against the oracle: the tensor is cut
+    into blocks of whole chunks, each block encoded by the oracle into its own
+    container on a host thread (a chunk's sections do not depend on other
+    chunks), and the block's nibble, sign|mantissa, count and record bytes
+    compared with the matching slices of the GPU container."""
+    from concurrent.futures import ThreadPoolExecutor
+    n = xh.size
+    C = L["C"]
+
+    def one(c0):
+        c1 = min(C, c0 + block_chunks)
+        lo, hi = c0 * chunk, min(n, c1 * chunk)
+        ref = oracle.encode(xh[lo:hi], dtype, cb, chunk)
+        R = _layout(hi - lo, dtype, chunk, (ref.size - _layout(hi - lo, dtype, chunk, 0)["size"]) // 3)
+        checks = [
+            ("nibbles", hb[L["nib"] + lo // 2: L["nib"] + (hi + 1) // 2], ref[R["nib"]: R["nib"] + (hi - lo + 1) // 2]),
+            ("sign|mantissa", hb[L["sm"] + (lo if dtype == 0 else lo // 8 * 3): L["sm"] + (hi if dtype == 0 else 3 * (-(-hi // 8)))],
+             ref[R["sm"]: R["sm"] + R["sm_bytes"]]),
+            ("counts", hb[L["counts"] + 4 * c0: L["counts"] + 4 * c1], ref[R["counts"]: R["index_end"]]),
+            ("records", hb[L["rec"] + 3 * int(off[c0]): L["rec"] + 3 * (int(off[c0]) + int(cnt[c0:c1].sum()))],
+             ref[R["rec"]: R["size"]]),
+        ]
+        for what, got, want in checks:
+            if got.size != want.size or not np.array_equal(got, want):
+                return "chunks %d..%d: %s differ" % (c0, c1 - 1, what)
+        return None
+
+    import os
+    with ThreadPoolExecutor(max(1, os.cpu_count() or 1)) as pool:
+        bad = [r for r in pool.map(one, range(0, C, block_chunks)) if r]
+    assert not bad, bad[:5]
+    return C
+
+
+def _full_size_check(name):
     dtype = W.dtype_of(name)
     n_layers, _ = W.layers_of(name)
     x = W.make_layers(name, 0, n_layers, DEV)
@@ -266,19 +317,22 @@ def _full_size_check(name, sample_chunks=12):
     assert n == W.numel(name)
     cal = W.calibration_tensor(name, DEV)
     cb, hist = sz.calibrate(cal, dtype)
-    # calibration on a sample of the calibration layer against the oracle
+    # calibration on the calibration layer against the oracle
     ref_cb = oracle.calibrate(oracle.histogram(np_bits(cal, dtype), dtype), dtype)
     np.testing.assert_array_equal(np.array(cb.values(), np.uint8), ref_cb)
     del cal
 
     chunk = 65536
-    blob = gpu_encode(x, cb, dtype, chunk, dirty=False)
+    blob = gpu_encode(x, cb, dtype, chunk, dirty=True)
     E = int(blob[24:32].cpu().numpy().view(np.uint64)[0])
     L = _layout(n, dtype, chunk, E)
     assert blob.numel() == L["size"]
-    hdr = blob[:64].cpu().numpy()
-    assert hdr[:4].view(np.uint32)[0] == 0x50495A53 and int(hdr[8:16].view(np.uint64)[0]) == n
-    np.testing.assert_array_equal(hdr[32:48], ref_cb)
+    hb = blob.cpu().numpy()
+
+    # header and inter-section padding, from the layout formula
+    np.testing.assert_array_equal(hb[:64], _expected_header(n, dtype, chunk, L["C"], E, ref_cb))
+    for lo, hi in ((L["index_end"], L["nib"]), (L["nib"] + (n + 1) // 2, L["sm"]), (L["sm"] + L["sm_bytes"], L["rec"])):
+        assert not hb[lo:hi].any(), "padding [%d, %d) not zero" % (lo, hi)
 
     # E = exponent mass outside the codebook, counted by torch on the device
     if dtype == 0:
@@ -292,31 +346,27 @@ def _full_size_check(name, sample_chunks=12):
     assert E == int(counts[~in_cb].sum())
 
     # index = exclusive prefix of the counts
-    cnt = blob[L["counts"]: L["counts"] + 4 * L["C"]].cpu().numpy().view(np.uint32).astype(np.uint64)
-    off = blob[L["index"]: L["index"] + 8 * L["C"]].cpu().numpy().view(np.uint64)
+    cnt = hb[L["counts"]: L["counts"] + 4 * L["C"]].view(np.uint32).astype(np.uint64)
+    off = hb[L["index"]: L["index"] + 8 * L["C"]].view(np.uint64)
     np.testing.assert_array_equal(off, np.concatenate([[0], np.cumsum(cnt)[:-1]]))
     assert int(cnt.sum()) == E
 
-    # sampled chunks against the oracle, chunk by chunk
-    rng = np.random.default_rng(0)
-    sample = sorted(set([0, L["C"] - 1] + list(rng.integers(0, L["C"], sample_chunks))))
-    sm_per_chunk = chunk if dtype == 0 else chunk * 3 // 8
-    for c in sample:
-        xs = np_bits(x[c * chunk: (c + 1) * chunk], dtype)
-        ref = oracle.encode(xs, dtype, ref_cb, chunk)
-        R = _layout(xs.size, dtype, chunk, oracle.parse_header(ref)[1].total_escapes)
-        got_nib = blob[L["nib"] + c * chunk // 2: L["nib"] + (c + 1) * chunk // 2].cpu().numpy()
-        np.testing.assert_array_equal(got_nib, ref[R["nib"]: R["nib"] + chunk // 2])
-        got_sm = blob[L["sm"] + c * sm_per_chunk: L["sm"] + (c + 1) * sm_per_chunk].cpu().numpy()
-        np.testing.assert_array_equal(got_sm, ref[R["sm"]: R["sm"] + sm_per_chunk])
-        k, o = int(cnt[c]), int(off[c])
-        assert 3 * k == R["size"] - R["rec"]
-        np.testing.assert_array_equal(blob[L["rec"] + 3 * o: L["rec"] + 3 * (o + k)].cpu().numpy(),
-                                      ref[R["rec"]: R["rec"] + 3 * k])
+    # every chunk against the oracle
+    xh = np_bits(x, dtype)
+    assert _compare_all_chunks(hb, xh, dtype, ref_cb, chunk, L, off, cnt) == L["C"]
+    del hb
 
     st, y = gpu_decode(blob, n, dtype)
     assert st == sz.OK
     assert torch.equal(y, x)
+    del y, blob
+
+    # an oracle-built container of a whole layer, decoded on the GPU
+    per = n // n_layers
+    ref = oracle.encode(xh[:per], dtype, ref_cb, chunk)
+    st, y = gpu_decode(torch.from_numpy(ref).to(DEV), per, dtype)
+    assert st == sz.OK
+    assert torch.equal(y, x[:per])
     return E / n
 
 
