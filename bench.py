@@ -63,6 +63,9 @@ def parse_args():
     p.add_argument("--no-workloads", action="store_true",
                    help="skip the per-workload object (the other four workloads, timed after the headline)")
     p.add_argument("--workload-steps", type=int, default=20, help="timed steps per workload of that object")
+    p.add_argument("--shard", action="store_true",
+                   help="under torchrun: rank r encodes and decodes chunks [r C / N, (r + 1) C / N) of one tensor "
+                        "(strong scaling) instead of a replica of the whole workload (weak scaling)")
     p.add_argument("--layers", type=int, default=32,
                    help="32-layer workloads: encode only L layers (a smaller case for profiling; "
                         "not a bench line)")
@@ -97,6 +100,28 @@ def reduce_over_ranks(x, world, device, op):
     t = torch.tensor([x], dtype=torch.float64, device=device)
     dist.all_reduce(t, op=dist.ReduceOp.MAX if op == "max" else dist.ReduceOp.SUM)
     return float(t.item())
+
+
+def shard_range(n, chunk, world, rank):
+    """Elements [lo, hi) of rank `rank`: a contiguous range of whole chunks,
+    chunks split as evenly as possible (the ranks' containers join into the
+    container of the whole tensor)."""
+    C = -(-n // chunk)
+    c0, c1 = C * rank // world, C * (rank + 1) // world
+    return min(n, c0 * chunk), min(n, c1 * chunk)
+
+
+def exclusive_scan_over_ranks(v, world, rank, device):
+    """Sum of `v` over the ranks below this one (0 on rank 0) and over all
+    ranks: where this rank's escape records start in the joined container."""
+    if world == 1:
+        return 0, v
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.int64, device=device)
+    got = [torch.zeros_like(t) for _ in range(world)]
+    dist.all_gather(got, t)
+    vals = [int(g.item()) for g in got]
+    return sum(vals[:rank]), sum(vals)
 
 
 # DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) of
@@ -240,7 +265,17 @@ class Workload:
     def calibration(self, device):
         return self.W.calibration_tensor(self.name, device)
 
-    def config(self, world):
+    def make_range(self, seed, lo, hi, device):
+        """Elements [lo, hi) of the workload (the layers that hold them are
+        generated, the rest is not)."""
+        if not self.layered:
+            return self.make(seed, device)[lo:hi].contiguous()
+        per = self.n // self.layers
+        l0, l1 = lo // per, -(-hi // per)
+        x = self.W.make_layers(self.name, seed, l1 - l0, device, first=self.first_layer + l0)
+        return x[lo - l0 * per: hi - l0 * per].contiguous()
+
+    def config(self, world, shard=False):
         label = self.name
         if self.layered and self.layers != 32:
             label = "%s (layers %d-%d only: profiling case)" % (self.name, self.first_layer,
@@ -251,13 +286,15 @@ class Workload:
                             + (" (layer 0)" if self.layered else ""),
                 "l2": ("inputs %.2f GB > 129 MB L2 (no flush needed)" % (self.n * self.elem_bytes / 1e9))
                 if self.n * self.elem_bytes > L2_BYTES else "L2 flushed (512 MB write) before every step",
-                "parallelism": "replicas of the workload per GPU, no collective" if world > 1 else "single GPU"}
+                "parallelism": ("chunk-range shards of one tensor, one container per GPU, no collective in the "
+                                "data path" if shard else "replicas of the workload per GPU, no collective")
+                if world > 1 else "single GPU"}
 
-    def algorithmic_bytes(self, E):
-        """(encode, decode) bytes the method must move: the elements, the two
-        dense streams, 3 bytes per escape record and 12 bytes of index per
-        chunk."""
-        n = self.n
+    def algorithmic_bytes(self, E, n=None):
+        """(encode, decode) bytes the method must move for n elements (default:
+        the workload's): the elements, the two dense streams, 3 bytes per
+        escape record and 12 bytes of index per chunk."""
+        n = self.n if n is None else n
         C = -(-n // CHUNK)
         streams = (n + 1) // 2 + (n if self.dtype == 0 else 3 * (-(-n // 8)))
         moved = n * self.elem_bytes + streams + 3 * E + 12 * C
@@ -447,7 +484,16 @@ def run_ours(args, world, rank, local):
     n, dtype = wl.n, wl.dtype
     raw_bytes = wl.elem_bytes * n
 
-    x = wl.make(rank, device)  # weak scaling: every rank has its own workload
+    if args.shard:
+        # strong scaling: the ranks split one tensor (seed 0) by whole chunks
+        lo, hi = shard_range(wl.n, CHUNK, world, rank)
+        x = wl.make_range(0, lo, hi, device)
+        n = hi - lo
+        raw_bytes = wl.elem_bytes * n
+        for leg in ("no_transfer", "no_online", "no_paged", "no_ablation", "no_workloads"):
+            setattr(args, leg, True)  # these legs measure whole workloads
+    else:
+        x = wl.make(rank, device)  # weak scaling: every rank has its own workload
     assert x.numel() == n
     cb, _ = sz.calibrate(wl.calibration(device), dtype)
 
@@ -514,7 +560,7 @@ def run_ours(args, world, rank, local):
     # kernels and two small memsets, decode a 4-byte memset, inside the events).
     peaks, peak_kind = measured_peaks()
     hbm = float(peaks["hbm_gbs"])
-    alg_encode, alg_decode = wl.algorithmic_bytes(E)
+    alg_encode, alg_decode = wl.algorithmic_bytes(E, n)
     tag = "bf16" if dtype == 0 else "e5m2"
     if enc_ms >= dec_ms:
         name, alg, ms = "encode_kernel<%s> (+ index and record kernels)" % tag, alg_encode, enc_ms
@@ -554,7 +600,7 @@ def run_ours(args, world, rank, local):
     e2e = None
     if not args.no_e2e:
         if wl.layered:
-            pieces = wl.layers
+            pieces = max(1, n // (wl.n // wl.layers))
         else:
             pieces = int(max(1, min(32, raw_bytes // (64 << 20))))
         piece_n = -(-(-(-n // pieces)) // CHUNK) * CHUNK
@@ -811,6 +857,15 @@ def run_ours(args, world, rank, local):
                                  "sample": "%d elements in %.1f s: passes over the first %d elements, %s" % (
                                      elems1, secs1, distinct1, what % block1)}}
 
+    # ---- shards: where this rank's records start in the joined container
+    # (an exclusive scan of the per-rank escape totals) and its size ----
+    shard = None
+    if args.shard:
+        base, E_all = exclusive_scan_over_ranks(E, world, rank, device)
+        joined = sz.compressed_size(wl.n, dtype, CHUNK, E_all)
+        shard = {"elements": n, "range": list(shard_range(wl.n, CHUNK, world, rank)), "escape_base": base,
+                 "joined_escapes": E_all, "joined_bytes": joined, "joined_ratio": round(wl.elem_bytes * wl.n / joined, 5)}
+
     # ---- the other workloads (one line carries all five), timed after the
     # headline's buffers are released ----
     workloads = None
@@ -827,9 +882,10 @@ def run_ours(args, world, rank, local):
     return {
         "metric": METRIC, "value": round(value, 3), "unit": "GB/s", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "u16" if dtype == 0 else "u8",
+        "scaling": "strong" if args.shard else "weak", "vs_baseline": None,
+        "dtype": "u16" if dtype == 0 else "u8",
         "data": "synthetic (seeded torch CPU generator, rounded on the GPU; recipe of the workload module)",
-        "config": wl.config(world),
+        "config": wl.config(world, args.shard), "shard": shard,
         "encode_gbs": round(enc_gbs, 2), "decode_gbs": round(dec_gbs, 2),
         "encode_hbm_frac": round(alg_encode / (enc_ms * 1e-3) / 1e9 / hbm, 4),
         "decode_hbm_frac": round(alg_decode / (dec_ms * 1e-3) / 1e9 / hbm, 4),

@@ -314,6 +314,23 @@ int splitzip_transfer(const void* d_src, void* d_dst, uint64_t n, int dtype, con
                       uint64_t d_scratch_bytes, void* h_stage, uint64_t h_stage_bytes, uint64_t* out_link_bytes,
                       float* out_ms, cudaStream_t stream);
 
+/* Join the containers of consecutive pieces of one tensor into the container
+ * of the whole tensor, byte-identical to encoding it in one call.  Chunks are
+ * independent (Method, "Escape stream": positions are 16-bit offsets within a
+ * chunk), so a tensor can be encoded in pieces of whole chunks -- one piece
+ * per GPU when the work is spread over several, or one per layer -- and
+ * joined afterwards; the escape offsets of piece i move by the escapes of
+ * pieces 0..i-1 (an exclusive scan of the per-piece totals).  Host memory
+ * only: h_parts[i] holds part_bytes[i] bytes of piece i's container (pieces
+ * in tensor order).  Every piece must have the same dtype, chunk size and
+ * codebook, and every piece but the last a whole number of chunks
+ * (SPLITZIP_ERR_INVALID_ARG otherwise); a malformed header or index gives
+ * SPLITZIP_ERR_CORRUPT.  *out_bytes receives the merged size; with h_out ==
+ * NULL nothing else happens (a size query), else out_capacity must cover
+ * that size (SPLITZIP_ERR_CAPACITY) and h_out receives the container. */
+int splitzip_merge(const void* const* h_parts, const uint64_t* part_bytes, uint32_t count, void* h_out,
+                   uint64_t out_capacity, uint64_t* out_bytes);
+
 /* Self-test of the bounded device wait.  Every wait of the encode and
  * decode kernels on a bulk-copy barrier gives up after a bounded number of SM
  * cycles (about one second), records SPLITZIP_ERR_TIMEOUT in the status word

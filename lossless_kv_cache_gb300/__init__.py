@@ -117,6 +117,8 @@ SIGNATURES = {
     "splitzip_transfer": (_int, [_vp, _vp, _u64, _int, ctypes.POINTER(Codebook), _u32, _u64, _int, _vp, _u64, _vp,
                                  _u64, _P_u64, ctypes.POINTER(ctypes.c_float), _vp]),
     "splitzip_selftest_bounded_wait": (_int, [_u64, _vp, _vp, _vp]),
+    "splitzip_merge": (_int, [ctypes.POINTER(ctypes.c_void_p), ctypes.POINTER(ctypes.c_uint64), _u32, _vp, _u64,
+                              _P_u64]),
 }
 
 _lib = None
@@ -236,6 +238,11 @@ def splitzip_selftest_bounded_wait(limit_cycles, d_status, d_cycles, stream):
     return lib().splitzip_selftest_bounded_wait(limit_cycles, d_status, d_cycles, stream)
 
 
+def splitzip_merge(h_parts, part_bytes, count, h_out, out_capacity, out_bytes):
+    """h_parts: ctypes array of c_void_p; part_bytes: ctypes array of c_uint64."""
+    return lib().splitzip_merge(h_parts, part_bytes, count, h_out, out_capacity, ctypes.byref(out_bytes))
+
+
 # ------------------------------------------------------------ size helpers
 
 def _size_call(fn, *args):
@@ -256,6 +263,20 @@ def compressed_size(n, dtype, chunk_elems, total_escapes):
 
 def workspace_size(n, dtype, chunk_elems=DEFAULT_CHUNK_ELEMS):
     return _size_call(splitzip_encode_workspace_size, n, dtype, chunk_elems)
+
+
+def merge(parts):
+    """Join host containers (numpy uint8 arrays, tensor order) of consecutive
+    whole-chunk pieces into the container of the whole tensor (numpy uint8)."""
+    import numpy as np
+    arrs = [np.ascontiguousarray(p, dtype=np.uint8) for p in parts]
+    ptrs = (ctypes.c_void_p * len(arrs))(*[a.ctypes.data for a in arrs])
+    sizes = (ctypes.c_uint64 * len(arrs))(*[a.size for a in arrs])
+    total = ctypes.c_uint64(0)
+    _check(splitzip_merge(ptrs, sizes, len(arrs), None, 0, total), "splitzip_merge")
+    out = np.empty(max(total.value, 1), dtype=np.uint8)
+    _check(splitzip_merge(ptrs, sizes, len(arrs), out.ctypes.data, out.size, total), "splitzip_merge")
+    return out[: total.value]
 
 
 def parse_header(blob_bytes):

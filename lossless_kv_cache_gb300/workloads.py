@@ -10,7 +10,8 @@ activations of Qwen, Llama and Phi models, which are not available here; the
 tensors below stand in for them.  Layout is contiguous
 [layer][K,V][token][kv_head][head_dim], channel = kv_head * 128 + dim.
 
-Every tensor is returned as raw bits: BF16 as torch.int16, E5M2 as torch.uint8.
+Every tensor is returned as raw bits: BF16 and FP16 as torch.int16, E5M2 as
+torch.uint8.
 Per-layer generators use seed ``seed * 1000 + layer`` so a 32-layer cache can be
 produced one layer at a time.  The random numbers are always drawn with the CPU
 generator (torch.Generator on the CPU, the seeds above), whatever device the
@@ -42,6 +43,12 @@ def to_bf16_bits(x):
 def to_e5m2_bits(x):
     # torch rounds to nearest even and does not saturate (overflow -> inf)
     return x.to(torch.float8_e5m2).view(torch.uint8)
+
+
+def to_fp16_bits(x):
+    # round to nearest even; values beyond 65504 would become inf (the
+    # recipes' scales stay far below it)
+    return x.to(torch.float16).view(torch.int16)
 
 
 def kv_tile_k_only(seed, tokens=1024, device="cpu"):
@@ -86,6 +93,10 @@ def kv_cache_layer_e5m2(seed, layer, tokens=65536, device="cpu"):
     return to_e5m2_bits(kv_cache_layer_f32(seed, layer, tokens).to(device)).reshape(-1)
 
 
+def kv_cache_layer_fp16(seed, layer, tokens=32768, device="cpu"):
+    return to_fp16_bits(kv_cache_layer_f32(seed, layer, tokens).to(device)).reshape(-1)
+
+
 def escape_stress(seed, chunks=64, chunk_elems=65536, sigma=3.0, device="cpu"):
     """Heavy-tailed values: Student-t(df=2) x per-element lognormal(0, sigma).
 
@@ -112,6 +123,13 @@ def special_e5m2_patterns():
     return torch.tensor(pats, dtype=torch.uint8)
 
 
+def special_fp16_patterns():
+    """Sign/zero/inf/NaN/subnormal bit patterns and their neighbours (FP16)."""
+    pats = [0x0000, 0x8000, 0x7C00, 0xFC00, 0x7E00, 0xFE00, 0x7E01, 0x7C01, 0xFFFF,
+            0x0001, 0x8001, 0x03FF, 0x83FF, 0x0400, 0x8400, 0x7BFF, 0xFBFF, 0x3C00, 0xBC00]
+    return torch.tensor(pats, dtype=torch.int32).to(torch.int16)
+
+
 def all_bf16_patterns():
     return torch.arange(65536, dtype=torch.int32).to(torch.int16)
 
@@ -135,6 +153,9 @@ WORKLOADS = {
                                     "BF16 Student-t(2) x lognormal(0,3), 64 chunks of 65536"),
     "kv_cache_32x2x65536x8x128_e5m2": (1, 32 * 2 * 65536 * CHANNELS,
                                        "FP8-E5M2 32 layers K+V, 65536 tok x 8 heads x 128"),
+    # beyond the five: the BF16 cache recipe rounded to FP16 instead
+    "kv_cache_32x2x32768x8x128_fp16": (2, 32 * 2 * 32768 * CHANNELS,
+                                       "FP16 32 layers K+V, 32768 tok x 8 heads x 128"),
 }
 
 
@@ -144,6 +165,8 @@ def layers_of(name):
         return 32, lambda seed, layer, device="cpu": kv_cache_layer_bf16(seed, layer, 32768, device)
     if name == "kv_cache_32x2x65536x8x128_e5m2":
         return 32, lambda seed, layer, device="cpu": kv_cache_layer_e5m2(seed, layer, 65536, device)
+    if name == "kv_cache_32x2x32768x8x128_fp16":
+        return 32, lambda seed, layer, device="cpu": kv_cache_layer_fp16(seed, layer, 32768, device)
     raise KeyError(name)
 
 
@@ -177,7 +200,8 @@ def make_layers(name, seed, n_layers, device="cpu", first=0):
 def calibration_tensor(name, device="cpu"):
     """The tensor each workload's codebook is calibrated on: seed 1 of the same
     recipe (for the 32-layer caches: layer 0 of seed 1)."""
-    if name in ("kv_cache_32x2x32768x8x128_bf16", "kv_cache_32x2x65536x8x128_e5m2"):
+    if name in ("kv_cache_32x2x32768x8x128_bf16", "kv_cache_32x2x65536x8x128_e5m2",
+                "kv_cache_32x2x32768x8x128_fp16"):
         _, layer = layers_of(name)
         return layer(1, 0, device)
     return make(name, 1, device)
@@ -192,7 +216,7 @@ def numel(name):
 
 
 def bytes_per_element(dtype):
-    return 2 if dtype == 0 else 1
+    return 1 if dtype == 1 else 2
 
 
 def gigabytes(n_bytes):

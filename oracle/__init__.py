@@ -3,7 +3,8 @@
 TEST INFRASTRUCTURE ONLY: tests/, ``__graft_entry__.smoke()`` and the CPU
 baseline leg of ``bench.py`` may use it; the product package never does.
 
-Arrays are numpy arrays of raw bits: BF16 as ``uint16``, FP8-E5M2 as ``uint8``.
+Arrays are numpy arrays of raw bits: BF16 and FP16 as ``uint16``, FP8-E5M2 as
+``uint8``.
 """
 import ctypes
 
@@ -13,6 +14,7 @@ from . import build_oracle
 
 BF16 = 0
 E5M2 = 1
+FP16 = 2
 OK, INVALID, CAPACITY, CORRUPT = 0, 1, 2, 3
 
 _lib = None
@@ -65,7 +67,7 @@ def _ptr(a):
 
 
 def _check_bits(x, dtype):
-    want = np.uint16 if dtype == BF16 else np.uint8
+    want = np.uint8 if dtype == E5M2 else np.uint16
     x = np.ascontiguousarray(x)
     if x.dtype != want:
         raise TypeError("dtype %d wants %s bits, got %s" % (dtype, want.__name__, x.dtype))
@@ -126,7 +128,7 @@ def encode(x, dtype, codebook, chunk_elems=65536):
 def decode_status(blob, n, dtype):
     """Decode ``blob``; return (status, decoded bits)."""
     blob = np.ascontiguousarray(blob, dtype=np.uint8)
-    out = np.zeros(n, dtype=np.uint16 if dtype == BF16 else np.uint8)
+    out = np.zeros(n, dtype=np.uint8 if dtype == E5M2 else np.uint16)
     st = lib().oracle_decode(_ptr(blob), blob.size, _ptr(out), n, dtype)
     return st, out
 

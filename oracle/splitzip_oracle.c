@@ -49,6 +49,13 @@
  *   READING R11 the 16-bit position is the in-chunk index.
  *   READING R12 no value is special: NaN, inf, zero and subnormal exponents
  *               are ordinary exponent values; there is no float arithmetic.
+ *   READING R16 FP16 (dtype 2; the page's "other formats", Significance): the
+ *               5-bit exponent (bits 14..10) is coded through the Top-16
+ *               codebook exactly as E5M2's; sign|mantissa s11 = (sign << 10) |
+ *               mantissa10, packed as an LSB-first bitstream, element i at bits
+ *               [11i, 11i+11), padded with zero bits to 11*ceil(n/8) bytes;
+ *               the escape exponent byte is the 5-bit value zero-extended.
+ *               4 + 11 = 15 bits per element bound the ratio by 16/15.
  */
 #include <stdint.h>
 #include <string.h>
@@ -56,6 +63,7 @@
 
 #define OR_BF16 0
 #define OR_E5M2 1
+#define OR_FP16 2
 
 #define OR_OK 0
 #define OR_INVALID 1
@@ -89,10 +97,16 @@ static uint64_t align16(uint64_t x) { return (x + 15u) & ~(uint64_t)15u; }
  * kept raw.  BF16 bit 15 = sign, bits 14..7 = exponent, bits 6..0 = mantissa.
  * E5M2 bit 7 = sign, bits 6..2 = exponent, bits 1..0 = mantissa. -------------- */
 
+static int valid_dtype(int dtype) { return dtype == OR_BF16 || dtype == OR_E5M2 || dtype == OR_FP16; }
+
 static unsigned exponent_bins(int dtype) { return dtype == OR_BF16 ? 256u : 32u; }
 
+/* bits of one element's sign|mantissa field in the packed streams (E5M2,
+ * FP16; BF16 stores it as one byte) */
+static unsigned sm_bits(int dtype) { return dtype == OR_FP16 ? 11u : 3u; }
+
 static unsigned read_element(const void* x, int dtype, uint64_t i) {
-    if (dtype == OR_BF16) {
+    if (dtype != OR_E5M2) {
         const uint8_t* p = (const uint8_t*)x + 2 * i;
         return (unsigned)p[0] | ((unsigned)p[1] << 8);
     }
@@ -100,7 +114,7 @@ static unsigned read_element(const void* x, int dtype, uint64_t i) {
 }
 
 static void write_element(void* out, int dtype, uint64_t i, unsigned v) {
-    if (dtype == OR_BF16) {
+    if (dtype != OR_E5M2) {
         uint8_t* p = (uint8_t*)out + 2 * i;
         p[0] = (uint8_t)v;
         p[1] = (uint8_t)(v >> 8);
@@ -111,18 +125,22 @@ static void write_element(void* out, int dtype, uint64_t i, unsigned v) {
 
 static unsigned exponent_of(int dtype, unsigned v) {
     if (dtype == OR_BF16) return (v >> 7) & 0xFFu;
+    if (dtype == OR_FP16) return (v >> 10) & 0x1Fu;
     return (v >> 2) & 0x1Fu;
 }
 
-/* sign|mantissa field: READING R3 (BF16), READING R7 (E5M2). */
+/* sign|mantissa field: READING R3 (BF16), READING R7 (E5M2), READING R16
+ * (FP16). */
 static unsigned sign_mantissa_of(int dtype, unsigned v) {
     if (dtype == OR_BF16) return (((v >> 15) & 1u) << 7) | (v & 0x7Fu);
+    if (dtype == OR_FP16) return (((v >> 15) & 1u) << 10) | (v & 0x3FFu);
     return (((v >> 7) & 1u) << 2) | (v & 0x3u);
 }
 
 /* inverse of the split: put sign, exponent and mantissa back in place. */
 static unsigned join_fields(int dtype, unsigned sm, unsigned e) {
     if (dtype == OR_BF16) return (((sm >> 7) & 1u) << 15) | ((e & 0xFFu) << 7) | (sm & 0x7Fu);
+    if (dtype == OR_FP16) return (((sm >> 10) & 1u) << 15) | ((e & 0x1Fu) << 10) | (sm & 0x3FFu);
     return (((sm >> 2) & 1u) << 7) | ((e & 0x1Fu) << 2) | (sm & 0x3u);
 }
 
@@ -130,6 +148,7 @@ static unsigned join_fields(int dtype, unsigned sm, unsigned e) {
 
 static uint64_t sm_stream_bytes(int dtype, uint64_t n) {
     if (dtype == OR_BF16) return n;
+    if (dtype == OR_FP16) return 11u * ((n + 7u) / 8u);
     return 3u * ((n + 7u) / 8u);
 }
 
@@ -162,7 +181,7 @@ uint64_t oracle_container_size(uint64_t n, int dtype, uint32_t chunk, uint64_t t
  * one codebook calibrated offline) ------------------------------------------- */
 
 int oracle_histogram(const void* x, uint64_t n, int dtype, uint64_t* hist256) {
-    if (!hist256 || (n && !x) || (dtype != OR_BF16 && dtype != OR_E5M2)) return OR_INVALID;
+    if (!hist256 || (n && !x) || !valid_dtype(dtype)) return OR_INVALID;
     for (int b = 0; b < 256; b++) hist256[b] = 0;
     for (uint64_t i = 0; i < n; i++) hist256[exponent_of(dtype, read_element(x, dtype, i))]++;
     return OR_OK;
@@ -174,7 +193,7 @@ int oracle_histogram(const void* x, uint64_t n, int dtype, uint64_t* hist256) {
  * count, the smaller value on a tie. ------------------------------------------ */
 
 int oracle_calibrate(const uint64_t* hist256, int dtype, uint8_t* cb16) {
-    if (!hist256 || !cb16 || (dtype != OR_BF16 && dtype != OR_E5M2)) return OR_INVALID;
+    if (!hist256 || !cb16 || !valid_dtype(dtype)) return OR_INVALID;
     unsigned bins = exponent_bins(dtype);
     for (unsigned b = bins; b < 256; b++)
         if (hist256[b] != 0) return OR_INVALID;
@@ -213,7 +232,7 @@ static int valid_codebook(const uint8_t* cb16, int dtype) {
  * is outside the codebook. */
 int oracle_chunk_escape_counts(const void* x, uint64_t n, int dtype, const uint8_t* cb16,
                                uint32_t chunk, uint32_t* counts) {
-    if ((n && (!x || !counts)) || !cb16 || (dtype != OR_BF16 && dtype != OR_E5M2) ||
+    if ((n && (!x || !counts)) || !cb16 || !valid_dtype(dtype) ||
         !valid_chunk(chunk) || !valid_codebook(cb16, dtype))
         return OR_INVALID;
     uint64_t C = (n + chunk - 1u) / chunk;
@@ -232,7 +251,7 @@ int oracle_chunk_escape_counts(const void* x, uint64_t n, int dtype, const uint8
 
 int oracle_encode(const void* x, uint64_t n, int dtype, const uint8_t* cb16, uint32_t chunk,
                   uint8_t* out, uint64_t capacity, uint64_t* out_size) {
-    if ((n && !x) || !cb16 || !out || !out_size || (dtype != OR_BF16 && dtype != OR_E5M2) ||
+    if ((n && !x) || !cb16 || !out || !out_size || !valid_dtype(dtype) ||
         !valid_chunk(chunk) || !valid_codebook(cb16, dtype))
         return OR_INVALID;
     uint64_t C = (n + chunk - 1u) / chunk;
@@ -289,9 +308,10 @@ int oracle_encode(const void* x, uint64_t n, int dtype, const uint8_t* cb16, uin
         if (dtype == OR_BF16) {
             out[L.sm_off + i] = (uint8_t)sm;
         } else {
-            for (unsigned b = 0; b < 3; b++) {
+            unsigned w = sm_bits(dtype);
+            for (unsigned b = 0; b < w; b++) {
                 if ((sm >> b) & 1u) {
-                    uint64_t bit = 3u * i + b;
+                    uint64_t bit = (uint64_t)w * i + b;
                     out[L.sm_off + bit / 8] |= (uint8_t)(1u << (bit % 8));
                 }
             }
@@ -315,7 +335,7 @@ int oracle_parse_header(const uint8_t* blob, uint64_t bytes, oracle_header_t* h)
     if (!blob || !h) return OR_INVALID;
     if (bytes < OR_HEADER_BYTES) return OR_CORRUPT;
     if (get_u32(blob) != OR_MAGIC || get_u16(blob + 4) != OR_VERSION) return OR_CORRUPT;
-    if (blob[6] != OR_BF16 && blob[6] != OR_E5M2) return OR_CORRUPT;
+    if (!valid_dtype(blob[6])) return OR_CORRUPT;
     if (blob[7] != 0) return OR_CORRUPT;
     for (int k = 48; k < 64; k++)
         if (blob[k] != 0) return OR_CORRUPT;
@@ -341,7 +361,7 @@ int oracle_parse_header(const uint8_t* blob, uint64_t bytes, oracle_header_t* h)
  * of the escaped elements with their original values. */
 
 int oracle_decode(const uint8_t* blob, uint64_t bytes, void* out, uint64_t n, int dtype) {
-    if (!blob || (n && !out) || (dtype != OR_BF16 && dtype != OR_E5M2)) return OR_INVALID;
+    if (!blob || (n && !out) || !valid_dtype(dtype)) return OR_INVALID;
     oracle_header_t h;
     int st = oracle_parse_header(blob, bytes, &h);
     if (st != OR_OK) return st;
@@ -368,9 +388,10 @@ int oracle_decode(const uint8_t* blob, uint64_t bytes, void* out, uint64_t n, in
         if (dtype == OR_BF16) {
             sm = blob[L.sm_off + i];
         } else {
+            unsigned w = sm_bits(dtype);
             sm = 0;
-            for (unsigned b = 0; b < 3; b++) {
-                uint64_t bit = 3u * i + b;
+            for (unsigned b = 0; b < w; b++) {
+                uint64_t bit = (uint64_t)w * i + b;
                 sm |= ((blob[L.sm_off + bit / 8] >> (bit % 8)) & 1u) << b;
             }
         }

@@ -4,7 +4,9 @@ import os
 import numpy as np
 
 GOLDEN_DIR = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
-CONTAINER_FIXTURES = ["bf16_five_elements.txt", "bf16_two_chunks_ragged.txt", "e5m2_nine_elements.txt"]
+CONTAINER_FIXTURES = ["bf16_five_elements.txt", "bf16_two_chunks_ragged.txt", "e5m2_nine_elements.txt",
+                      "fp16_nine_elements.txt"]
+DTYPES = {"bf16": 0, "e5m2": 1, "fp16": 2}
 
 
 def _lines(name):
@@ -22,7 +24,7 @@ def load_container(name):
     for tok in _lines(name):
         key = tok[0]
         if key == "dtype":
-            fx["dtype"] = {"bf16": 0, "e5m2": 1}[tok[1]]
+            fx["dtype"] = DTYPES[tok[1]]
         elif key in ("chunk_elems", "n", "size"):
             fx[key] = int(tok[1])
         elif key == "input_default":
@@ -35,7 +37,7 @@ def load_container(name):
             fx["bytes"].append((int(tok[1]), [int(t, 16) for t in tok[2:]]))
         else:
             raise ValueError("unknown fixture key %r in %s" % (key, name))
-    bits = np.uint16 if fx["dtype"] == 0 else np.uint8
+    bits = np.uint8 if fx["dtype"] == 1 else np.uint16
     x = np.full(fx["n"], fx["default"], dtype=bits)
     for i, v in inputs:
         x[i] = v
@@ -51,7 +53,7 @@ def load_calibration_cases(name="calibration_ties.txt"):
     cases = []
     for tok in _lines(name):
         if tok[0] == "case":
-            cases.append({"dtype": {"bf16": 0, "e5m2": 1}[tok[1]], "hist": np.zeros(256, np.uint64)})
+            cases.append({"dtype": DTYPES[tok[1]], "hist": np.zeros(256, np.uint64)})
         elif tok[0] == "hist":
             cases[-1]["hist"][int(tok[1])] = int(tok[2])
         elif tok[0] == "expect":

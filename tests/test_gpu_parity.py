@@ -247,6 +247,8 @@ def test_chunk_aligned_shards_match_single_container():
     rw = whole[hw.escrec_off: hw.escrec_off + 3 * hw.total_escapes]
     np.testing.assert_array_equal(rw[: 3 * E0], parts[0][hp[0].escrec_off: hp[0].escrec_off + 3 * E0])
     np.testing.assert_array_equal(rw[3 * E0:], parts[1][hp[1].escrec_off: hp[1].size])
+    # and the library's merge joins the two shard containers into the whole one
+    np.testing.assert_array_equal(sz.merge(parts), whole)
 
 
 # ------------------------------------------- the 4.3 GB workloads, whole

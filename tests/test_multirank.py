@@ -1,11 +1,14 @@
 """Multi-rank path on CPU: two gloo ranks.
 
 The codec shards by whole chunks with no data exchange: each rank encodes its
-own chunk range, and the only cross-rank steps are the barrier and the
-max/sum reductions bench.py uses for its timing and byte totals.  This test
-runs those reductions on two processes and checks that containers encoded per
-rank (by the CPU oracle: no GPU here) hold exactly the corresponding sections
-of the single-rank container.
+own chunk range (bench.shard_range, as bench.py --shard does), and the only
+cross-rank steps are the barrier, the max/sum reductions bench.py uses for
+its timing and byte totals, and the exclusive scan of the per-rank escape
+totals that places each rank's records in the joined container.  This test
+runs those steps on two processes, encodes each rank's range with the CPU
+oracle (no GPU here), and joins the gathered per-rank containers with the
+library's splitzip_merge: the result must be the single-rank container, byte
+for byte.
 """
 import os
 import socket
@@ -39,11 +42,13 @@ def _worker(rank, world, port, results):
     chunk = 4096
     x = W.escape_stress(0, chunks=6, chunk_elems=chunk, sigma=2.0).numpy().view(np.uint16)[:6 * chunk - 100]
     cb = oracle.calibrate(oracle.histogram(x, 0), 0)
-    lo, hi = (0, 3 * chunk) if rank == 0 else (3 * chunk, x.size)  # whole chunks per rank
+    lo, hi = bench.shard_range(x.size, chunk, w, r)  # whole chunks per rank
     mine = oracle.encode(x[lo:hi], 0, cb, chunk)
+    E_mine = oracle.parse_header(mine)[1].total_escapes
+    base, E_all = bench.exclusive_scan_over_ranks(E_mine, w, r, "cpu")
     blobs = [None] * w
     dist.all_gather_object(blobs, mine)
-    results[rank] = (mx, sm, blobs if rank == 0 else None, x if rank == 0 else None, cb)
+    results[rank] = (mx, sm, blobs if rank == 0 else None, x if rank == 0 else None, cb, (lo, hi, E_mine, base, E_all))
     dist.destroy_process_group()
 
 
@@ -72,11 +77,18 @@ def test_two_gloo_ranks_reduce_and_shard():
     for p in procs:
         p.join(240)
         assert p.exitcode == 0
-    mx, sm, blobs, x, cb = results[0]
+    mx, sm, blobs, x, cb, scan0 = results[0]
+    scan1 = results[1][5]
     assert (mx, sm) == (2.0, 3.0) and results[1][:2] == (2.0, 3.0)
+    # the ranks' ranges tile the tensor; the scan gives each rank its record base
+    assert scan0[0] == 0 and scan0[1] == scan1[0] and scan1[1] == x.size
+    assert scan0[3] == 0 and scan1[3] == scan0[2] and scan0[4] == scan1[4] == scan0[2] + scan1[2]
 
     import oracle
-    whole = _sections(oracle.encode(x, 0, cb, 4096))
+    import lossless_kv_cache_gb300 as sz
+    whole_blob = oracle.encode(x, 0, cb, 4096)
+    np.testing.assert_array_equal(sz.merge(blobs), whole_blob)
+    whole = _sections(whole_blob)
     parts = [_sections(b) for b in blobs]
     assert whole["E"] == sum(p["E"] for p in parts)
     np.testing.assert_array_equal(whole["counts"], np.concatenate([p["counts"] for p in parts]))

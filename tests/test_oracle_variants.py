@@ -110,3 +110,11 @@ def test_variant_corruptions_are_rejected():
     b = blob.copy()
     b[81] = 0xF0  # element 3 becomes a sentinel too: two sentinels, one escape
     assert oracle.decode_variant_status(b, 5, oracle.BF16)[0] == oracle.CORRUPT
+
+
+def test_variants_are_defined_for_bf16_and_e5m2_only():
+    """The ablation formats (readings V1-V3) are defined for the page's two
+    dtypes; the oracle refuses FP16 for them."""
+    x = np.arange(4096, dtype=np.uint16)
+    with pytest.raises(ValueError):
+        oracle.encode_variant(x, oracle.FP16, oracle.variant_codebook(np.arange(16), oracle.TOP8), 4096, oracle.TOP8)
