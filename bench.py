@@ -41,6 +41,13 @@ DEFAULT_WORKLOAD = "kv_cache_32x2x32768x8x128_bf16"
 CHUNK = 65536
 LINKS_GBS = (50.0, 100.0)
 L2_BYTES = 129 * 1000 * 1000
+ELEMENT_DTYPE = {0: "bf16", 1: "fp8_e5m2", 2: "fp16"}
+
+
+def signmant_bytes(dtype, n):
+    """Bytes of the sign|mantissa stream: BF16 1 per element, E5M2 3 and FP16
+    11 per 8 elements."""
+    return n if dtype == 0 else (11 if dtype == 2 else 3) * (-(-n // 8))
 
 
 def parse_args():
@@ -249,7 +256,8 @@ class Workload:
         self.name = name
         self.dtype = W.dtype_of(name)
         self.elem_bytes = W.bytes_per_element(self.dtype)
-        self.layered = name in ("kv_cache_32x2x32768x8x128_bf16", "kv_cache_32x2x65536x8x128_e5m2")
+        self.layered = name in ("kv_cache_32x2x32768x8x128_bf16", "kv_cache_32x2x65536x8x128_e5m2",
+                                "kv_cache_32x2x32768x8x128_fp16")
         self.layers = layers if self.layered else None
         self.first_layer = first_layer if self.layered else 0
         if self.layered and not (0 <= first_layer and layers >= 1 and first_layer + layers <= 32):
@@ -281,7 +289,7 @@ class Workload:
             label = "%s (layers %d-%d only: profiling case)" % (self.name, self.first_layer,
                                                                 self.first_layer + self.layers - 1)
         return {"workload": label, "elements": self.n,
-                "element_dtype": "bf16" if self.dtype == 0 else "fp8_e5m2", "chunk_elems": CHUNK,
+                "element_dtype": ELEMENT_DTYPE[self.dtype], "chunk_elems": CHUNK,
                 "codebook": "Top-16 from the seed-1 calibration tensor"
                             + (" (layer 0)" if self.layered else ""),
                 "l2": ("inputs %.2f GB > 129 MB L2 (no flush needed)" % (self.n * self.elem_bytes / 1e9))
@@ -296,7 +304,7 @@ class Workload:
         escape record and 12 bytes of index per chunk."""
         n = self.n if n is None else n
         C = -(-n // CHUNK)
-        streams = (n + 1) // 2 + (n if self.dtype == 0 else 3 * (-(-n // 8)))
+        streams = (n + 1) // 2 + signmant_bytes(self.dtype, n)
         moved = n * self.elem_bytes + streams + 3 * E + 12 * C
         return moved, moved
 
@@ -356,7 +364,7 @@ def measure_workload(name, steps, warmup, device, hbm):
     for L in LINKS_GBS:
         t_plain = raw / (L * 1e9)
         link["%d_GBps" % int(L)] = round(t_plain / ((enc + dec) * 1e-3 + size / (L * 1e9)), 4)
-    res = {"elements": n, "element_dtype": "bf16" if dtype == 0 else "fp8_e5m2", "steps": steps,
+    res = {"elements": n, "element_dtype": ELEMENT_DTYPE[dtype], "steps": steps,
            "encode_ms": round(enc, 5), "decode_ms": round(dec, 5),
            "encode_gbs": round(raw / (enc * 1e-3) / 1e9, 2), "decode_gbs": round(raw / (dec * 1e-3) / 1e9, 2),
            "round_trip_gbs": round(raw / ((enc + dec) * 1e-3) / 1e9, 2),
@@ -411,11 +419,11 @@ def oracle_throughput(x_dev, dtype, cb_exps, seconds, threads):
     elements per container)."""
     from concurrent.futures import ThreadPoolExecutor
     cb = np.asarray(cb_exps, dtype=np.uint8)
-    eb = 2 if dtype == 0 else 1
+    eb = 1 if dtype == 1 else 2
     block = oracle_block(x_dev.numel(), threads)
     distinct = min(x_dev.numel(), 2 * threads * block)
     host = x_dev[:distinct].cpu().numpy()
-    host = host.view(np.uint16) if dtype == 0 else host
+    host = host if dtype == 1 else host.view(np.uint16)
     blocks = [host[i: i + block] for i in range(0, distinct, block)]
     done, t_total = 0, 0.0
     with ThreadPoolExecutor(threads) as pool:
@@ -441,7 +449,7 @@ def run_reference(args, world, rank):
     else:
         x = wl.make(0, "cpu").numpy()
         cal = wl.calibration("cpu").numpy()
-    if wl.dtype == 0:
+    if wl.dtype != 1:
         x, cal = x.view(np.uint16), cal.view(np.uint16)
     cb = oracle.calibrate(oracle.histogram(cal, wl.dtype), wl.dtype)
     from concurrent.futures import ThreadPoolExecutor
@@ -466,7 +474,7 @@ def run_reference(args, world, rank):
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * total / len(times), 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "u16" if wl.dtype == 0 else "u8",
+        "dtype": "u8" if wl.dtype == 1 else "u16",
         "data": "synthetic (seeded torch CPU generator)", "config": wl.config(world),
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
                          "sample": sample},
@@ -561,7 +569,7 @@ def run_ours(args, world, rank, local):
     peaks, peak_kind = measured_peaks()
     hbm = float(peaks["hbm_gbs"])
     alg_encode, alg_decode = wl.algorithmic_bytes(E, n)
-    tag = "bf16" if dtype == 0 else "e5m2"
+    tag = {0: "bf16", 1: "e5m2", 2: "fp16"}[dtype]
     if enc_ms >= dec_ms:
         name, alg, ms = "encode_kernel<%s> (+ index and record kernels)" % tag, alg_encode, enc_ms
     else:
@@ -874,7 +882,8 @@ def run_ours(args, world, rank, local):
         torch.cuda.empty_cache()
         workloads = {}
         for other in ("kv_tile_1x1024x8x128_bf16", "llama_layer_2x8192x8x128_bf16",
-                      "escape_stress_64x65536_bf16", "kv_cache_32x2x65536x8x128_e5m2"):
+                      "escape_stress_64x65536_bf16", "kv_cache_32x2x65536x8x128_e5m2",
+                      "kv_cache_32x2x32768x8x128_fp16"):
             workloads[other] = measure_workload(other, args.workload_steps, args.warmup, device, hbm)
 
     if rank != 0:
@@ -883,7 +892,7 @@ def run_ours(args, world, rank, local):
         "metric": METRIC, "value": round(value, 3), "unit": "GB/s", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
         "scaling": "strong" if args.shard else "weak", "vs_baseline": None,
-        "dtype": "u16" if dtype == 0 else "u8",
+        "dtype": "u8" if dtype == 1 else "u16",
         "data": "synthetic (seeded torch CPU generator, rounded on the GPU; recipe of the workload module)",
         "config": wl.config(world, args.shard), "shard": shard,
         "encode_gbs": round(enc_gbs, 2), "decode_gbs": round(dec_gbs, 2),

@@ -2,13 +2,14 @@
  * splitzip.h — C ABI of the GB300 (sm_103a) SplitZip lossless KV-cache codec.
  *
  * Method: "SplitZip: Ultra Fast Lossless KV Compression for Disaggregated LLM
- * Serving" (gist.science summary page), section "Method: SplitZip".  A BF16 or
- * FP8-E5M2 tensor is split into
+ * Serving" (gist.science summary page), section "Method: SplitZip".  A BF16,
+ * FP8-E5M2 or FP16 tensor is split into
  *   - a 4-bit code per element: the exponent mapped through an offline
  *     calibrated Top-16 codebook, two codes per byte ("Encoding strategy:
  *     Fixed-length coding");
  *   - the sign and mantissa bits, stored raw ("Sign/mantissa preservation";
- *     FP8-E5M2 per Contributions 4);
+ *     FP8-E5M2 per Contributions 4; FP16, one of the other formats the page's
+ *     Significance section points to, is this library's extension);
  *   - a sparse escape stream of (16-bit in-chunk position, 8-bit exponent)
  *     for exponents outside the codebook ("Escape stream").
  * Decoding maps every code back through a 16-entry table and then overwrites
@@ -25,8 +26,8 @@
  *     the GPU are written to *d_status (a device int) in stream order.
  *   - Device pointers must be 16-byte aligned (SPLITZIP_ERR_INVALID_ARG
  *     otherwise).
- *   - Elements are raw bits: BF16 as 16-bit little-endian words, FP8-E5M2 as
- *     bytes.  No value is special: NaN, inf, signed zeros and subnormals round
+ *   - Elements are raw bits: BF16 and FP16 as 16-bit little-endian words,
+ *     FP8-E5M2 as bytes.  No value is special: NaN, inf, signed zeros and subnormals round
  *     trip bit for bit.
  *   - On any error the contents of output buffers are unspecified, but no
  *     access is made outside the buffers at the sizes passed in.
@@ -48,13 +49,15 @@
  *   A16     sign|mantissa stream: BF16 one byte per element,
  *           (sign << 7) | mantissa7; FP8-E5M2 3 bits per element,
  *           (sign << 2) | mantissa2, LSB-first bitstream, element i at bits
- *           [3i, 3i+3), padded with zero bits to 3*ceil(n/8) bytes
+ *           [3i, 3i+3), padded with zero bits to 3*ceil(n/8) bytes; FP16 11
+ *           bits per element, (sign << 10) | mantissa10, the same way at bits
+ *           [11i, 11i+11), 11*ceil(n/8) bytes
  *   A16     escape records, 3 bytes each: the in-chunk position (u16,
- *           little-endian) then the original exponent (u8; E5M2: the 5-bit
- *           exponent zero-extended); chunk by chunk, ascending position
- *           within a chunk; the container ends after the last record.
+ *           little-endian) then the original exponent (u8; E5M2 and FP16:
+ *           the 5-bit exponent zero-extended); chunk by chunk, ascending
+ *           position within a chunk; the container ends after the last record.
  * Size = A16(64 + 12C) + A16(ceil(n/2)) + A16(S) + 3E, A16 = round up to 16,
- * S = n (BF16) or 3*ceil(n/8) (FP8-E5M2).
+ * S = n (BF16), 3*ceil(n/8) (FP8-E5M2) or 11*ceil(n/8) (FP16).
  * chunk_elems is a power of two in [64, 65536] (the 16-bit position field of
  * the escape records bounds it; the page uses 65,536-element chunks).
  */
@@ -70,7 +73,8 @@ extern "C" {
 
 typedef enum {
     SPLITZIP_BF16 = 0,      /* bfloat16: 1 sign, 8 exponent, 7 mantissa bits */
-    SPLITZIP_FP8_E5M2 = 1   /* FP8-E5M2: 1 sign, 5 exponent, 2 mantissa bits */
+    SPLITZIP_FP8_E5M2 = 1,  /* FP8-E5M2: 1 sign, 5 exponent, 2 mantissa bits */
+    SPLITZIP_FP16 = 2       /* IEEE half: 1 sign, 5 exponent, 10 mantissa bits */
 } splitzip_dtype_t;
 
 typedef enum {
@@ -87,7 +91,7 @@ typedef enum {
 #define SPLITZIP_HEADER_BYTES 64u
 
 /* Top-16 codebook: code i stands for exponent exps[i].  The 16 values must be
- * distinct and below 256 (BF16) or 32 (FP8-E5M2). */
+ * distinct and below 256 (BF16) or 32 (FP8-E5M2, FP16). */
 typedef struct {
     uint8_t dtype;    /* splitzip_dtype_t */
     uint8_t exps[16];
@@ -111,7 +115,7 @@ const char* splitzip_status_string(int status);
 /* Exponent histogram of n elements (Results, "Ablations: Calibration": the
  * codebook is calibrated offline from exponent statistics).
  * d_x: n elements of `dtype`; d_hist256: 256 u64 counts, overwritten (bins
- * 32..255 stay 0 for FP8-E5M2).  Enqueued on `stream`. */
+ * 32..255 stay 0 for FP8-E5M2 and FP16).  Enqueued on `stream`. */
 int splitzip_exponent_histogram(const void* d_x, uint64_t n, int dtype, uint64_t* d_hist256,
                                 cudaStream_t stream);
 
@@ -124,7 +128,7 @@ int splitzip_exponent_histogram(const void* d_x, uint64_t n, int dtype, uint64_t
  * all work queued on every stream of the device has finished (so a histogram
  * that splitzip_exponent_histogram enqueued on any stream, non-blocking
  * streams included, is complete) and copies the 256 counts to the host.
- * FP8-E5M2 histograms with counts in bins >= 32 are rejected. */
+ * FP8-E5M2 and FP16 histograms with counts in bins >= 32 are rejected. */
 int splitzip_calibrate(const uint64_t* hist256, int hist_is_device, int dtype,
                        splitzip_codebook_t* out_cb);
 
@@ -137,8 +141,8 @@ int splitzip_compressed_size(uint64_t n, int dtype, uint32_t chunk_elems, uint64
 int splitzip_max_compressed_size(uint64_t n, int dtype, uint32_t chunk_elems, uint64_t* out_bytes);
 
 /* Device scratch bytes splitzip_encode needs for n elements: about 4 bytes
- * per element (each tile of 16 KB of input -- 8,192 BF16 or 16,384 E5M2
- * elements -- or each chunk when chunks are smaller, has a staging slot big
+ * per element (each tile of 16 KB of input -- 8,192 BF16 / FP16 or 16,384
+ * E5M2 elements -- or each chunk when chunks are smaller, has a staging slot big
  * enough for all of its elements to escape) plus 40 bytes per tile and 4 per
  * 256 tiles. */
 int splitzip_encode_workspace_size(uint64_t n, int dtype, uint32_t chunk_elems, uint64_t* out_bytes);
@@ -230,8 +234,8 @@ int splitzip_decode(const void* d_in, uint64_t in_bytes, void* d_out, uint64_t n
  * splitzip_encode_paged encodes the n_pages * page_elems elements of those
  * pages, gathered by the encoder's tensor-map copies straight from the pool:
  * the container is byte-identical to splitzip_encode of the gathered tensor.
- * page_elems must be a multiple of the encoder's tile (8,192 BF16 or 16,384
- * E5M2 elements, or chunk_elems when that is smaller).  The workspace and
+ * page_elems must be a multiple of the encoder's tile (8,192 BF16 / FP16 or
+ * 16,384 E5M2 elements, or chunk_elems when that is smaller).  The workspace and
  * output sizes are those of n = n_pages * page_elems elements.  A page index
  * outside [0, pool_pages) is reported in *d_status as
  * SPLITZIP_ERR_INVALID_ARG (and never read). */

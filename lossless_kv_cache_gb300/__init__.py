@@ -19,6 +19,7 @@ LIB_PATH = os.path.join(_HERE, "libsplitzip.so")
 
 BF16 = 0
 FP8_E5M2 = 1
+FP16 = 2
 OK, ERR_INVALID_ARG, ERR_CAPACITY, ERR_CORRUPT, ERR_CUDA, ERR_TIMEOUT, ERR_UNSUPPORTED = range(7)
 DEFAULT_CHUNK_ELEMS = 65536
 HEADER_BYTES = 64
@@ -306,7 +307,7 @@ def _stream_handle(stream):
 
 def _bits_dtype(dtype):
     torch = _torch()
-    return torch.int16 if dtype == BF16 else torch.uint8
+    return torch.uint8 if dtype == FP8_E5M2 else torch.int16
 
 
 def _check(st, where):

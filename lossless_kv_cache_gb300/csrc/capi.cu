@@ -20,7 +20,7 @@ struct DeviceState {
     bool ready;
     int status;
     int sms;
-    int encode_bpsm[2], decode_bpsm[2], hist_bpsm[2];
+    int encode_bpsm[3], decode_bpsm[3], hist_bpsm[3];  // per dtype
 };
 
 std::mutex g_mutex;
@@ -46,7 +46,7 @@ int device_state(DeviceState* out) {
         if (major != 10 || minor != 3) {
             d.status = SPLITZIP_ERR_UNSUPPORTED;  // the kernels are built for sm_103a only
         } else {
-            for (int t = 0; t < 2; ++t) {
+            for (int t = 0; t < 3; ++t) {
                 if (occupancy_encode(&d.encode_bpsm[t], t) != cudaSuccess ||
                     occupancy_decode(&d.decode_bpsm[t], t) != cudaSuccess ||
                     occupancy_histogram(&d.hist_bpsm[t], t) != cudaSuccess) {
@@ -62,7 +62,7 @@ int device_state(DeviceState* out) {
 }
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
-bool valid_dtype(int dtype) { return dtype == SPLITZIP_BF16 || dtype == SPLITZIP_FP8_E5M2; }
+bool valid_dtype(int dtype) { return dtype == SPLITZIP_BF16 || dtype == SPLITZIP_FP8_E5M2 || dtype == SPLITZIP_FP16; }
 bool valid_chunk(uint32_t c) { return c >= kMinChunk && c <= kMaxChunk && (c & (c - 1u)) == 0u; }
 uint32_t exponent_bins(int dtype) { return dtype == SPLITZIP_BF16 ? 256u : 32u; }
 
@@ -173,7 +173,7 @@ int make_input_map(const void* d_in, int dtype, EncodeArgs* a, CUtensorMap* map,
     const cuuint32_t box[2] = {cuuint32_t(box_row_bytes / eb), cuuint32_t(tile_bytes / box_row_bytes)};
     const cuuint32_t elem_strides[2] = {1u, 1u};
     const CUresult r =
-        encode(map, dtype == SPLITZIP_BF16 ? CU_TENSOR_MAP_DATA_TYPE_UINT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 2,
+        encode(map, eb == 2 ? CU_TENSOR_MAP_DATA_TYPE_UINT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 2,
                const_cast<void*>(d_in), dims, strides, box, elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE,
                box_row_bytes == 128u ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -263,7 +263,7 @@ int splitzip_exponent_histogram(const void* d_x, uint64_t n, int dtype, uint64_t
     }
     if (n == 0) return SPLITZIP_OK;
     const uint64_t vec_per_block = uint64_t(kHistThreads);
-    const uint64_t vecs = n * (dtype == SPLITZIP_BF16 ? 2 : 1) / 16;
+    const uint64_t vecs = n * elem_bytes(dtype) / 16;
     const int grid = grid_for((vecs + vec_per_block - 1) / vec_per_block, d.sms, d.hist_bpsm[dtype]);
     return launch_histogram(d_x, n, dtype, reinterpret_cast<unsigned long long*>(d_hist256), grid, stream) ==
                    cudaSuccess

@@ -99,6 +99,27 @@ __device__ __forceinline__ uint32_t merge_e5m2(uint32_t g, uint32_t e) {
     return t * 32u + ((y & 0x00030003u) | e);
 }
 
+// FP16: a 22-bit pair value p (s11 of the even element | s11 of the odd one
+// << 11) and both elements' exponents e already at bits 10..14 and 26..30 give
+// the output word: mantissas stay at bits 0..9 / move to 16..25, signs move
+// from bits 10 and 21 to 15 and 31 (fields never overlap).
+__device__ __forceinline__ uint32_t merge_fp16(uint32_t p, uint32_t e) {
+    return e | (p & 0x3FFu) | ((p << 5) & 0x03FF8000u) | ((p << 10) & 0x80000000u);
+}
+
+// FP16: 8 elements from 8 codes (one nibble word) and the unit's 88 bits of
+// s11 (f0, f1, f2 = the 96 bits from the unit's first byte): pair k sits at
+// bits [22k, 22k + 22).  lut4 maps a nibble byte to both exponents in place.
+__device__ __forceinline__ uint4 decode_unit_fp16(uint32_t nib, uint32_t f0, uint32_t f1, uint32_t f2,
+                                                  const uint32_t* lut4) {
+    const uint32_t p0 = f0 & 0x3FFFFFu;
+    const uint32_t p1 = __funnelshift_r(f0, f1, 22) & 0x3FFFFFu;
+    const uint32_t p2 = __funnelshift_r(f1, f2, 12) & 0x3FFFFFu;
+    const uint32_t p3 = (f2 >> 2) & 0x3FFFFFu;
+    return make_uint4(merge_fp16(p0, lut4[nib & 0xFFu]), merge_fp16(p1, lut4[(nib >> 8) & 0xFFu]),
+                      merge_fp16(p2, lut4[(nib >> 16) & 0xFFu]), merge_fp16(p3, lut4[nib >> 24]));
+}
+
 __device__ __forceinline__ uint16_t lut_at(const uint16_t* lut2, uint32_t byte) {
     return *reinterpret_cast<const uint16_t*>(reinterpret_cast<const uint8_t*>(lut2) + 2u * byte);
 }
@@ -131,11 +152,14 @@ constexpr int kBlock = kConsumers + 32;  // + one producer warp
 // copies in flight while one decodes (BF16 1.21 ms vs 1.27 ms with four
 // 8,192-element stages at 2 CTAs; E5M2 1.44 ms vs 1.63 ms with four
 // 8,192-element stages, 1.44 ms at 32,768 elements and 2 CTAs).
-template <int DT> constexpr int kStages = DT == SPLITZIP_BF16 ? 1 : 2;
+// FP16 (8 nibble + 22 sign|mantissa KB a sub-tile) takes BF16's single stage.
+template <int DT> constexpr int kStages = DT == SPLITZIP_FP8_E5M2 ? 2 : 1;
 template <int DT> constexpr uint32_t kSub = 16384u;
 template <int DT> constexpr uint32_t kNibCap = kSub<DT> / 2 + 32;  // + room for a 16-byte window shift
-// sign|mantissa bytes of a sub-tile: BF16 one per element, E5M2 3 per 8 elements
-template <int DT> constexpr uint32_t kSmCap = (DT == SPLITZIP_BF16 ? kSub<DT> : 3 * kSub<DT> / 8) + 32;
+// sign|mantissa bytes of a sub-tile: BF16 one per element, E5M2 3 and FP16
+// 11 per 8 elements
+template <int DT> constexpr uint32_t kSmCap =
+    (DT == SPLITZIP_BF16 ? kSub<DT> : (DT == SPLITZIP_FP16 ? 11 : 3) * kSub<DT> / 8) + 32;
 template <int DT> constexpr uint32_t kStageBytes = (kNibCap<DT> + kSmCap<DT> + 127u) & ~127u;
 template <int DT> constexpr uint32_t kRingBytes = kStages<DT> * kStageBytes<DT>;
 // A chunk's escape records are brought into shared memory with one bulk copy
@@ -145,7 +169,7 @@ template <int DT> constexpr uint32_t kRingBytes = kStages<DT> * kStageBytes<DT>;
 // a chunk with more escapes reads them from the escape stream instead.  Either
 // way each sub-tile is patched right after its stores, while its lines are
 // still in L2.
-template <int DT> constexpr uint32_t kRecCap = DT == SPLITZIP_BF16 ? 8192u : 7680u;
+template <int DT> constexpr uint32_t kRecCap = DT == SPLITZIP_BF16 ? 8192u : DT == SPLITZIP_FP16 ? 6144u : 7680u;
 // resident CTAs per SM the kernel is compiled for (register budget)
 template <int DT> constexpr int kDecodeMinBlocks = 3;
 // per buffer: 3 bytes a record + room for a 16-byte window shift
@@ -155,6 +179,7 @@ template <int DT> constexpr uint32_t kDecodeSmem = kRingBytes<DT> + 2 * kRecByte
 // the CTAs of one SM share its 228 KB (each also takes ~1 KB static + 1 KB reserved)
 static_assert(kDecodeMinBlocks<SPLITZIP_BF16> * (kDecodeSmem<SPLITZIP_BF16> + 2048) <= 228 * 1024, "smem");
 static_assert(kDecodeMinBlocks<SPLITZIP_FP8_E5M2> * (kDecodeSmem<SPLITZIP_FP8_E5M2> + 2048) <= 228 * 1024, "smem");
+static_assert(kDecodeMinBlocks<SPLITZIP_FP16> * (kDecodeSmem<SPLITZIP_FP16> + 3072) <= 228 * 1024, "smem");
 
 struct SubTile {
     Window nib, sm;
@@ -167,6 +192,8 @@ __device__ __forceinline__ SubTile subtile_windows(const uint8_t* nibbles, const
     t.nib = window_of(nibbles + g / 2, (cnt + 1u) / 2u);
     if constexpr (DT == SPLITZIP_BF16)
         t.sm = window_of(signmant + g, cnt);
+    else if constexpr (DT == SPLITZIP_FP16)
+        t.sm = window_of(signmant + g / 8u * 11u, 11u * ((cnt + 7u) / 8u));
     else
         t.sm = window_of(signmant + g / 8u * 3u, 3u * ((cnt + 7u) / 8u));
     return t;
@@ -204,11 +231,22 @@ struct OutMap {
     }
 };
 
+// FP16: the 96 bits from smem byte address a (four aligned words, shifted)
+__device__ __forceinline__ void load96(const uint8_t* a, uint32_t& f0, uint32_t& f1, uint32_t& f2) {
+    const uint32_t* w = reinterpret_cast<const uint32_t*>(reinterpret_cast<uintptr_t>(a) & ~uintptr_t(3));
+    const uint32_t sh = 8u * uint32_t(reinterpret_cast<uintptr_t>(a) & 3u);
+    const uint32_t w0 = w[0], w1 = w[1], w2 = w[2], w3 = w[3];
+    f0 = __funnelshift_r(w0, w1, sh);
+    f1 = __funnelshift_r(w1, w2, sh);
+    f2 = __funnelshift_r(w2, w3, sh);
+}
+
 template <int DT, bool PAGED>
 __device__ __forceinline__ void decode_subtile(const uint8_t* nb, const uint8_t* sb, const OutMap<PAGED>& om,
-                                               uint64_t g, uint32_t cnt, int tid, const uint16_t* lut2) {
-    constexpr uint32_t EB = DT == SPLITZIP_BF16 ? 2u : 1u;
-    constexpr uint32_t UE = DT == SPLITZIP_BF16 ? 8u : 16u;
+                                               uint64_t g, uint32_t cnt, int tid, const uint16_t* lut2,
+                                               const uint32_t* lut4) {
+    constexpr uint32_t EB = DT == SPLITZIP_FP8_E5M2 ? 1u : 2u;
+    constexpr uint32_t UE = DT == SPLITZIP_FP8_E5M2 ? 16u : 8u;
     const uint32_t units = (cnt + UE - 1u) / UE;
     const uint32_t rounds = (units + kConsumers - 1u) / kConsumers;
 #pragma unroll 2
@@ -221,6 +259,12 @@ __device__ __forceinline__ void decode_subtile(const uint8_t* nb, const uint8_t*
                 const uint32_t nib = *reinterpret_cast<const uint32_t*>(nb + e / 2);
                 const uint2 sm = *reinterpret_cast<const uint2*>(sb + e);
                 o = decode_unit_bf16(nib, sm, lut2);
+            } else if constexpr (DT == SPLITZIP_FP16) {
+                // 11 bytes of s11 per unit, at any byte of the stage
+                const uint32_t nib = *reinterpret_cast<const uint32_t*>(nb + e / 2);
+                uint32_t f0, f1, f2;
+                load96(sb + 11u * u, f0, f1, f2);
+                o = decode_unit_fp16(nib, f0, f1, f2, lut4);
             } else {
                 // 6 bytes of s3 per unit, 2-byte aligned in the stage
                 const uint16_t* s16 = reinterpret_cast<const uint16_t*>(sb + 6u * u);
@@ -239,6 +283,12 @@ __device__ __forceinline__ void decode_subtile(const uint8_t* nb, const uint8_t*
                 for (uint32_t b = 0; b < (valid + 1u) / 2u; ++b) nib |= uint32_t(nb[e / 2 + b]) << (8u * b);
                 for (uint32_t b = 0; b < valid; ++b) smw |= uint64_t(sb[e + b]) << (8u * b);
                 o = decode_unit_bf16(nib, make_uint2(uint32_t(smw), uint32_t(smw >> 32)), lut2);
+            } else if constexpr (DT == SPLITZIP_FP16) {
+                uint32_t nib = 0, f[3] = {0u, 0u, 0u};
+                for (uint32_t b = 0; b < (valid + 1u) / 2u; ++b) nib |= uint32_t(nb[e / 2 + b]) << (8u * b);
+                const uint8_t* s8 = sb + 11u * u;
+                for (uint32_t b = 0; b < 11u; ++b) f[b >> 2] |= uint32_t(s8[b]) << (8u * (b & 3u));
+                o = decode_unit_fp16(nib, f[0], f[1], f[2], lut4);
             } else {
                 uint64_t nw = 0, sw = 0;
                 for (uint32_t b = 0; b < (valid + 1u) / 2u; ++b) nw |= uint64_t(nb[e / 2 + b]) << (8u * b);
@@ -250,9 +300,9 @@ __device__ __forceinline__ void decode_subtile(const uint8_t* nb, const uint8_t*
             uint64_t off;
             if (om.at(g + e, EB, off)) {
                 for (uint32_t b = 0; b < valid; ++b) {
-                    const uint32_t q = DT == SPLITZIP_BF16 ? b >> 1 : b >> 2;
+                    const uint32_t q = EB == 2 ? b >> 1 : b >> 2;
                     const uint32_t w = q == 0 ? o.x : q == 1 ? o.y : q == 2 ? o.z : o.w;
-                    if constexpr (DT == SPLITZIP_BF16)
+                    if constexpr (EB == 2)
                         reinterpret_cast<uint16_t*>(om.base + off)[b] = uint16_t(w >> (16u * (b & 1u)));
                     else
                         (om.base + off)[b] = uint8_t(w >> (8u * (b & 3u)));
@@ -274,12 +324,14 @@ template <int DT, bool PAGED>
 __device__ __forceinline__ bool patch_one(const OutMap<PAGED>& om, uint64_t base, uint32_t len, int64_t prev,
                                           uint32_t pos, uint32_t ex) {
     if (pos >= len || int64_t(pos) <= prev || ex >= (DT == SPLITZIP_BF16 ? 256u : 32u)) return false;
-    constexpr uint32_t EB = DT == SPLITZIP_BF16 ? 2u : 1u;
+    constexpr uint32_t EB = DT == SPLITZIP_FP8_E5M2 ? 1u : 2u;
+    // bit of the exponent field within a 16-bit (BF16, FP16) or 8-bit element
+    constexpr uint32_t kExpShift = DT == SPLITZIP_BF16 ? 7u : DT == SPLITZIP_FP16 ? 10u : 2u;
     uint64_t byte;
     if (!om.at(base + pos, EB, byte)) return true;  // (reported: a page outside the pool)
     uint8_t* o = om.base;
     if ((byte | 3u) < om.limit) {
-        const uint32_t sh = uint32_t(byte & 3u) * 8u + (DT == SPLITZIP_BF16 ? 7u : 2u);
+        const uint32_t sh = uint32_t(byte & 3u) * 8u + kExpShift;
         const uint32_t field = (DT == SPLITZIP_BF16 ? 0xFFu : 0x1Fu) << sh;
         unsigned int* w = reinterpret_cast<unsigned int*>(o + (byte & ~uint64_t(3)));
         atomicAnd(w, ~field);
@@ -287,6 +339,9 @@ __device__ __forceinline__ bool patch_one(const OutMap<PAGED>& om, uint64_t base
     } else if constexpr (DT == SPLITZIP_BF16) {
         uint16_t* e = reinterpret_cast<uint16_t*>(o + byte);
         *e = uint16_t((*e & 0x807Fu) | (ex << 7));
+    } else if constexpr (DT == SPLITZIP_FP16) {
+        uint16_t* e = reinterpret_cast<uint16_t*>(o + byte);
+        *e = uint16_t((*e & 0x83FFu) | (ex << 10));
     } else {
         o[byte] = uint8_t((o[byte] & 0x83u) | (ex << 2));
     }
@@ -310,6 +365,8 @@ __global__ void __launch_bounds__(kBlock, kDecodeMinBlocks<DT>) decode_kernel(co
     // nibble byte -> (exponent of low code) | (exponent of high code) << 8,
     // both shifted left by 2 for E5M2 (their place in the output byte)
     __shared__ uint16_t lut2[256];
+    // FP16: nibble byte -> (exponent of low code) << 10 | (of high code) << 26
+    __shared__ uint32_t lut4[DT == SPLITZIP_FP16 ? 256 : 1];
     constexpr uint32_t kNoRecords = 0xFFFFFFFFu;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -328,8 +385,12 @@ __global__ void __launch_bounds__(kBlock, kDecodeMinBlocks<DT>) decode_kernel(co
     }
     __syncthreads();
     if (!header_ok) return;
-    for (int b = tid; b < 256; b += kBlock)
-        lut2[b] = uint16_t((hdr.codebook[b & 15] | (hdr.codebook[b >> 4] << 8)) << (DT == SPLITZIP_BF16 ? 0 : 2));
+    for (int b = tid; b < 256; b += kBlock) {
+        if constexpr (DT == SPLITZIP_FP16)
+            lut4[b] = (uint32_t(hdr.codebook[b & 15]) << 10) | (uint32_t(hdr.codebook[b >> 4]) << 26);
+        else
+            lut2[b] = uint16_t((hdr.codebook[b & 15] | (hdr.codebook[b >> 4] << 8)) << (DT == SPLITZIP_BF16 ? 0 : 2));
+    }
     __syncthreads();
 
     const uint8_t* in = a.in;
@@ -340,7 +401,7 @@ __global__ void __launch_bounds__(kBlock, kDecodeMinBlocks<DT>) decode_kernel(co
     const uint32_t* counts = reinterpret_cast<const uint32_t*>(in + L.counts_off);
     const uint8_t* records = in + L.escrec_off;  // 3 bytes each: position u16 LE, exponent
     const uint64_t chunk = hdr.chunk, C = hdr.n_chunks, E = hdr.E;
-    const uint32_t EBo = DT == SPLITZIP_BF16 ? 2u : 1u;
+    const uint32_t EBo = DT == SPLITZIP_FP8_E5M2 ? 1u : 2u;
     const OutMap<PAGED> om{static_cast<uint8_t*>(a.out),
                            PAGED ? (a.pool_pages << a.page_shift) * EBo : a.n * EBo,
                            a.pages, a.pool_pages, a.page_shift, a.status};
@@ -431,7 +492,7 @@ __global__ void __launch_bounds__(kBlock, kDecodeMinBlocks<DT>) decode_kernel(co
             const SubTile t = subtile_windows<DT>(nibbles, signmant, base + s0, n_sub);
             const uint8_t* src = stages + stage * kStageBytes<DT>;
             decode_subtile<DT, PAGED>(src + t.nib.offset, src + kNibCap<DT> + t.sm.offset, om, base + s0, n_sub, tid,
-                                      lut2);
+                                      lut2, lut4);
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty_bar[stage]);
             if (!patch) continue;
@@ -457,6 +518,11 @@ cudaError_t launch_decode(const DecodeArgs& a, int grid, cudaStream_t s) {
             decode_kernel<SPLITZIP_BF16, true><<<grid, kBlock, kDecodeSmem<SPLITZIP_BF16>, s>>>(a);
         else
             decode_kernel<SPLITZIP_BF16, false><<<grid, kBlock, kDecodeSmem<SPLITZIP_BF16>, s>>>(a);
+    } else if (a.dtype == SPLITZIP_FP16) {
+        if (paged)
+            decode_kernel<SPLITZIP_FP16, true><<<grid, kBlock, kDecodeSmem<SPLITZIP_FP16>, s>>>(a);
+        else
+            decode_kernel<SPLITZIP_FP16, false><<<grid, kBlock, kDecodeSmem<SPLITZIP_FP16>, s>>>(a);
     } else {
         if (paged)
             decode_kernel<SPLITZIP_FP8_E5M2, true><<<grid, kBlock, kDecodeSmem<SPLITZIP_FP8_E5M2>, s>>>(a);
@@ -470,10 +536,13 @@ cudaError_t launch_decode(const DecodeArgs& a, int grid, cudaStream_t s) {
 // the contiguous and the paged instances); the occupancy is the contiguous
 // instance's.
 cudaError_t occupancy_decode(int* blocks_per_sm, int dtype) {
-    const bool bf16 = dtype == SPLITZIP_BF16;
-    auto k = bf16 ? decode_kernel<SPLITZIP_BF16, false> : decode_kernel<SPLITZIP_FP8_E5M2, false>;
-    auto kp = bf16 ? decode_kernel<SPLITZIP_BF16, true> : decode_kernel<SPLITZIP_FP8_E5M2, true>;
-    const int smem = int(bf16 ? kDecodeSmem<SPLITZIP_BF16> : kDecodeSmem<SPLITZIP_FP8_E5M2>);
+    const bool bf16 = dtype == SPLITZIP_BF16, fp16 = dtype == SPLITZIP_FP16;
+    auto k = bf16 ? decode_kernel<SPLITZIP_BF16, false>
+             : fp16 ? decode_kernel<SPLITZIP_FP16, false> : decode_kernel<SPLITZIP_FP8_E5M2, false>;
+    auto kp = bf16 ? decode_kernel<SPLITZIP_BF16, true>
+              : fp16 ? decode_kernel<SPLITZIP_FP16, true> : decode_kernel<SPLITZIP_FP8_E5M2, true>;
+    const int smem = int(bf16 ? kDecodeSmem<SPLITZIP_BF16>
+                         : fp16 ? kDecodeSmem<SPLITZIP_FP16> : kDecodeSmem<SPLITZIP_FP8_E5M2>);
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(kp, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;

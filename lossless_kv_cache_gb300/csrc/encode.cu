@@ -46,8 +46,9 @@ constexpr uint32_t kStageBytes = kTileBytes;
 // the 2.1 G-element BF16 and 4.3 G-element E5M2 caches: BF16 runs fastest as
 // one CTA per SM with an 8-stage ring (1.18 ms; 1.25-1.28 ms at 2 or 3 CTAs),
 // E5M2 with 2 CTAs of 4 stages (1.50 ms; 1.84 ms at one CTA).
-template <int DT> constexpr int kStages = DT == SPLITZIP_BF16 ? 8 : 4;
-template <int DT> constexpr int kMinBlocks = DT == SPLITZIP_BF16 ? 1 : 2;
+// FP16 (two bytes an element, like BF16) takes BF16's shape.
+template <int DT> constexpr int kStages = DT == SPLITZIP_FP8_E5M2 ? 4 : 8;
+template <int DT> constexpr int kMinBlocks = DT == SPLITZIP_FP8_E5M2 ? 2 : 1;
 // + room to align the ring to 1024 bytes, which the 128-byte swizzle needs
 template <int DT> constexpr uint32_t kEncodeSmem = kStages<DT> * kStageBytes + 1024;
 constexpr int kFinishThreads = kGroupTiles;  // one thread per tile of the group
@@ -58,7 +59,7 @@ static_assert(kConsumers * kThreadBytes == kTileBytes, "one tile = 64 bytes per 
 //   bits 16 + 4k .. 19 + 4k  the element's code (0 when it escapes)
 //   bit  12 + k              the element's escape flag
 //   bits 3k .. 3k + 1        E5M2 only: the element's 2 mantissa bits
-// BF16 tables are indexed by the exponent, E5M2 tables by the byte without
+// BF16 and FP16 tables are indexed by the exponent, E5M2 tables by the byte without
 // its sign (exponent and mantissa: 128 entries, so elements that differ only
 // in sign hit the same entry instead of another bank).  The four entries of a
 // group have disjoint bits, so their sum -- plus, for E5M2, the four sign bits
@@ -67,7 +68,7 @@ static_assert(kConsumers * kThreadBytes == kTileBytes, "one tile = 64 bytes per 
 // packed 3-bit sign|mantissa values (bits 0..11).
 __device__ __forceinline__ uint32_t table_entry(int dtype, int k, uint32_t index, const uint8_t* code) {
     uint32_t e = index, s3 = 0;
-    if (dtype != SPLITZIP_BF16) {  // index = exponent << 2 | mantissa
+    if (dtype == SPLITZIP_FP8_E5M2) {  // index = exponent << 2 | mantissa
         e = (index >> 2) & 31u;
         s3 = index & 3u;
     }
@@ -86,6 +87,13 @@ __device__ __forceinline__ uint32_t tab_at(const uint32_t* tab, int k, uint32_t 
 __device__ __forceinline__ uint32_t group_bf16(const uint32_t* tab, uint32_t x, uint32_t y) {
     return tab_at(tab, 0, (x >> 5) & 0x3FCu) + tab_at(tab, 1, (x >> 21) & 0x3FCu) +
            tab_at(tab, 2, (y >> 5) & 0x3FCu) + tab_at(tab, 3, (y >> 21) & 0x3FCu);
+}
+
+// FP16: the group of four elements in words x (elements 0, 1) and y (2, 3);
+// the table index is the exponent (bits 10..14 of each 16-bit element).
+__device__ __forceinline__ uint32_t group_fp16(const uint32_t* tab, uint32_t x, uint32_t y) {
+    return tab_at(tab, 0, (x >> 8) & 0x7Cu) + tab_at(tab, 1, (x >> 24) & 0x7Cu) +
+           tab_at(tab, 2, (y >> 8) & 0x7Cu) + tab_at(tab, 3, (y >> 24) & 0x7Cu);
 }
 
 // E5M2: the group of four elements in word w.  The sign of byte k (bit
@@ -150,6 +158,12 @@ template <> struct ThreadOut<SPLITZIP_BF16> {
     uint32_t sm[8];   // 32 sign|mantissa bytes
     uint32_t mask;    // escape flags, bit b = element b
 };
+template <> struct ThreadOut<SPLITZIP_FP16> {
+    static constexpr uint32_t kElems = 32;
+    uint32_t nib[4];  // 16 nibble bytes
+    uint32_t sm[11];  // 44 bytes: 32 sign|mantissa fields of 11 bits, LSB-first
+    uint32_t mask;
+};
 template <> struct ThreadOut<SPLITZIP_FP8_E5M2> {
     static constexpr uint32_t kElems = 64;
     uint32_t nib[8];  // 32 nibble bytes
@@ -167,6 +181,28 @@ __device__ __forceinline__ void encode_piece(const uint32_t* tab, uint4 v, int i
     const uint32_t lo1 = __byte_perm(v.z, v.w, 0x6420), hi1 = __byte_perm(v.z, v.w, 0x7531);
     o.sm[2 * i] = (hi0 & 0x80808080u) | (lo0 & 0x7F7F7F7Fu);
     o.sm[2 * i + 1] = (hi1 & 0x80808080u) | (lo1 & 0x7F7F7F7Fu);
+}
+
+// One 16-byte piece (FP16: 8 elements) into slot i of the thread's results.
+// The sign|mantissa fields of a word's two elements form one 22-bit value
+// (s11 of the even element | s11 of the odd one << 11): the even element's
+// sign (bit 15) moves to bit 10 and the odd element's mantissa (bits 16..25)
+// to bits 11..20 with the same shift by 5, its sign (bit 31) to bit 21.  Pair
+// j of the thread's 16 lands at bit 22 j of its 352-bit run (o.sm, zeroed by
+// the caller), possibly across two words.
+__device__ __forceinline__ void encode_piece(const uint32_t* tab, uint4 v, int i, ThreadOut<SPLITZIP_FP16>& o) {
+    const uint32_t s0 = group_fp16(tab, v.x, v.y), s1 = group_fp16(tab, v.z, v.w);
+    o.nib[i] = __byte_perm(s0, s1, 0x7632);
+    o.mask |= (((s0 >> 12) & 0xFu) | ((s1 >> 8) & 0xF0u)) << (8 * i);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const uint32_t x = w[j];
+        const uint32_t pair = (x & 0x3FFu) | ((x >> 5) & 0x1FFC00u) | ((x >> 10) & 0x200000u);
+        const int bit = 22 * (4 * i + j);
+        o.sm[bit >> 5] |= pair << (bit & 31);
+        if ((bit & 31) > 10) o.sm[(bit >> 5) + 1] |= pair >> (32 - (bit & 31));
+    }
 }
 
 // One 16-byte piece (E5M2: 16 elements); the packed sign|mantissa of the
@@ -198,7 +234,7 @@ template <int DT>
 __global__ void __launch_bounds__(kBlock, kMinBlocks<DT>)
     encode_kernel(const __grid_constant__ EncodeArgs a, const __grid_constant__ CUtensorMap map,
                   const __grid_constant__ EncodeLut lut) {
-    constexpr uint32_t EB = DT == SPLITZIP_BF16 ? 2u : 1u;
+    constexpr uint32_t EB = DT == SPLITZIP_FP8_E5M2 ? 1u : 2u;
     using Out = ThreadOut<DT>;
     constexpr uint32_t TE = Out::kElems;  // elements per consumer thread per tile
     constexpr int kStages = splitzip::kStages<DT>;
@@ -318,10 +354,15 @@ __global__ void __launch_bounds__(kBlock, kMinBlocks<DT>)
             const uint32_t ne = FULL ? TE : (len > my_elem ? min(len - my_elem, TE) : 0u);
             Out o;
             [[maybe_unused]] uint32_t p[8];  // E5M2 packed sign|mantissa groups
-            if constexpr (DT == SPLITZIP_BF16)
+            if constexpr (DT == SPLITZIP_BF16) {
                 o.mask = 0u;
-            else
+            } else if constexpr (DT == SPLITZIP_FP16) {
+                o.mask = 0u;
+#pragma unroll
+                for (int k = 0; k < 11; ++k) o.sm[k] = 0u;
+            } else {
                 o.mask[0] = o.mask[1] = 0u;
+            }
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 uint4 v;
@@ -332,10 +373,10 @@ __global__ void __launch_bounds__(kBlock, kMinBlocks<DT>)
                     v = load_partial(in + tb + L, min(16u, len * EB - L));
                 else
                     v = make_uint4(0u, 0u, 0u, 0u);
-                if constexpr (DT == SPLITZIP_BF16)
-                    encode_piece(tab, v, i, o);
-                else
+                if constexpr (DT == SPLITZIP_FP8_E5M2)
                     encode_piece(tab, v, i, o, p);
+                else
+                    encode_piece(tab, v, i, o);
             }
 
             // ---- nibble and sign|mantissa streams ----
@@ -353,6 +394,24 @@ __global__ void __launch_bounds__(kBlock, kMinBlocks<DT>)
                         nb[b >> 1] = uint8_t(b + 1 < ne ? (w & 0xFFu) : (w & 0xFu));
                     }
                     for (uint32_t b = 0; b < ne; ++b) sb[b] = uint8_t(o.sm[b >> 2] >> (8 * (b & 3u)));
+                } else {
+                    o.mask = 0u;
+                }
+            } else if constexpr (DT == SPLITZIP_FP16) {
+                // 44 bytes from byte 44 t of the tile's run: 4-byte aligned
+                uint8_t* sb = signmant + (base + my_elem) / 8 * 11;
+                if (FULL || ne == TE) {
+                    __stcs(reinterpret_cast<uint4*>(nb), make_uint4(o.nib[0], o.nib[1], o.nib[2], o.nib[3]));
+#pragma unroll
+                    for (int k = 0; k < 11; ++k) __stcs(reinterpret_cast<unsigned int*>(sb) + k, o.sm[k]);
+                } else if (ne > 0u) {
+                    o.mask &= (1u << (ne & 31u)) - 1u;  // ne < 32 here
+                    for (uint32_t b = 0; b < ne; b += 2) {
+                        const uint32_t w = o.nib[b >> 3] >> (4 * (b & 7u));
+                        nb[b >> 1] = uint8_t(b + 1 < ne ? (w & 0xFFu) : (w & 0xFu));
+                    }
+                    // 11 bytes per started group of 8 elements (pad bits are 0)
+                    for (uint32_t b = 0; b < 11u * ((ne + 7u) / 8u); ++b) sb[b] = uint8_t(o.sm[b >> 2] >> (8 * (b & 3u)));
                 } else {
                     o.mask = 0u;
                 }
@@ -386,7 +445,7 @@ __global__ void __launch_bounds__(kBlock, kMinBlocks<DT>)
 
             // ---- the warp's escapes, in element order, to its staging region ----
             uint32_t cnt;
-            if constexpr (DT == SPLITZIP_BF16)
+            if constexpr (DT != SPLITZIP_FP8_E5M2)
                 cnt = __popc(o.mask);
             else
                 cnt = __popc(o.mask[0]) + __popc(o.mask[1]);
@@ -402,13 +461,14 @@ __global__ void __launch_bounds__(kBlock, kMinBlocks<DT>)
                 const uint32_t e = my_elem + b;  // element of the tile
                 const uint32_t B = e * EB;       // its first byte in the tile
                 if (FULL || B + EB <= in_stage)
-                    return DT == SPLITZIP_BF16 ? uint32_t(*reinterpret_cast<const uint16_t*>(st + swizzled(B)))
-                                               : uint32_t(st[swizzled(B)]);
-                return DT == SPLITZIP_BF16 ? uint32_t(reinterpret_cast<const uint16_t*>(in)[base + e])
-                                           : uint32_t(in[base + e]);
+                    return EB == 2 ? uint32_t(*reinterpret_cast<const uint16_t*>(st + swizzled(B)))
+                                   : uint32_t(st[swizzled(B)]);
+                return EB == 2 ? uint32_t(reinterpret_cast<const uint16_t*>(in)[base + e]) : uint32_t(in[base + e]);
             };
             auto record = [&](uint32_t b, uint32_t x) -> uint32_t {
-                const uint32_t exponent = DT == SPLITZIP_BF16 ? (x >> 7) & 0xFFu : (x >> 2) & 0x1Fu;
+                const uint32_t exponent = DT == SPLITZIP_BF16   ? (x >> 7) & 0xFFu
+                                          : DT == SPLITZIP_FP16 ? (x >> 10) & 0x1Fu
+                                                                : (x >> 2) & 0x1Fu;
                 return ((pos0 + my_elem + b) << 8) | exponent;
             };
             // the thread's escapes go contiguously into the warp's region of
@@ -416,9 +476,9 @@ __global__ void __launch_bounds__(kBlock, kMinBlocks<DT>)
             if (cnt) {
                 uint32_t* slot = a.staging + tile * a.tile_elems + uint32_t(warp) * (TE * 32u) + (incl - cnt);
 #pragma unroll
-                for (int h = 0; h < (DT == SPLITZIP_BF16 ? 1 : 2); ++h) {
+                for (int h = 0; h < (DT == SPLITZIP_FP8_E5M2 ? 2 : 1); ++h) {
                     uint32_t m;
-                    if constexpr (DT == SPLITZIP_BF16)
+                    if constexpr (DT != SPLITZIP_FP8_E5M2)
                         m = o.mask;
                     else
                         m = o.mask[h];
@@ -616,6 +676,8 @@ cudaError_t launch_encode(const EncodeArgs& a, const EncodeLut& lut, const CUten
                           cudaStream_t s) {
     if (a.dtype == SPLITZIP_BF16)
         encode_kernel<SPLITZIP_BF16><<<grid, kBlock, kEncodeSmem<SPLITZIP_BF16>, s>>>(a, map, lut);
+    else if (a.dtype == SPLITZIP_FP16)
+        encode_kernel<SPLITZIP_FP16><<<grid, kBlock, kEncodeSmem<SPLITZIP_FP16>, s>>>(a, map, lut);
     else
         encode_kernel<SPLITZIP_FP8_E5M2><<<grid, kBlock, kEncodeSmem<SPLITZIP_FP8_E5M2>, s>>>(a, map, lut);
     cudaError_t e = cudaGetLastError();
@@ -631,8 +693,12 @@ cudaError_t launch_encode(const EncodeArgs& a, const EncodeLut& lut, const CUten
 }
 
 cudaError_t occupancy_encode(int* blocks_per_sm, int dtype) {
-    auto k = dtype == SPLITZIP_BF16 ? encode_kernel<SPLITZIP_BF16> : encode_kernel<SPLITZIP_FP8_E5M2>;
-    const int smem = int(dtype == SPLITZIP_BF16 ? kEncodeSmem<SPLITZIP_BF16> : kEncodeSmem<SPLITZIP_FP8_E5M2>);
+    auto k = dtype == SPLITZIP_BF16   ? encode_kernel<SPLITZIP_BF16>
+             : dtype == SPLITZIP_FP16 ? encode_kernel<SPLITZIP_FP16>
+                                      : encode_kernel<SPLITZIP_FP8_E5M2>;
+    const int smem = int(dtype == SPLITZIP_BF16   ? kEncodeSmem<SPLITZIP_BF16>
+                         : dtype == SPLITZIP_FP16 ? kEncodeSmem<SPLITZIP_FP16>
+                                                  : kEncodeSmem<SPLITZIP_FP8_E5M2>);
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, k, kBlock, smem);

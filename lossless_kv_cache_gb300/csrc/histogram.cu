@@ -16,6 +16,9 @@ __device__ __forceinline__ void count_word(uint32_t w, uint32_t* h) {
     if constexpr (DT == SPLITZIP_BF16) {
         atomicAdd(&h[(w >> 7) & 0xFFu], 1u);
         atomicAdd(&h[(w >> 23) & 0xFFu], 1u);
+    } else if constexpr (DT == SPLITZIP_FP16) {
+        atomicAdd(&h[(w >> 10) & 0x1Fu], 1u);
+        atomicAdd(&h[(w >> 26) & 0x1Fu], 1u);
     } else {
 #pragma unroll
         for (int k = 0; k < 4; ++k) atomicAdd(&h[(w >> (8 * k + 2)) & 0x1Fu], 1u);
@@ -26,7 +29,7 @@ template <int DT>
 __global__ void __launch_bounds__(kHistThreads)
 histogram_kernel(const uint8_t* x, uint64_t n, unsigned long long* hist) {
     constexpr int kWarps = kHistThreads / 32;
-    constexpr uint64_t kElemBytes = DT == SPLITZIP_BF16 ? 2 : 1;
+    constexpr uint64_t kElemBytes = DT == SPLITZIP_FP8_E5M2 ? 1 : 2;
     __shared__ uint32_t h[kWarps][256];
     for (int i = threadIdx.x; i < kWarps * 256; i += kHistThreads) (&h[0][0])[i] = 0u;
     __syncthreads();
@@ -48,6 +51,9 @@ histogram_kernel(const uint8_t* x, uint64_t n, unsigned long long* hist) {
             if constexpr (DT == SPLITZIP_BF16) {
                 const uint32_t b = uint32_t(x[2 * i]) | (uint32_t(x[2 * i + 1]) << 8);
                 e = (b >> 7) & 0xFFu;
+            } else if constexpr (DT == SPLITZIP_FP16) {
+                const uint32_t b = uint32_t(x[2 * i]) | (uint32_t(x[2 * i + 1]) << 8);
+                e = (b >> 10) & 0x1Fu;
             } else {
                 e = (uint32_t(x[i]) >> 2) & 0x1Fu;
             }
@@ -94,6 +100,8 @@ cudaError_t launch_histogram(const void* x, uint64_t n, int dtype, unsigned long
     const uint8_t* p = static_cast<const uint8_t*>(x);
     if (dtype == SPLITZIP_BF16)
         histogram_kernel<SPLITZIP_BF16><<<grid, kHistThreads, 0, s>>>(p, n, hist);
+    else if (dtype == SPLITZIP_FP16)
+        histogram_kernel<SPLITZIP_FP16><<<grid, kHistThreads, 0, s>>>(p, n, hist);
     else
         histogram_kernel<SPLITZIP_FP8_E5M2><<<grid, kHistThreads, 0, s>>>(p, n, hist);
     return cudaGetLastError();
@@ -102,6 +110,9 @@ cudaError_t launch_histogram(const void* x, uint64_t n, int dtype, unsigned long
 cudaError_t occupancy_histogram(int* blocks_per_sm, int dtype) {
     if (dtype == SPLITZIP_BF16)
         return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, histogram_kernel<SPLITZIP_BF16>,
+                                                             kHistThreads, 0);
+    if (dtype == SPLITZIP_FP16)
+        return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, histogram_kernel<SPLITZIP_FP16>,
                                                              kHistThreads, 0);
     return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm,
                                                          histogram_kernel<SPLITZIP_FP8_E5M2>, kHistThreads, 0);

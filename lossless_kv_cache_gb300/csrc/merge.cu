@@ -108,8 +108,9 @@ extern "C" int splitzip_merge(const void* const* h_parts, const uint64_t* part_b
         // dense streams: every piece but the last holds whole chunks (a multiple
         // of 64 elements), so its bytes start on a byte boundary of the stream
         std::memcpy(o + L.nibble_off + elem0 / 2, p.b + h.nibble_off, (h.n_elems + 1) / 2);
-        const uint64_t sm_at = dtype == SPLITZIP_BF16 ? elem0 : elem0 / 8 * 3;
-        std::memcpy(o + L.signmant_off + sm_at, p.b + h.signmant_off, signmant_bytes(dtype, h.n_elems));
+        // (elem0 is a multiple of 8: the earlier pieces' streams end on whole bytes)
+        std::memcpy(o + L.signmant_off + signmant_bytes(dtype, elem0), p.b + h.signmant_off,
+                    signmant_bytes(dtype, h.n_elems));
         std::memcpy(o + L.escrec_off + 3 * esc0, p.b + h.escrec_off, 3 * h.total_escapes);
         chunk0 += h.n_chunks;
         elem0 += h.n_elems;

@@ -16,7 +16,7 @@ constexpr uint32_t kMinChunk = 64;
 constexpr uint32_t kMaxChunk = 65536;
 
 // Work decomposition of the encoder.  A tile is the unit of work of one
-// encode CTA trip: 16 KB of input (8,192 BF16 or 16,384 E5M2 elements), or the
+// encode CTA trip: 16 KB of input (8,192 BF16 / FP16 or 16,384 E5M2 elements), or the
 // chunk when chunks are smaller, so a tile never straddles a chunk (chunk
 // sizes are powers of two >= 64).  Each of the 256 consumer threads of a CTA
 // owns 64 contiguous bytes of the tile.
@@ -30,10 +30,13 @@ constexpr uint8_t kEscapeFlag = 0x10;
 
 __host__ __device__ inline uint64_t align16(uint64_t x) { return (x + 15u) & ~uint64_t(15); }
 
-__host__ __device__ inline uint32_t elem_bytes(int dtype) { return dtype == SPLITZIP_BF16 ? 2u : 1u; }
+__host__ __device__ inline uint32_t elem_bytes(int dtype) { return dtype == SPLITZIP_FP8_E5M2 ? 1u : 2u; }
 
+// Bytes of the sign|mantissa stream: BF16 one byte per element, E5M2 3 bits
+// and FP16 11 bits per element, packed in groups of 8 elements.
 __host__ __device__ inline uint64_t signmant_bytes(int dtype, uint64_t n) {
-    return dtype == SPLITZIP_BF16 ? n : 3u * ((n + 7u) / 8u);
+    if (dtype == SPLITZIP_BF16) return n;
+    return (dtype == SPLITZIP_FP16 ? 11u : 3u) * ((n + 7u) / 8u);
 }
 
 // Byte offsets of every section of a container (format v1, see splitzip.h).

@@ -73,7 +73,7 @@ int plan_for(uint64_t n, int dtype, uint32_t chunk, uint64_t piece_elems, int co
     int st = splitzip_max_compressed_size(piece_elems, dtype, chunk, &cap);
     if (st != SPLITZIP_OK) return st;
     if ((st = splitzip_encode_workspace_size(piece_elems, dtype, chunk, &ws)) != SPLITZIP_OK) return st;
-    const uint64_t eb = dtype == SPLITZIP_BF16 ? 2u : 1u;
+    const uint64_t eb = elem_bytes(dtype);
     p->piece_elems = piece_elems;
     p->pieces = (n + piece_elems - 1) / piece_elems;
     // raw pieces cross the link as they are
@@ -158,7 +158,7 @@ extern "C" int splitzip_transfer(const void* d_src, void* d_dst, uint64_t n, int
                                  int compress, void* d_scratch, uint64_t d_scratch_bytes, void* h_stage,
                                  uint64_t h_stage_bytes, uint64_t* out_link_bytes, float* out_ms,
                                  cudaStream_t stream) {
-    if (dtype != SPLITZIP_BF16 && dtype != SPLITZIP_FP8_E5M2) return SPLITZIP_ERR_INVALID_ARG;
+    if (dtype != SPLITZIP_BF16 && dtype != SPLITZIP_FP8_E5M2 && dtype != SPLITZIP_FP16) return SPLITZIP_ERR_INVALID_ARG;
     if (compress != 0 && compress != 1) return SPLITZIP_ERR_INVALID_ARG;
     Plan p;
     int st = plan_for(n, dtype, chunk_elems, piece_elems, compress, &p);
@@ -175,7 +175,7 @@ extern "C" int splitzip_transfer(const void* d_src, void* d_dst, uint64_t n, int
         cudaGetLastError();
         return SPLITZIP_ERR_CUDA;
     }
-    const uint64_t eb = dtype == SPLITZIP_BF16 ? 2u : 1u;
+    const uint64_t eb = elem_bytes(dtype);
     const uint8_t* src = static_cast<const uint8_t*>(d_src);
     uint8_t* dst = static_cast<uint8_t*>(d_dst);
     // both scratch areas start at the slot alignment

@@ -44,7 +44,7 @@ def test_status_strings(splitzip_lib):
     assert sz.splitzip_status_string(99) == "unknown status"
 
 
-@pytest.mark.parametrize("dtype", [sz.BF16, sz.FP8_E5M2])
+@pytest.mark.parametrize("dtype", [sz.BF16, sz.FP8_E5M2, sz.FP16])
 @pytest.mark.parametrize("chunk", [64, 256, 8192, 65536])
 def test_sizes_match_oracle(splitzip_lib, dtype, chunk):
     for n in (0, 1, 2, 7, 31, 64, 65, 1000, 65537, 2**31 + 3, 2**32):
@@ -75,7 +75,7 @@ def test_workspace_size(splitzip_lib):
 
 def test_size_argument_errors(splitzip_lib):
     out = ctypes.c_uint64(0)
-    assert sz.splitzip_max_compressed_size(10, 2, 65536, out) == sz.ERR_INVALID_ARG      # dtype
+    assert sz.splitzip_max_compressed_size(10, 3, 65536, out) == sz.ERR_INVALID_ARG      # dtype
     assert sz.splitzip_max_compressed_size(10, 0, 100, out) == sz.ERR_INVALID_ARG        # not pow2
     assert sz.splitzip_max_compressed_size(10, 0, 32, out) == sz.ERR_INVALID_ARG         # < 64
     assert sz.splitzip_max_compressed_size(10, 0, 131072, out) == sz.ERR_INVALID_ARG     # > 65536
@@ -260,3 +260,16 @@ def test_selftest_argument_errors(splitzip_lib):
     assert sz.splitzip_selftest_bounded_wait(100, None, None, 0) == sz.ERR_INVALID_ARG
     assert sz.splitzip_selftest_bounded_wait(100, A + 2, None, 0) == sz.ERR_INVALID_ARG
     assert sz.splitzip_selftest_bounded_wait(100, A, A + 4, 0) == sz.ERR_INVALID_ARG
+
+
+def test_fp16_calibrate_and_ablation_refusal(splitzip_lib):
+    # FP16 histograms have 32 bins; the ablation formats are defined for BF16 and E5M2 only
+    h = np.zeros(256, dtype=np.uint64)
+    h[[3, 15, 16, 14]] = [5, 900, 400, 400]
+    cb = sz.Codebook()
+    assert sz.splitzip_calibrate(h.ctypes.data, 0, sz.FP16, cb) == sz.OK
+    np.testing.assert_array_equal(np.array(cb.values(), np.uint8), oracle.calibrate(h, sz.FP16))
+    h[40] = 1
+    assert sz.splitzip_calibrate(h.ctypes.data, 0, sz.FP16, cb) == sz.ERR_INVALID_ARG
+    out = ctypes.c_uint64(0)
+    assert sz.splitzip_ablation_max_size(100, sz.FP16, 65536, 1, out) == sz.ERR_INVALID_ARG

@@ -38,7 +38,11 @@ def a16(x):
 
 def np_bits(t, dtype):
     a = t.cpu().numpy()
-    return a.view(np.uint16) if dtype == sz.BF16 else a
+    return a if dtype == sz.FP8_E5M2 else a.view(np.uint16)
+
+
+def sm_stream_bytes(n, dtype):
+    return n if dtype == sz.BF16 else (11 if dtype == sz.FP16 else 3) * (-(-n // 8))
 
 
 def gpu_encode(x_dev, cb, dtype, chunk, dirty=True):
@@ -54,7 +58,7 @@ def gpu_encode(x_dev, cb, dtype, chunk, dirty=True):
 
 
 def gpu_decode(blob_dev, n, dtype, in_bytes=None):
-    out = torch.empty(max(n, 1), dtype=torch.int16 if dtype == sz.BF16 else torch.uint8, device=DEV)
+    out = torch.empty(max(n, 1), dtype=torch.uint8 if dtype == sz.FP8_E5M2 else torch.int16, device=DEV)
     status = torch.full((4,), -1, dtype=torch.int32, device=DEV)
     sz.decode_into(blob_dev, blob_dev.numel() if in_bytes is None else in_bytes, out, n, dtype, status)
     torch.cuda.synchronize()
@@ -68,7 +72,7 @@ def codebook_of(exps, dtype):
 def roundtrip_vs_oracle(bits, dtype, cb_exps, chunk):
     """Encode on the GPU and with the oracle; bytes must match; both
     containers decode on the GPU to the input."""
-    x = torch.from_numpy(bits.view(np.int16) if dtype == sz.BF16 else bits).to(DEV)
+    x = torch.from_numpy(bits if dtype == sz.FP8_E5M2 else bits.view(np.int16)).to(DEV)
     blob = gpu_encode(x, codebook_of(cb_exps, dtype), dtype, chunk)
     ref = oracle.encode(bits, dtype, np.asarray(cb_exps, np.uint8), chunk)
     got = blob.cpu().numpy()
@@ -257,7 +261,7 @@ def _layout(n, dtype, chunk, E):
     C = -(-n // chunk)
     nib = a16(64 + 12 * C)
     sm = nib + a16((n + 1) // 2)
-    sm_bytes = n if dtype == 0 else 3 * (-(-n // 8))
+    sm_bytes = sm_stream_bytes(n, dtype)
     rec = sm + a16(sm_bytes)
     return dict(C=C, index=64, counts=64 + 8 * C, index_end=64 + 12 * C, nib=nib, sm=sm, sm_bytes=sm_bytes,
                 rec=rec, size=rec + 3 * E)
@@ -293,7 +297,7 @@ def _compare_all_chunks(hb, xh, dtype, cb, chunk, L, off, cnt, block_chunks=16):
         R = _layout(hi - lo, dtype, chunk, (ref.size - _layout(hi - lo, dtype, chunk, 0)["size"]) // 3)
         checks = [
             ("nibbles", hb[L["nib"] + lo // 2: L["nib"] + (hi + 1) // 2], ref[R["nib"]: R["nib"] + (hi - lo + 1) // 2]),
-            ("sign|mantissa", hb[L["sm"] + (lo if dtype == 0 else lo // 8 * 3): L["sm"] + (hi if dtype == 0 else 3 * (-(-hi // 8)))],
+            ("sign|mantissa", hb[L["sm"] + sm_stream_bytes(lo, dtype): L["sm"] + sm_stream_bytes(hi, dtype)],
              ref[R["sm"]: R["sm"] + R["sm_bytes"]]),
             ("counts", hb[L["counts"] + 4 * c0: L["counts"] + 4 * c1], ref[R["counts"]: R["index_end"]]),
             ("records", hb[L["rec"] + 3 * int(off[c0]): L["rec"] + 3 * (int(off[c0]) + int(cnt[c0:c1].sum()))],
@@ -337,8 +341,10 @@ def _full_size_check(name):
         assert not hb[lo:hi].any(), "padding [%d, %d) not zero" % (lo, hi)
 
     # E = exponent mass outside the codebook, counted by torch on the device
-    if dtype == 0:
+    if dtype == sz.BF16:
         e = (x.view(torch.int16).to(torch.int32) >> 7) & 0xFF
+    elif dtype == sz.FP16:
+        e = (x.view(torch.int16).to(torch.int32) >> 10) & 0x1F
     else:
         e = (x.to(torch.int32) >> 2) & 0x1F
     counts = torch.bincount(e.flatten(), minlength=256).cpu().numpy()
@@ -381,4 +387,10 @@ def test_kv_cache_32_layer_bf16_full_size():
 @pytest.mark.slow
 def test_kv_cache_32_layer_e5m2_full_size():
     rate = _full_size_check("kv_cache_32x2x65536x8x128_e5m2")
+    assert 0.0 < rate < 0.5
+
+
+@pytest.mark.slow
+def test_kv_cache_32_layer_fp16_full_size():
+    rate = _full_size_check("kv_cache_32x2x32768x8x128_fp16")
     assert 0.0 < rate < 0.5

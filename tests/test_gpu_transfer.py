@@ -33,11 +33,14 @@ def bits(dtype, n, seed):
     if dtype == sz.BF16:
         x = W.escape_stress(seed, chunks=-(-n // 65536), chunk_elems=65536)[:n]
         return x.numpy().view(np.uint16), x.cuda()
+    if dtype == sz.FP16:
+        x = W.kv_cache_layer_fp16(seed, 3, tokens=-(-n // 2048))[:n]
+        return x.numpy().view(np.uint16), x.cuda()
     x = W.kv_cache_layer_e5m2(seed, 3, tokens=-(-n // 1024))[:n]
     return x.numpy(), x.cuda()
 
 
-@pytest.mark.parametrize("dtype", [sz.BF16, sz.FP8_E5M2])
+@pytest.mark.parametrize("dtype", [sz.BF16, sz.FP8_E5M2, sz.FP16])
 @pytest.mark.parametrize("chunk,piece", [(65536, 65536), (4096, 3 * 4096)])
 def test_transfer_matches_oracle(dtype, chunk, piece):
     n = 9 * 65536 + 12345  # ten or more pieces: the ring of four slots is reused; a ragged last piece
@@ -51,7 +54,7 @@ def test_transfer_matches_oracle(dtype, chunk, piece):
         torch.cuda.synchronize()
         assert torch.equal(y, x)
         assert ms > 0
-        eb = 2 if dtype == sz.BF16 else 1
+        eb = 1 if dtype == sz.FP8_E5M2 else 2
         pieces = [(i, min(piece, n - i)) for i in range(0, n, piece)]
         if not compress:
             assert link == n * eb

@@ -19,10 +19,12 @@ from lossless_kv_cache_gb300 import workloads as W
 def _tensor(dtype, n):
     if dtype == 0:
         return W.escape_stress(3, chunks=5, chunk_elems=65536).numpy().view(np.uint16)[:n]
+    if dtype == 2:
+        return W.kv_cache_layer_fp16(1, 2, tokens=160).numpy().view(np.uint16)[:n]
     return W.kv_cache_layer_e5m2(1, 2, tokens=300).numpy()[:n]
 
 
-@pytest.mark.parametrize("dtype", [0, 1])
+@pytest.mark.parametrize("dtype", [0, 1, 2])
 @pytest.mark.parametrize("chunk", [64, 4096, 65536])
 def test_merge_of_oracle_pieces_is_the_whole_container(dtype, chunk):
     n = 5 * 65536 - 333

@@ -17,10 +17,12 @@ from tests.test_gpu_parity import _compare_all_chunks, _expected_header, _layout
 def _case(dtype):
     if dtype == 0:
         return W.escape_stress(0, chunks=40, chunk_elems=4096).numpy().view(np.uint16)[: 40 * 4096 - 1000]
+    if dtype == 2:
+        return W.kv_cache_layer_fp16(0, 1, tokens=80).numpy().view(np.uint16)[:-40]
     return W.kv_cache_layer_e5m2(0, 1, tokens=100).numpy()[:-24]
 
 
-@pytest.mark.parametrize("dtype", [0, 1])
+@pytest.mark.parametrize("dtype", [0, 1, 2])
 def test_checker_accepts_the_oracle_and_catches_planted_bits(dtype):
     chunk = 4096
     x = _case(dtype)
