@@ -318,6 +318,64 @@ int splitzip_transfer(const void* d_src, void* d_dst, uint64_t n, int dtype, con
                       uint64_t d_scratch_bytes, void* h_stage, uint64_t h_stage_bytes, uint64_t* out_link_bytes,
                       float* out_ms, cudaStream_t stream);
 
+/* Batches: several tensors, each into (or from) its own container, in one
+ * launch sequence.  The page's transfers are per request and per layer
+ * (section "Results": the gains vary with sequence length and batch size), so
+ * a serving engine moves many pieces of a few megabytes; at that size a call
+ * costs its launches, not HBM time, and a batch pays them once.
+ * splitzip_encode and splitzip_decode take the same path on their own for
+ * small tensors (encode: up to 8,192 tiles -- 67,108,864 BF16 / FP16 or
+ * 134,217,728 E5M2 elements at the default chunk, as one cooperative kernel
+ * when the tiles fit the GPU at once; decode: up to 2^21 elements), so a
+ * single small call gains the same way.
+ * Limits: 1..SPLITZIP_MAX_BATCH items, each of at most
+ * SPLITZIP_MAX_BATCH_ITEM_ELEMS elements (SPLITZIP_ERR_UNSUPPORTED beyond);
+ * all items share dtype, chunk size and codebook; one status word for the
+ * whole batch (the first error of any item).  The item arrays are host memory
+ * read during the call only; every pointer in them follows the rules of the
+ * single-tensor calls (device, 16-byte aligned; d_out_size 8-byte aligned). */
+#define SPLITZIP_MAX_BATCH 256u
+#define SPLITZIP_MAX_BATCH_ITEM_ELEMS (1ull << 26)
+
+typedef struct {
+    const void* d_in;      /* n elements */
+    uint64_t n;
+    void* d_out;           /* the item's container, out_capacity >= splitzip_max_compressed_size */
+    uint64_t out_capacity;
+    uint64_t* d_out_size;  /* device u64: the container's size */
+} splitzip_encode_item_t;
+
+typedef struct {
+    const void* d_in;      /* in_bytes bytes of container (>= its size) */
+    uint64_t in_bytes;
+    void* d_out;           /* n elements */
+    uint64_t n;
+} splitzip_decode_item_t;
+
+/* Workspace bytes for splitzip_encode_batch: each item's
+ * splitzip_encode_workspace_size rounded up to 256 bytes, summed; h_n: the
+ * items' element counts (host). */
+int splitzip_encode_batch_workspace_size(const uint64_t* h_n, uint32_t count, int dtype, uint32_t chunk_elems,
+                                         uint64_t* out_bytes);
+
+/* Encode every item into its own container (byte-identical to splitzip_encode
+ * of that item).  Three kernels for the whole batch, chained with
+ * programmatic dependent launch: one CTA per 16 KB tile of every item, the
+ * index of every item, the escape records of every tile.  d_ws: at least
+ * splitzip_encode_batch_workspace_size bytes, contents need not be
+ * initialised; d_status: device int, set by the call (SPLITZIP_OK or the
+ * first error).  Calls that share d_ws must not overlap on the GPU. */
+int splitzip_encode_batch(const splitzip_encode_item_t* h_items, uint32_t count, int dtype,
+                          const splitzip_codebook_t* cb, uint32_t chunk_elems, void* d_ws, uint64_t ws_bytes,
+                          int* d_status, cudaStream_t stream);
+
+/* Decode every item's container into its elements (each bit-identical to
+ * splitzip_decode of it), checked as splitzip_decode checks; errors of any
+ * item go to *d_status.  A one-thread kernel clears the status word, then one
+ * CTA per 16,384 elements of every item decodes, patches and checks. */
+int splitzip_decode_batch(const splitzip_decode_item_t* h_items, uint32_t count, int dtype, int* d_status,
+                          cudaStream_t stream);
+
 /* Join the containers of consecutive pieces of one tensor into the container
  * of the whole tensor, byte-identical to encoding it in one call.  Chunks are
  * independent (Method, "Escape stream": positions are 16-bit offsets within a

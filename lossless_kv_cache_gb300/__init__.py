@@ -66,6 +66,22 @@ class Header(ctypes.Structure):
     ]
 
 
+class EncodeItem(ctypes.Structure):
+    """splitzip_encode_item_t."""
+    _fields_ = [("d_in", ctypes.c_void_p), ("n", ctypes.c_uint64), ("d_out", ctypes.c_void_p),
+                ("out_capacity", ctypes.c_uint64), ("d_out_size", ctypes.c_void_p)]
+
+
+class DecodeItem(ctypes.Structure):
+    """splitzip_decode_item_t."""
+    _fields_ = [("d_in", ctypes.c_void_p), ("in_bytes", ctypes.c_uint64), ("d_out", ctypes.c_void_p),
+                ("n", ctypes.c_uint64)]
+
+
+MAX_BATCH = 256                 # SPLITZIP_MAX_BATCH
+MAX_BATCH_ITEM_ELEMS = 1 << 26  # SPLITZIP_MAX_BATCH_ITEM_ELEMS
+
+
 class _Address(ctypes.c_void_p):
     """A pointer argument: an integer address, None (NULL), or an object with
     data_ptr() (a torch tensor).  Anything else -- notably a str or bytes, which
@@ -120,6 +136,10 @@ SIGNATURES = {
     "splitzip_selftest_bounded_wait": (_int, [_u64, _vp, _vp, _vp]),
     "splitzip_merge": (_int, [ctypes.POINTER(ctypes.c_void_p), ctypes.POINTER(ctypes.c_uint64), _u32, _vp, _u64,
                               _P_u64]),
+    "splitzip_encode_batch_workspace_size": (_int, [ctypes.POINTER(ctypes.c_uint64), _u32, _int, _u32, _P_u64]),
+    "splitzip_encode_batch": (_int, [ctypes.POINTER(EncodeItem), _u32, _int, ctypes.POINTER(Codebook), _u32, _vp,
+                                     _u64, _vp, _vp]),
+    "splitzip_decode_batch": (_int, [ctypes.POINTER(DecodeItem), _u32, _int, _vp, _vp]),
 }
 
 _lib = None
@@ -242,6 +262,22 @@ def splitzip_selftest_bounded_wait(limit_cycles, d_status, d_cycles, stream):
 def splitzip_merge(h_parts, part_bytes, count, h_out, out_capacity, out_bytes):
     """h_parts: ctypes array of c_void_p; part_bytes: ctypes array of c_uint64."""
     return lib().splitzip_merge(h_parts, part_bytes, count, h_out, out_capacity, ctypes.byref(out_bytes))
+
+
+def splitzip_encode_batch_workspace_size(h_n, count, dtype, chunk_elems, out_bytes):
+    """h_n: ctypes array of c_uint64."""
+    return lib().splitzip_encode_batch_workspace_size(h_n, count, dtype, chunk_elems, ctypes.byref(out_bytes))
+
+
+def splitzip_encode_batch(h_items, count, dtype, cb, chunk_elems, d_ws, ws_bytes, d_status, stream):
+    """h_items: ctypes array of EncodeItem."""
+    return lib().splitzip_encode_batch(h_items, count, dtype, ctypes.byref(cb), chunk_elems, d_ws, ws_bytes, d_status,
+                                       stream)
+
+
+def splitzip_decode_batch(h_items, count, dtype, d_status, stream):
+    """h_items: ctypes array of DecodeItem."""
+    return lib().splitzip_decode_batch(h_items, count, dtype, d_status, stream)
 
 
 # ------------------------------------------------------------ size helpers
@@ -373,6 +409,51 @@ def decode(blob, n, dtype, stream=None):
     decode_into(blob, blob.numel(), out, n, dtype, status, stream)
     _check(int(status[0].item()), "splitzip_decode (device)")
     return out[:n]
+
+
+def batch_workspace_size(ns, dtype, chunk_elems=DEFAULT_CHUNK_ELEMS):
+    arr = (ctypes.c_uint64 * len(ns))(*ns)
+    out = ctypes.c_uint64(0)
+    _check(splitzip_encode_batch_workspace_size(arr, len(ns), dtype, chunk_elems, out),
+           "splitzip_encode_batch_workspace_size")
+    return out.value
+
+
+def encode_batch(xs, cb, dtype, chunk_elems=DEFAULT_CHUNK_ELEMS, stream=None):
+    """Encode each device tensor of ``xs`` into its own container with one
+    batched call; returns the containers (uint8 device tensors of their exact
+    sizes).  Synchronises to read the sizes."""
+    torch = _torch()
+    dev = xs[0].device
+    caps = [max_compressed_size(x.numel(), dtype, chunk_elems) for x in xs]
+    outs = [torch.empty(c, dtype=torch.uint8, device=dev) for c in caps]
+    sizes = torch.zeros(len(xs), dtype=torch.int64, device=dev)
+    status = torch.zeros(4, dtype=torch.int32, device=dev)
+    ws_bytes = batch_workspace_size([x.numel() for x in xs], dtype, chunk_elems)
+    ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
+    items = (EncodeItem * len(xs))()
+    for i, (x, o, c) in enumerate(zip(xs, outs, caps)):
+        items[i] = EncodeItem(x.data_ptr() if x.numel() else 0, x.numel(), o.data_ptr(), c,
+                              sizes.data_ptr() + 8 * i)
+    _check(splitzip_encode_batch(items, len(xs), dtype, cb, chunk_elems, ws.data_ptr(), ws_bytes, status.data_ptr(),
+                                 _stream_handle(stream)), "splitzip_encode_batch")
+    _check(int(status[0].item()), "splitzip_encode_batch (device)")
+    return [o[: int(n)] for o, n in zip(outs, sizes.cpu().tolist())]
+
+
+def decode_batch_status(blobs, ns, dtype, stream=None):
+    """Decode device containers ``blobs`` (element counts ``ns``) with one
+    batched call; returns (device status, decoded tensors)."""
+    torch = _torch()
+    dev = blobs[0].device
+    outs = [torch.empty(max(n, 1), dtype=_bits_dtype(dtype), device=dev) for n in ns]
+    status = torch.full((4,), -1, dtype=torch.int32, device=dev)
+    items = (DecodeItem * len(blobs))()
+    for i, (b, o, n) in enumerate(zip(blobs, outs, ns)):
+        items[i] = DecodeItem(b.data_ptr(), b.numel(), o.data_ptr() if n else 0, n)
+    _check(splitzip_decode_batch(items, len(blobs), dtype, status.data_ptr(), _stream_handle(stream)),
+           "splitzip_decode_batch")
+    return int(status[0].item()), [o[:n] for o, n in zip(outs, ns)]
 
 
 def transfer_scratch_size(n, dtype, piece_elems, compress=True, chunk_elems=DEFAULT_CHUNK_ELEMS):

@@ -15,7 +15,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build", "splitzip")
 LIB = os.path.join(PKG, "libsplitzip.so")
-SOURCES = ["capi.cu", "encode.cu", "decode.cu", "histogram.cu", "encode_noalloc.cu", "transfer.cu", "ablation.cu", "selftest.cu", "merge.cu"]
+SOURCES = ["capi.cu", "encode.cu", "decode.cu", "histogram.cu", "encode_noalloc.cu", "transfer.cu", "ablation.cu", "selftest.cu", "merge.cu", "batch.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2,-Wall", "--expt-relaxed-constexpr"]
 

@@ -14,6 +14,14 @@ using namespace splitzip;
 namespace {
 
 constexpr uint64_t kMaxElems = uint64_t(1) << 48;  // keeps every size below 2^52
+// Up to these sizes a single call takes the small-tensor kernels of batch.cu
+// (the persistent kernels' grids would not fill the GPU, and launches and
+// dependent memory round trips dominate): encode by one cooperative kernel
+// when every tile gets its own resident CTA, else by the two-kernel batch
+// path up to kSmallEncodeTiles; decode by the batch decoder up to
+// kSmallDecodeElems.
+constexpr uint64_t kSmallEncodeTiles = 8192;
+constexpr uint64_t kSmallDecodeElems = uint64_t(1) << 21;
 constexpr int kMaxDevices = 64;
 
 struct DeviceState {
@@ -21,6 +29,7 @@ struct DeviceState {
     int status;
     int sms;
     int encode_bpsm[3], decode_bpsm[3], hist_bpsm[3];  // per dtype
+    int coop_encode_bpsm[3];
 };
 
 std::mutex g_mutex;
@@ -49,7 +58,8 @@ int device_state(DeviceState* out) {
             for (int t = 0; t < 3; ++t) {
                 if (occupancy_encode(&d.encode_bpsm[t], t) != cudaSuccess ||
                     occupancy_decode(&d.decode_bpsm[t], t) != cudaSuccess ||
-                    occupancy_histogram(&d.hist_bpsm[t], t) != cudaSuccess) {
+                    occupancy_histogram(&d.hist_bpsm[t], t) != cudaSuccess ||
+                    occupancy_coop(&d.coop_encode_bpsm[t], t) != cudaSuccess) {
                     cudaGetLastError();
                     return SPLITZIP_ERR_CUDA;
                 }
@@ -300,6 +310,19 @@ int encode_call(const void* d_in, uint64_t n, int dtype, const splitzip_codebook
     }
     DeviceState d;
     if ((st = device_state(&d)) != SPLITZIP_OK) return st;
+    if (!paged.pages && W.n_tiles > 0 && W.n_tiles <= kSmallEncodeTiles) {
+        // a small tensor (batch.cu)
+        const SmallEncodeItem item{d_in, n, d_out, d_out_size, d_ws};
+        const uint8_t* host_cb = device_cb ? nullptr : cb->exps;
+        const uint8_t* dev_cb = device_cb ? reinterpret_cast<const uint8_t*>(cb) : nullptr;
+        const uint64_t resident = uint64_t(d.sms) * uint64_t(d.coop_encode_bpsm[dtype]);
+        const cudaError_t e =
+            W.n_tiles <= resident
+                ? launch_coop_encode(item, dtype, host_cb, dev_cb, chunk_elems, d_status, int(W.n_tiles), stream)
+                : launch_small_encode(&item, 1, dtype, host_cb, dev_cb, chunk_elems, d_status, stream);
+        if (e != cudaSuccess) cudaGetLastError();
+        return e == cudaSuccess ? SPLITZIP_OK : SPLITZIP_ERR_CUDA;
+    }
     CUtensorMap map;
     const uint64_t mapped = paged.pages ? paged.pool_pages * paged.page_elems * eb : n * eb;
     if ((st = make_input_map(d_in, dtype, &a, &map, mapped)) != SPLITZIP_OK) return st;
@@ -356,6 +379,13 @@ int decode_call(const void* d_in, uint64_t in_bytes, void* d_out, uint64_t n, in
     DeviceState d;
     int st = device_state(&d);
     if (st != SPLITZIP_OK) return st;
+    if (!pages && n <= kSmallDecodeElems) {
+        // a small tensor: a status clear and one CTA per 8,192 elements (batch.cu)
+        const SmallDecodeItem item{d_in, in_bytes, d_out, n};
+        const cudaError_t e = launch_small_decode(&item, 1, dtype, d_status, stream);
+        if (e != cudaSuccess) cudaGetLastError();
+        return e == cudaSuccess ? SPLITZIP_OK : SPLITZIP_ERR_CUDA;
+    }
     if (cudaMemsetAsync(d_status, 0, sizeof(int), stream) != cudaSuccess) {
         cudaGetLastError();
         return SPLITZIP_ERR_CUDA;
@@ -415,6 +445,70 @@ int splitzip_decode_paged(const void* d_in, uint64_t in_bytes, void* d_pool, uin
     if (n_pages > kMaxElems / page_elems || pool_pages > kMaxElems / page_elems) return SPLITZIP_ERR_UNSUPPORTED;
     return decode_call(d_in, in_bytes, d_pool, n_pages * page_elems, dtype, d_status, stream, d_pages, pool_pages,
                        log2_of(page_elems));
+}
+
+int splitzip_encode_batch_workspace_size(const uint64_t* h_n, uint32_t count, int dtype, uint32_t chunk_elems,
+                                         uint64_t* out_bytes) {
+    if (!h_n || !out_bytes || count == 0 || count > SPLITZIP_MAX_BATCH) return SPLITZIP_ERR_INVALID_ARG;
+    uint64_t total = 0;
+    for (uint32_t i = 0; i < count; ++i) {
+        const int st = check_geometry(h_n[i], dtype, chunk_elems);
+        if (st != SPLITZIP_OK) return st;
+        if (h_n[i] > SPLITZIP_MAX_BATCH_ITEM_ELEMS) return SPLITZIP_ERR_UNSUPPORTED;
+        total += (workspace_for(h_n[i], dtype, chunk_elems).bytes + 255u) & ~uint64_t(255);
+    }
+    *out_bytes = total;
+    return SPLITZIP_OK;
+}
+
+int splitzip_encode_batch(const splitzip_encode_item_t* h_items, uint32_t count, int dtype,
+                          const splitzip_codebook_t* cb, uint32_t chunk_elems, void* d_ws, uint64_t ws_bytes,
+                          int* d_status, cudaStream_t stream) {
+    if (!h_items || count == 0 || count > SPLITZIP_MAX_BATCH) return SPLITZIP_ERR_INVALID_ARG;
+    if (!valid_dtype(dtype) || !valid_chunk(chunk_elems)) return SPLITZIP_ERR_INVALID_ARG;
+    int st = check_codebook(cb, dtype);
+    if (st != SPLITZIP_OK) return st;
+    if (!d_status || !aligned(d_status, 4)) return SPLITZIP_ERR_INVALID_ARG;
+    SmallEncodeItem items[SPLITZIP_MAX_BATCH];
+    uint64_t ws_off = 0;
+    for (uint32_t i = 0; i < count; ++i) {
+        const splitzip_encode_item_t& it = h_items[i];
+        if ((st = check_geometry(it.n, dtype, chunk_elems)) != SPLITZIP_OK) return st;
+        if (it.n > SPLITZIP_MAX_BATCH_ITEM_ELEMS) return SPLITZIP_ERR_UNSUPPORTED;
+        if (it.n > 0 && (!it.d_in || !aligned(it.d_in, 16))) return SPLITZIP_ERR_INVALID_ARG;
+        if (!it.d_out || !aligned(it.d_out, 16) || !it.d_out_size || !aligned(it.d_out_size, 8))
+            return SPLITZIP_ERR_INVALID_ARG;
+        if (it.out_capacity < layout_for(it.n, dtype, chunk_elems, it.n).size) return SPLITZIP_ERR_CAPACITY;
+        items[i] = SmallEncodeItem{it.d_in, it.n, it.d_out, it.d_out_size, static_cast<uint8_t*>(d_ws) + ws_off};
+        ws_off += (workspace_for(it.n, dtype, chunk_elems).bytes + 255u) & ~uint64_t(255);
+    }
+    if (ws_bytes < ws_off) return SPLITZIP_ERR_CAPACITY;
+    if (ws_off > 0 && (!d_ws || !aligned(d_ws, 16))) return SPLITZIP_ERR_INVALID_ARG;
+    DeviceState d;
+    if ((st = device_state(&d)) != SPLITZIP_OK) return st;
+    return launch_small_encode(items, count, dtype, cb->exps, nullptr, chunk_elems, d_status, stream) == cudaSuccess
+               ? SPLITZIP_OK
+               : SPLITZIP_ERR_CUDA;
+}
+
+int splitzip_decode_batch(const splitzip_decode_item_t* h_items, uint32_t count, int dtype, int* d_status,
+                          cudaStream_t stream) {
+    if (!h_items || count == 0 || count > SPLITZIP_MAX_BATCH || !valid_dtype(dtype)) return SPLITZIP_ERR_INVALID_ARG;
+    if (!d_status || !aligned(d_status, 4)) return SPLITZIP_ERR_INVALID_ARG;
+    SmallDecodeItem items[SPLITZIP_MAX_BATCH];
+    for (uint32_t i = 0; i < count; ++i) {
+        const splitzip_decode_item_t& it = h_items[i];
+        if (!it.d_in || !aligned(it.d_in, 16)) return SPLITZIP_ERR_INVALID_ARG;
+        if (it.n > 0 && (!it.d_out || !aligned(it.d_out, 16))) return SPLITZIP_ERR_INVALID_ARG;
+        if (it.n > SPLITZIP_MAX_BATCH_ITEM_ELEMS) return SPLITZIP_ERR_UNSUPPORTED;
+        if (it.in_bytes < kHeaderBytes) return SPLITZIP_ERR_CORRUPT;
+        items[i] = SmallDecodeItem{it.d_in, it.in_bytes, it.d_out, it.n};
+    }
+    DeviceState d;
+    const int st = device_state(&d);
+    if (st != SPLITZIP_OK) return st;
+    return launch_small_decode(items, count, dtype, d_status, stream) == cudaSuccess ? SPLITZIP_OK
+                                                                                     : SPLITZIP_ERR_CUDA;
 }
 
 int splitzip_parse_header(const void* h_blob, uint64_t bytes, splitzip_header_t* out) {

@@ -31,6 +31,7 @@
 //     records to their place in the escape stream.
 #include <type_traits>
 
+#include "encode_core.cuh"
 #include "splitzip_internal.cuh"
 #include "tma_pipeline.cuh"
 
@@ -53,182 +54,6 @@ template <int DT> constexpr int kMinBlocks = DT == SPLITZIP_FP8_E5M2 ? 2 : 1;
 template <int DT> constexpr uint32_t kEncodeSmem = kStages<DT> * kStageBytes + 1024;
 constexpr int kFinishThreads = kGroupTiles;  // one thread per tile of the group
 static_assert(kConsumers * kThreadBytes == kTileBytes, "one tile = 64 bytes per consumer thread");
-
-// Position table entries (four tables, one per position k = 0..3 of an
-// element within its group of four consecutive elements):
-//   bits 16 + 4k .. 19 + 4k  the element's code (0 when it escapes)
-//   bit  12 + k              the element's escape flag
-//   bits 3k .. 3k + 1        E5M2 only: the element's 2 mantissa bits
-// BF16 and FP16 tables are indexed by the exponent, E5M2 tables by the byte without
-// its sign (exponent and mantissa: 128 entries, so elements that differ only
-// in sign hit the same entry instead of another bank).  The four entries of a
-// group have disjoint bits, so their sum -- plus, for E5M2, the four sign bits
-// moved to bits 3k + 2 -- is the group's two nibble bytes (bits 16..31, even
-// element in the low nibble), its escape mask (bits 12..15) and its 12 bits of
-// packed 3-bit sign|mantissa values (bits 0..11).
-__device__ __forceinline__ uint32_t table_entry(int dtype, int k, uint32_t index, const uint8_t* code) {
-    uint32_t e = index, s3 = 0;
-    if (dtype == SPLITZIP_FP8_E5M2) {  // index = exponent << 2 | mantissa
-        e = (index >> 2) & 31u;
-        s3 = index & 3u;
-    }
-    const uint32_t t = code[e];
-    const uint32_t c = (t & kEscapeFlag) ? (1u << (12 + k)) : (uint32_t(t & 15u) << (16 + 4 * k));
-    return c | (s3 << (3 * k));
-}
-
-// Entry of table k at byte offset `off` (index * 4).
-__device__ __forceinline__ uint32_t tab_at(const uint32_t* tab, int k, uint32_t off) {
-    return *reinterpret_cast<const uint32_t*>(reinterpret_cast<const uint8_t*>(tab + 256 * k) + off);
-}
-
-// BF16: the group of four elements in words x (elements 0, 1) and y (2, 3);
-// the table index is the exponent (bits 7..14 of each 16-bit element).
-__device__ __forceinline__ uint32_t group_bf16(const uint32_t* tab, uint32_t x, uint32_t y) {
-    return tab_at(tab, 0, (x >> 5) & 0x3FCu) + tab_at(tab, 1, (x >> 21) & 0x3FCu) +
-           tab_at(tab, 2, (y >> 5) & 0x3FCu) + tab_at(tab, 3, (y >> 21) & 0x3FCu);
-}
-
-// FP16: the group of four elements in words x (elements 0, 1) and y (2, 3);
-// the table index is the exponent (bits 10..14 of each 16-bit element).
-__device__ __forceinline__ uint32_t group_fp16(const uint32_t* tab, uint32_t x, uint32_t y) {
-    return tab_at(tab, 0, (x >> 8) & 0x7Cu) + tab_at(tab, 1, (x >> 24) & 0x7Cu) +
-           tab_at(tab, 2, (y >> 8) & 0x7Cu) + tab_at(tab, 3, (y >> 24) & 0x7Cu);
-}
-
-// E5M2: the group of four elements in word w.  The sign of byte k (bit
-// 8k + 7) belongs at bit 3k + 2: the high word of (signs * 0x08421000) has it
-// there (term k is shifted by 27 - 5k), and every other product term lands on
-// a bit of its own (checked for all 16 terms: no carries), so one mask keeps
-// exactly the four signs.
-__device__ __forceinline__ uint32_t group_e5m2(const uint32_t* tab, uint32_t w) {
-    const uint32_t signs = __umulhi(w & 0x80808080u, 0x08421000u) & 0x924u;
-    return tab_at(tab, 0, (w << 2) & 0x1FCu) + tab_at(tab, 1, (w >> 6) & 0x1FCu) +
-           tab_at(tab, 2, (w >> 14) & 0x1FCu) + tab_at(tab, 3, (w >> 22) & 0x1FCu) + signs;
-}
-
-// Stage position of byte L of a tile: the tensor-map copy stores every
-// 128-byte row r with its 16-byte pieces permuted by XOR with (r mod 8).
-__device__ __forceinline__ uint32_t swizzled(uint32_t L) { return L ^ (((L >> 7) & 7u) << 4); }
-
-// Load `nbytes` (< 16) bytes into a zero-filled vector (only the last bytes
-// of a tensor are not covered by whole rows of the tensor map).
-__device__ __forceinline__ uint4 load_partial(const uint8_t* p, uint32_t nbytes) {
-    uint32_t w[4] = {0u, 0u, 0u, 0u};
-#pragma unroll
-    for (uint32_t i = 0; i < 16; ++i)
-        if (i < nbytes) w[i >> 2] |= uint32_t(p[i]) << (8 * (i & 3));
-    return make_uint4(w[0], w[1], w[2], w[3]);
-}
-
-// Header fields known before any tile is encoded (E is written at the end),
-// and the zero padding between sections, whose places depend only on n.
-__device__ void write_header_and_padding(const EncodeArgs& a, const uint8_t* codebook) {
-    uint8_t* h = a.out;
-    uint32_t* h32 = reinterpret_cast<uint32_t*>(h);
-    h32[0] = kMagic;
-    h32[1] = uint32_t(kVersion) | (uint32_t(a.dtype) << 16);  // version, dtype, reserved 0
-    reinterpret_cast<uint64_t*>(h)[1] = a.n;
-    h32[4] = a.chunk_elems;
-    h32[5] = uint32_t(a.n_chunks);
-    uint32_t cb[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-        cb[i] = uint32_t(codebook[4 * i]) | (uint32_t(codebook[4 * i + 1]) << 8) |
-                (uint32_t(codebook[4 * i + 2]) << 16) | (uint32_t(codebook[4 * i + 3]) << 24);
-    reinterpret_cast<uint4*>(h)[2] = make_uint4(cb[0], cb[1], cb[2], cb[3]);
-    reinterpret_cast<uint4*>(h)[3] = make_uint4(0u, 0u, 0u, 0u);
-    const Layout L = layout_for(a.n, a.dtype, a.chunk_elems, 0);
-    for (uint64_t i = L.index_end; i < L.nibble_off; ++i) h[i] = 0;
-    for (uint64_t i = L.nibble_off + (a.n + 1) / 2; i < L.signmant_off; ++i) h[i] = 0;
-    for (uint64_t i = L.signmant_off + signmant_bytes(a.dtype, a.n); i < L.escrec_off; ++i) h[i] = 0;
-    if (a.n_tiles == 0) {  // no tile will finish the header
-        reinterpret_cast<uint64_t*>(h)[3] = 0;
-        *a.out_size = L.size;
-    }
-}
-
-__device__ __forceinline__ void report(int* status, int code) { atomicCAS(status, SPLITZIP_OK, code); }
-
-// Per-thread results of one tile: BF16 32 elements, E5M2 64 elements.
-template <int DT> struct ThreadOut;
-template <> struct ThreadOut<SPLITZIP_BF16> {
-    static constexpr uint32_t kElems = 32;
-    uint32_t nib[4];  // 16 nibble bytes
-    uint32_t sm[8];   // 32 sign|mantissa bytes
-    uint32_t mask;    // escape flags, bit b = element b
-};
-template <> struct ThreadOut<SPLITZIP_FP16> {
-    static constexpr uint32_t kElems = 32;
-    uint32_t nib[4];  // 16 nibble bytes
-    uint32_t sm[11];  // 44 bytes: 32 sign|mantissa fields of 11 bits, LSB-first
-    uint32_t mask;
-};
-template <> struct ThreadOut<SPLITZIP_FP8_E5M2> {
-    static constexpr uint32_t kElems = 64;
-    uint32_t nib[8];  // 32 nibble bytes
-    uint32_t s3[6];   // 24 bytes of packed 3-bit sign|mantissa
-    uint32_t mask[2];
-};
-
-// One 16-byte piece (BF16: 8 elements) into slot i of the thread's results.
-__device__ __forceinline__ void encode_piece(const uint32_t* tab, uint4 v, int i, ThreadOut<SPLITZIP_BF16>& o) {
-    const uint32_t s0 = group_bf16(tab, v.x, v.y), s1 = group_bf16(tab, v.z, v.w);
-    o.nib[i] = __byte_perm(s0, s1, 0x7632);
-    o.mask |= (((s0 >> 12) & 0xFu) | ((s1 >> 8) & 0xF0u)) << (8 * i);
-    // sign (bit 7 of the high byte) | mantissa (bits 6..0 of the low byte)
-    const uint32_t lo0 = __byte_perm(v.x, v.y, 0x6420), hi0 = __byte_perm(v.x, v.y, 0x7531);
-    const uint32_t lo1 = __byte_perm(v.z, v.w, 0x6420), hi1 = __byte_perm(v.z, v.w, 0x7531);
-    o.sm[2 * i] = (hi0 & 0x80808080u) | (lo0 & 0x7F7F7F7Fu);
-    o.sm[2 * i + 1] = (hi1 & 0x80808080u) | (lo1 & 0x7F7F7F7Fu);
-}
-
-// One 16-byte piece (FP16: 8 elements) into slot i of the thread's results.
-// The sign|mantissa fields of a word's two elements form one 22-bit value
-// (s11 of the even element | s11 of the odd one << 11): the even element's
-// sign (bit 15) moves to bit 10 and the odd element's mantissa (bits 16..25)
-// to bits 11..20 with the same shift by 5, its sign (bit 31) to bit 21.  Pair
-// j of the thread's 16 lands at bit 22 j of its 352-bit run (o.sm, zeroed by
-// the caller), possibly across two words.
-__device__ __forceinline__ void encode_piece(const uint32_t* tab, uint4 v, int i, ThreadOut<SPLITZIP_FP16>& o) {
-    const uint32_t s0 = group_fp16(tab, v.x, v.y), s1 = group_fp16(tab, v.z, v.w);
-    o.nib[i] = __byte_perm(s0, s1, 0x7632);
-    o.mask |= (((s0 >> 12) & 0xFu) | ((s1 >> 8) & 0xF0u)) << (8 * i);
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        const uint32_t x = w[j];
-        const uint32_t pair = (x & 0x3FFu) | ((x >> 5) & 0x1FFC00u) | ((x >> 10) & 0x200000u);
-        const int bit = 22 * (4 * i + j);
-        o.sm[bit >> 5] |= pair << (bit & 31);
-        if ((bit & 31) > 10) o.sm[(bit >> 5) + 1] |= pair >> (32 - (bit & 31));
-    }
-}
-
-// One 16-byte piece (E5M2: 16 elements); the packed sign|mantissa of the
-// piece (48 bits) is left in p[2i], p[2i+1] (24 bits each).
-__device__ __forceinline__ void encode_piece(const uint32_t* tab, uint4 v, int i, ThreadOut<SPLITZIP_FP8_E5M2>& o,
-                                             uint32_t* p) {
-    const uint32_t s0 = group_e5m2(tab, v.x), s1 = group_e5m2(tab, v.y);
-    const uint32_t s2 = group_e5m2(tab, v.z), s3 = group_e5m2(tab, v.w);
-    o.nib[2 * i] = __byte_perm(s0, s1, 0x7632);
-    o.nib[2 * i + 1] = __byte_perm(s2, s3, 0x7632);
-    const uint32_t f = ((s0 >> 12) & 0xFu) | ((s1 >> 8) & 0xF0u) | ((s2 >> 4) & 0xF00u) | (s3 & 0xF000u);
-    o.mask[i >> 1] |= f << (16 * (i & 1));
-    p[2 * i] = (s0 & 0xFFFu) | ((s1 & 0xFFFu) << 12);
-    p[2 * i + 1] = (s2 & 0xFFFu) | ((s3 & 0xFFFu) << 12);
-}
-
-// Eight 24-bit groups -> 24 bytes of the 3-bit stream.
-__device__ __forceinline__ void pack_s3_stream(const uint32_t* p, uint32_t* out) {
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-        const uint32_t* q = p + 4 * h;
-        out[3 * h] = q[0] | (q[1] << 24);
-        out[3 * h + 1] = (q[1] >> 8) | (q[2] << 16);
-        out[3 * h + 2] = (q[2] >> 16) | (q[3] << 8);
-    }
-}
 
 template <int DT>
 __global__ void __launch_bounds__(kBlock, kMinBlocks<DT>)
@@ -276,7 +101,8 @@ __global__ void __launch_bounds__(kBlock, kMinBlocks<DT>)
             mbar_init(&empty_bar[s], kConsumerWarps);
         }
         mbar_init_fence();
-        if (blockIdx.x == 0) write_header_and_padding(a, cb_s);
+        if (blockIdx.x == 0)
+            write_header_and_padding(a.out, a.dtype, a.n, a.chunk_elems, a.n_chunks, cb_s, a.out_size);
     }
     __syncthreads();
 

@@ -89,6 +89,10 @@ __host__ __device__ inline Workspace workspace_for(uint64_t n, int dtype, uint32
     return W;
 }
 
+// First error of a call: the status word keeps the first code written after
+// it was cleared.
+__device__ __forceinline__ void report(int* status, int code) { atomicCAS(status, SPLITZIP_OK, code); }
+
 struct EncodeLut {
     uint8_t code[256];  // exponent -> code | kEscapeFlag
 };
@@ -152,6 +156,37 @@ cudaError_t launch_decode(const DecodeArgs& a, int grid, cudaStream_t s);
 cudaError_t launch_codebook(const unsigned long long* hist, int dtype, uint8_t* cb, cudaStream_t s);
 cudaError_t launch_histogram(const void* x, uint64_t n, int dtype, unsigned long long* hist, int grid,
                              cudaStream_t s);
+
+// Small tensors and batches (batch.cu): one item of a call.  An encode item's
+// workspace has the splitzip_encode layout for its n.
+constexpr uint32_t kMaxBatch = 256;
+struct SmallEncodeItem {
+    const void* in;
+    uint64_t n;
+    void* out;
+    uint64_t* out_size;
+    void* ws;
+};
+struct SmallDecodeItem {
+    const void* in;
+    uint64_t in_bytes;
+    void* out;
+    uint64_t n;
+};
+// Batch encode: two kernels (one CTA per tile of every item; one per chunk)
+// chained with programmatic dependent launch; the status word is set by the
+// call.  codebook: host codebook bytes, or dev_codebook (then codebook is
+// unused).
+cudaError_t launch_small_encode(const SmallEncodeItem* items, uint32_t count, int dtype, const uint8_t* codebook,
+                                const uint8_t* dev_codebook, uint32_t chunk, int* status, cudaStream_t s);
+// Batch decode: a status clear, then one CTA per 8,192 elements of every item.
+cudaError_t launch_small_decode(const SmallDecodeItem* items, uint32_t count, int dtype, int* status,
+                                cudaStream_t s);
+// One small tensor encoded by one cooperative kernel (grid <= the co-resident
+// CTAs that occupancy_coop gives; n > 0).
+cudaError_t launch_coop_encode(const SmallEncodeItem& item, int dtype, const uint8_t* codebook,
+                               const uint8_t* dev_codebook, uint32_t chunk, int* status, int grid, cudaStream_t s);
+cudaError_t occupancy_coop(int* encode_blocks_per_sm, int dtype);
 
 // Resident CTAs per SM of each kernel; the encode/decode versions also raise
 // the kernels' dynamic shared-memory limit (call once per device).

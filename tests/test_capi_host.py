@@ -273,3 +273,52 @@ def test_fp16_calibrate_and_ablation_refusal(splitzip_lib):
     assert sz.splitzip_calibrate(h.ctypes.data, 0, sz.FP16, cb) == sz.ERR_INVALID_ARG
     out = ctypes.c_uint64(0)
     assert sz.splitzip_ablation_max_size(100, sz.FP16, 65536, 1, out) == sz.ERR_INVALID_ARG
+
+
+def test_batch_workspace_and_argument_errors(splitzip_lib):
+    ns = [0, 1, 70000, 1 << 20]
+    arr = (ctypes.c_uint64 * 4)(*ns)
+    out = ctypes.c_uint64(0)
+    assert sz.splitzip_encode_batch_workspace_size(arr, 4, sz.BF16, 65536, out) == sz.OK
+    assert out.value == sum(-(-sz.workspace_size(n, sz.BF16) // 256) * 256 for n in ns)
+    assert sz.splitzip_encode_batch_workspace_size(arr, 0, sz.BF16, 65536, out) == sz.ERR_INVALID_ARG
+    assert sz.splitzip_encode_batch_workspace_size(arr, 257, sz.BF16, 65536, out) == sz.ERR_INVALID_ARG
+    big = (ctypes.c_uint64 * 1)(sz.MAX_BATCH_ITEM_ELEMS + 1)
+    assert sz.splitzip_encode_batch_workspace_size(big, 1, sz.BF16, 65536, out) == sz.ERR_UNSUPPORTED
+
+    A = 1 << 20  # never dereferenced: the checks come first
+    cb = sz.Codebook.make(sz.BF16, range(16))
+    cap = sz.max_compressed_size(1000, sz.BF16)
+    ws = sz.batch_workspace_size([1000], sz.BF16)
+
+    def enc(**kw):
+        it = dict(d_in=A, n=1000, d_out=A, out_capacity=cap, d_out_size=A)
+        it.update({k: v for k, v in kw.items() if k in it})
+        items = (sz.EncodeItem * 1)(sz.EncodeItem(it["d_in"], it["n"], it["d_out"], it["out_capacity"], it["d_out_size"]))
+        return sz.splitzip_encode_batch(items, kw.get("count", 1), kw.get("dtype", sz.BF16), kw.get("cb", cb), 65536,
+                                        A, kw.get("ws", ws), kw.get("status", A), 0)
+
+    assert enc(count=0) == sz.ERR_INVALID_ARG
+    assert enc(dtype=3) == sz.ERR_INVALID_ARG
+    assert enc(cb=sz.Codebook.make(sz.FP8_E5M2, range(16))) == sz.ERR_INVALID_ARG
+    assert enc(d_in=A + 8) == sz.ERR_INVALID_ARG
+    assert enc(d_out=None) == sz.ERR_INVALID_ARG
+    assert enc(d_out_size=A + 4) == sz.ERR_INVALID_ARG
+    assert enc(out_capacity=cap - 1) == sz.ERR_CAPACITY
+    assert enc(ws=ws - 1) == sz.ERR_CAPACITY
+    assert enc(status=None) == sz.ERR_INVALID_ARG
+    assert enc(n=sz.MAX_BATCH_ITEM_ELEMS + 1, out_capacity=1 << 40) == sz.ERR_UNSUPPORTED
+
+    def dec(**kw):
+        it = dict(d_in=A, in_bytes=1 << 20, d_out=A, n=1000)
+        it.update({k: v for k, v in kw.items() if k in it})
+        items = (sz.DecodeItem * 1)(sz.DecodeItem(it["d_in"], it["in_bytes"], it["d_out"], it["n"]))
+        return sz.splitzip_decode_batch(items, kw.get("count", 1), kw.get("dtype", sz.BF16), kw.get("status", A), 0)
+
+    assert dec(count=257) == sz.ERR_INVALID_ARG
+    assert dec(dtype=7) == sz.ERR_INVALID_ARG
+    assert dec(d_in=A + 2) == sz.ERR_INVALID_ARG
+    assert dec(d_out=A + 2) == sz.ERR_INVALID_ARG
+    assert dec(in_bytes=63) == sz.ERR_CORRUPT
+    assert dec(n=sz.MAX_BATCH_ITEM_ELEMS + 1) == sz.ERR_UNSUPPORTED
+    assert dec(status=A + 1) == sz.ERR_INVALID_ARG
