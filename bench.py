@@ -70,6 +70,7 @@ def parse_args():
     p.add_argument("--no-workloads", action="store_true",
                    help="skip the per-workload object (the other four workloads, timed after the headline)")
     p.add_argument("--workload-steps", type=int, default=20, help="timed steps per workload of that object")
+    p.add_argument("--no-batch", action="store_true", help="skip the batched-call leg")
     p.add_argument("--shard", action="store_true",
                    help="under torchrun: rank r encodes and decodes chunks [r C / N, (r + 1) C / N) of one tensor "
                         "(strong scaling) instead of a replica of the whole workload (weak scaling)")
@@ -374,6 +375,81 @@ def measure_workload(name, steps, warmup, device, hbm):
            "link_model_speedup": link, "verified": ok,
            "l2": "flushed (512 MB write) before every step" if flush is not None else "inputs larger than L2"}
     del x, bufs, out, flush
+    torch.cuda.empty_cache()
+    return res
+
+
+# ---------------------------------------------------------- batches
+
+def measure_batch(dtype, device, warmup, pieces=32, steps=10):
+    """`pieces` tensors of 1,048,576 elements: per step all of them encoded
+    and decoded by single calls, or by one splitzip_encode_batch and one
+    splitzip_decode_batch; CUDA events on the launching stream, a 512 MB L2
+    flush before every step; every piece checked bit for bit."""
+    import ctypes
+    import lossless_kv_cache_gb300 as sz
+    from lossless_kv_cache_gb300 import workloads as W
+    make = W.kv_tile_k_only if dtype == 0 else (lambda seed: W.kv_cache_layer_fp16(seed, 0, tokens=512))
+    xs = [make(i).to(device) for i in range(pieces)]
+    n = xs[0].numel()
+    cb, _ = sz.calibrate(make(1000).to(device), dtype)
+    stream = torch.cuda.current_stream()
+    h = stream.cuda_stream
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=device)
+    cap = sz.max_compressed_size(n, dtype)
+    outs = torch.empty(pieces, cap, dtype=torch.uint8, device=device)
+    sizes = torch.zeros(pieces, dtype=torch.int64, device=device)
+    status = torch.zeros(4, dtype=torch.int32, device=device)
+    ys = [torch.empty_like(x) for x in xs]
+    ws1 = sz.workspace_size(n, dtype)
+    ws = torch.empty(max(sz.batch_workspace_size([n] * pieces, dtype), ws1, 16), dtype=torch.uint8, device=device)
+    enc_items = (sz.EncodeItem * pieces)(*[sz.EncodeItem(x.data_ptr(), n, outs[i].data_ptr(), cap,
+                                                         sizes.data_ptr() + 8 * i) for i, x in enumerate(xs)])
+    dec_items = (sz.DecodeItem * pieces)(*[sz.DecodeItem(outs[i].data_ptr(), cap, ys[i].data_ptr(), n)
+                                           for i in range(pieces)])
+    ws_batch = ws.numel()
+
+    def singles():
+        for i, x in enumerate(xs):
+            st = sz.splitzip_encode(x.data_ptr(), n, dtype, cb, CHUNK, outs[i].data_ptr(), cap, ws.data_ptr(), ws1,
+                                    sizes.data_ptr() + 8 * i, status.data_ptr(), h)
+            st |= sz.splitzip_decode(outs[i].data_ptr(), cap, ys[i].data_ptr(), n, dtype, status.data_ptr() + 4, h)
+            if st != sz.OK:
+                raise sz.SplitZipError(st, "single calls")
+
+    def batched():
+        st = sz.splitzip_encode_batch(enc_items, pieces, dtype, cb, CHUNK, ws.data_ptr(), ws_batch, status.data_ptr(), h)
+        st |= sz.splitzip_decode_batch(dec_items, pieces, dtype, status.data_ptr() + 4, h)
+        if st != sz.OK:
+            raise sz.SplitZipError(st, "batched calls")
+
+    res = {}
+    for label, fn in (("single_calls", singles), ("batched", batched)):
+        for _ in range(max(warmup, 3)):
+            fn()
+        torch.cuda.synchronize()
+        for y in ys:
+            y.fill_(0)
+        ts = []
+        for _ in range(steps):
+            flush.fill_(5)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(b))
+        ok = int(status[0]) == sz.OK and int(status[1]) == sz.OK and all(torch.equal(x, y) for x, y in zip(xs, ys))
+        ms = statistics.median(ts)
+        res[label] = {"ms_per_step": round(ms, 4), "us_per_piece": round(1e3 * ms / pieces, 3),
+                      "round_trip_gbs": round(pieces * n * 2 / (ms * 1e-3) / 1e9, 2), "verified": ok}
+    res["pieces"] = pieces
+    res["piece_elems"] = n
+    res["element_dtype"] = ELEMENT_DTYPE[dtype]
+    res["speedup"] = round(res["single_calls"]["ms_per_step"] / res["batched"]["ms_per_step"], 3)
+    res["what"] = ("per step every piece encoded and decoded (round trip), L2 flushed before the step; median of %d "
+                   "steps" % steps)
+    del xs, ys, outs, ws, flush
     torch.cuda.empty_cache()
     return res
 
@@ -874,6 +950,13 @@ def run_ours(args, world, rank, local):
         shard = {"elements": n, "range": list(shard_range(wl.n, CHUNK, world, rank)), "escape_base": base,
                  "joined_escapes": E_all, "joined_bytes": joined, "joined_ratio": round(wl.elem_bytes * wl.n / joined, 5)}
 
+    # ---- batches: 32 per-layer K tiles of 1,048,576 elements (the kv-tile
+    # recipe, seeds 0..31) as 32 single encode + decode calls against one
+    # batched encode and one batched decode (L2 flushed before each step) ----
+    batch = None
+    if not args.no_batch and not args.shard:
+        batch = measure_batch(dtype if dtype != 1 else 0, device, args.warmup)
+
     # ---- the other workloads (one line carries all five), timed after the
     # headline's buffers are released ----
     workloads = None
@@ -903,7 +986,7 @@ def run_ours(args, world, rank, local):
         "per_kernel": per_kernel, "link_model": link,
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clk,
         "transfer": transfer, "online_calibration": online, "paged": paged, "ablation": ablation,
-        "workloads": workloads,
+        "workloads": workloads, "batch": batch,
         "gpu_launches": 5 * K,  # timed steps: encode (streaming, group, index, records kernels) + decode
     }
 
