@@ -101,7 +101,10 @@ def test_traffic_table_agrees_with_its_profiles():
     # one decimal) is the figure the bench line reports
     for (workload, op), t in bench.TRAFFIC.items():
         with open(os.path.join(bench.ROOT, t["profile"])) as f:
-            rows = [line.split("|") for line in f if line.startswith("| %s" % op)]
+            lines = f.readlines()
+        header = [c.strip() for c in next(l for l in lines if l.startswith("| call |")).split("|")]
+        col = header.index("DRAM traffic MB")
+        rows = [line.split("|") for line in lines if line.startswith("| %s" % op)]
         assert len(rows) == 1, (workload, op)
-        printed = float(rows[0][3].strip().split()[0].replace(",", ""))
+        printed = float(rows[0][col].strip().split()[0].replace(",", ""))
         assert printed == round(t["bytes"] / 1e6, 1), (workload, op, printed, t["bytes"])
