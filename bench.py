@@ -142,24 +142,24 @@ _ENC_SOURCES = ('encode.cu', 'encode_core.cuh', 'tma_pipeline.cuh', 'splitzip_in
 _DEC_SOURCES = ('decode.cu', 'decode_core.cuh', 'tma_pipeline.cuh', 'splitzip_internal.cuh')
 TRAFFIC = {
     ("kv_cache_32x2x32768x8x128_bf16", "encode"): {
-        "bytes": 8094598912, "sources": _ENC_SOURCES,
-        "sha256": "ebf95f8bea582450107ab200c9ad62b4bc210ef331d7f9c5a24b5b28dfcb235a",
+        "bytes": 8094703104, "sources": _ENC_SOURCES,
+        "sha256": "04b4d7872e8cb1e7b95fab7079a4dafc77d4ecdd5e224b850979229c887700cf",
         "profile": "profiles/launches_kv_cache_32x2x32768x8x128_bf16.md"},
     ("kv_cache_32x2x32768x8x128_bf16", "decode"): {
         "bytes": 7645132800, "sources": _DEC_SOURCES,
         "sha256": "d8321a995cfc98490c2239d82f7b57ab5cb8b211cd6c7e46aab6f4ce0544df86",
         "profile": "profiles/launches_kv_cache_32x2x32768x8x128_bf16.md"},
     ("kv_cache_32x2x65536x8x128_e5m2", "encode"): {
-        "bytes": 9082540800, "sources": _ENC_SOURCES,
-        "sha256": "ebf95f8bea582450107ab200c9ad62b4bc210ef331d7f9c5a24b5b28dfcb235a",
+        "bytes": 9082554112, "sources": _ENC_SOURCES,
+        "sha256": "04b4d7872e8cb1e7b95fab7079a4dafc77d4ecdd5e224b850979229c887700cf",
         "profile": "profiles/launches_kv_cache_32x2x65536x8x128_e5m2.md"},
     ("kv_cache_32x2x65536x8x128_e5m2", "decode"): {
         "bytes": 8306477568, "sources": _DEC_SOURCES,
         "sha256": "d8321a995cfc98490c2239d82f7b57ab5cb8b211cd6c7e46aab6f4ce0544df86",
         "profile": "profiles/launches_kv_cache_32x2x65536x8x128_e5m2.md"},
     ("kv_cache_32x2x32768x8x128_fp16", "encode"): {
-        "bytes": 8914620416, "sources": _ENC_SOURCES,
-        "sha256": "ebf95f8bea582450107ab200c9ad62b4bc210ef331d7f9c5a24b5b28dfcb235a",
+        "bytes": 8899547392, "sources": _ENC_SOURCES,
+        "sha256": "04b4d7872e8cb1e7b95fab7079a4dafc77d4ecdd5e224b850979229c887700cf",
         "profile": "profiles/launches_kv_cache_32x2x32768x8x128_fp16.md"},
     ("kv_cache_32x2x32768x8x128_fp16", "decode"): {
         "bytes": 8428215808, "sources": _DEC_SOURCES,
