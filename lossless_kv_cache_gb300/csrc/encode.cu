@@ -10,18 +10,20 @@
 // Four kernels, no inter-block waits:
 //   encode_kernel (the streaming pass, persistent CTAs of 8 consumer warps +
 //     1 producer warp): the producer streams each of the CTA's 16 KB tiles
-//     into a 4-stage shared-memory ring with tensor-map copies (TMA,
+//     into a shared-memory ring (BF16 8 stages at one CTA per SM, E5M2 and
+//     FP16 4 stages at two) with tensor-map copies (TMA,
 //     cp.async.bulk.tensor, 128-byte swizzle, mbarrier); every consumer
 //     thread owns 64 contiguous bytes of the tile.  Per element it does one
 //     shared-memory lookup in a table for the element's position within its
 //     group of four; the table entries already sit at their final bit
 //     positions, so the sum of four entries is the group's two nibble bytes,
 //     its escape flags and (E5M2) its packed 3-bit sign|mantissa values.  The
-//     nibble and sign|mantissa streams go out with 16-byte stores; a warp scan
-//     orders the warp's escapes, each thread writes its own contiguously into
-//     the warp's region of the tile's staging slot after those of the lower
-//     lanes, and the warp's count goes to the workspace; no synchronisation
-//     between the warps.
+//     nibble and sign|mantissa streams go out with 16-byte stores (FP16's
+//     11-bit stream by way of a per-warp shared-memory transpose); a warp
+//     scan orders the warp's escapes, each thread writes its own contiguously
+//     into the warp's region of the tile's staging slot after those of the
+//     lower lanes, and the warp's count goes to the workspace; no
+//     synchronisation between the warps.
 //   encode_group_kernel (one CTA per group of 256 tiles): the group's total.
 //   encode_index_kernel (one CTA per group of 256 tiles): the sum of the
 //     earlier groups' totals plus a block scan of the group's tile counts give
