@@ -143,7 +143,7 @@ _DEC_SOURCES = ('decode.cu', 'decode_core.cuh', 'tma_pipeline.cuh', 'splitzip_in
 TRAFFIC = {
     ("kv_cache_32x2x32768x8x128_bf16", "encode"): {
         "bytes": 8094703104, "sources": _ENC_SOURCES,
-        "sha256": "6961494a314a9c63c310542f8de9535b9ee1beb1f838bf78cec91e14a7802bca",
+        "sha256": "b9d2429a3c9e0fc6620e6962b5084c0bf8f2119f6531fc1381c90c32a958aca9",
         "profile": "profiles/launches_kv_cache_32x2x32768x8x128_bf16.md"},
     ("kv_cache_32x2x32768x8x128_bf16", "decode"): {
         "bytes": 7645132800, "sources": _DEC_SOURCES,
@@ -151,7 +151,7 @@ TRAFFIC = {
         "profile": "profiles/launches_kv_cache_32x2x32768x8x128_bf16.md"},
     ("kv_cache_32x2x65536x8x128_e5m2", "encode"): {
         "bytes": 9082554112, "sources": _ENC_SOURCES,
-        "sha256": "6961494a314a9c63c310542f8de9535b9ee1beb1f838bf78cec91e14a7802bca",
+        "sha256": "b9d2429a3c9e0fc6620e6962b5084c0bf8f2119f6531fc1381c90c32a958aca9",
         "profile": "profiles/launches_kv_cache_32x2x65536x8x128_e5m2.md"},
     ("kv_cache_32x2x65536x8x128_e5m2", "decode"): {
         "bytes": 8306477568, "sources": _DEC_SOURCES,
@@ -159,7 +159,7 @@ TRAFFIC = {
         "profile": "profiles/launches_kv_cache_32x2x65536x8x128_e5m2.md"},
     ("kv_cache_32x2x32768x8x128_fp16", "encode"): {
         "bytes": 8899547392, "sources": _ENC_SOURCES,
-        "sha256": "6961494a314a9c63c310542f8de9535b9ee1beb1f838bf78cec91e14a7802bca",
+        "sha256": "b9d2429a3c9e0fc6620e6962b5084c0bf8f2119f6531fc1381c90c32a958aca9",
         "profile": "profiles/launches_kv_cache_32x2x32768x8x128_fp16.md"},
     ("kv_cache_32x2x32768x8x128_fp16", "decode"): {
         "bytes": 8428215808, "sources": _DEC_SOURCES,

@@ -179,7 +179,11 @@ __global__ void __launch_bounds__(kBlock, kMinBlocks<DT>)
 
         // Full-size tiles delivered whole take a copy of the body in which
         // every bounds test folds away at compile time; in the other copy each
-        // thread handles only its `ne` elements of the tile.
+        // thread handles only its `ne` elements of the tile.  The stores and
+        // the record staging are written out here rather than through the
+        // small-tensor encoder's helpers (store_streams, stage_records): this
+        // loop is bound by its per-tile latency chain, and the helper-based
+        // body measured 2.8 % slower on the BF16 cache.
         auto body = [&](auto full_tag) {
             constexpr bool FULL = decltype(full_tag)::value;
             // elements of this thread in the tile (all TE of them in a full tile)
