@@ -7,9 +7,10 @@ These cases have more tiles than that, so they exercise the streaming
 encoder's partial-tile body: a ragged last tile, the last bytes past the
 tensor map's whole 128-byte rows, tiles smaller than 16 KB throughout (chunks
 of 64 and 4,096 elements), and FP16's per-thread stores beside its
-shared-memory transpose.  Above 2^21 elements the decode is the streaming
-decoder too.  Each container must equal the oracle's byte for byte, and both
-containers must decode on the GPU to the input (tolerance 0: integer work).
+shared-memory transpose.  Every case is also above 2^21 elements, so its
+decode is the streaming decoder's too.  Each container must equal the
+oracle's byte for byte, and both containers must decode on the GPU to the
+input (tolerance 0: integer work).
 """
 import numpy as np
 import pytest
@@ -21,7 +22,8 @@ from tests.test_gpu_parity import roundtrip_vs_oracle
 
 pytestmark = pytest.mark.gpu
 
-SMALL_PATH_MAX_TILES = 8192  # the C ABI's small-tensor threshold (tiles of one call)
+SMALL_PATH_MAX_TILES = 8192  # the C ABI's small-tensor encode threshold (tiles of one call)
+SMALL_DECODE_MAX_ELEMS = 1 << 21  # and its small-tensor decode threshold
 TILE_BYTES = 16384
 
 
@@ -61,7 +63,8 @@ def _input(dtype, n, seed):
 @pytest.mark.parametrize("chunk,extra", [(64, 37), (4096, 5), (65536, 777)])
 def test_streaming_encoder_ragged(dtype, chunk, extra):
     te = _tile_elems(dtype, chunk)
-    n = (SMALL_PATH_MAX_TILES + 1) * te + extra  # one tile past the small path, then a ragged tail
-    assert -(-n // te) > SMALL_PATH_MAX_TILES
+    # past both small-tensor limits, then a ragged tail
+    n = max((SMALL_PATH_MAX_TILES + 1) * te, SMALL_DECODE_MAX_ELEMS) + extra
+    assert -(-n // te) > SMALL_PATH_MAX_TILES and n > SMALL_DECODE_MAX_ELEMS
     x, cb = _input(dtype, n, seed=chunk + dtype)
     roundtrip_vs_oracle(x, dtype, cb, chunk)
