@@ -142,24 +142,24 @@ _ENC_SOURCES = ('encode.cu', 'encode_core.cuh', 'tma_pipeline.cuh', 'splitzip_in
 _DEC_SOURCES = ('decode.cu', 'decode_core.cuh', 'tma_pipeline.cuh', 'splitzip_internal.cuh')
 TRAFFIC = {
     ("kv_cache_32x2x32768x8x128_bf16", "encode"): {
-        "bytes": 8094703104, "sources": _ENC_SOURCES,
-        "sha256": "b9d2429a3c9e0fc6620e6962b5084c0bf8f2119f6531fc1381c90c32a958aca9",
+        "bytes": 8094332672, "sources": _ENC_SOURCES,
+        "sha256": "9217e4744acd0af809a8d324b8dd0ed304e46e1e71df9964714513941fb28543",
         "profile": "profiles/launches_kv_cache_32x2x32768x8x128_bf16.md"},
     ("kv_cache_32x2x32768x8x128_bf16", "decode"): {
         "bytes": 7645132800, "sources": _DEC_SOURCES,
         "sha256": "d8321a995cfc98490c2239d82f7b57ab5cb8b211cd6c7e46aab6f4ce0544df86",
         "profile": "profiles/launches_kv_cache_32x2x32768x8x128_bf16.md"},
     ("kv_cache_32x2x65536x8x128_e5m2", "encode"): {
-        "bytes": 9082554112, "sources": _ENC_SOURCES,
-        "sha256": "b9d2429a3c9e0fc6620e6962b5084c0bf8f2119f6531fc1381c90c32a958aca9",
+        "bytes": 9081885952, "sources": _ENC_SOURCES,
+        "sha256": "9217e4744acd0af809a8d324b8dd0ed304e46e1e71df9964714513941fb28543",
         "profile": "profiles/launches_kv_cache_32x2x65536x8x128_e5m2.md"},
     ("kv_cache_32x2x65536x8x128_e5m2", "decode"): {
         "bytes": 8306477568, "sources": _DEC_SOURCES,
         "sha256": "d8321a995cfc98490c2239d82f7b57ab5cb8b211cd6c7e46aab6f4ce0544df86",
         "profile": "profiles/launches_kv_cache_32x2x65536x8x128_e5m2.md"},
     ("kv_cache_32x2x32768x8x128_fp16", "encode"): {
-        "bytes": 8899547392, "sources": _ENC_SOURCES,
-        "sha256": "b9d2429a3c9e0fc6620e6962b5084c0bf8f2119f6531fc1381c90c32a958aca9",
+        "bytes": 8898562816, "sources": _ENC_SOURCES,
+        "sha256": "9217e4744acd0af809a8d324b8dd0ed304e46e1e71df9964714513941fb28543",
         "profile": "profiles/launches_kv_cache_32x2x32768x8x128_fp16.md"},
     ("kv_cache_32x2x32768x8x128_fp16", "decode"): {
         "bytes": 8428215808, "sources": _DEC_SOURCES,

@@ -31,6 +31,11 @@
 //     entries of the group's chunks; the last group writes E and the size.
 //   encode_records_kernel (a warp per 4 tiles): moves every tile's staged
 //     records to their place in the escape stream.
+// The three short kernels are launched with programmatic stream
+// serialization: each is scheduled while its predecessor drains (the
+// streaming kernel lets it once every CTA has issued its last copy) and waits
+// in griddepcontrol.wait for that grid to complete before it reads its
+// results (BF16 cache encode 1.327 -> 1.305 ms, same-box timing).
 #include <type_traits>
 
 #include "encode_core.cuh"
@@ -145,6 +150,9 @@ __global__ void __launch_bounds__(kBlock, kMinBlocks<DT>)
                 mbar_arrive(&full_bar[stage]);  // the consumers read this tile from global memory
             }
         }
+        // every copy of this CTA is issued: the call's next kernel may be
+        // scheduled (it waits for this grid to complete before it reads)
+        asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
         if (!drain_stages(full_bar, kStages, it)) report(a.error, SPLITZIP_ERR_TIMEOUT);
         return;
     }
@@ -376,6 +384,11 @@ __device__ __forceinline__ uint32_t tile_count(const EncodeArgs& a, uint64_t t) 
 // One CTA per group of kGroupTiles tiles: the group's escape total (a plain
 // store, so the streaming pass needs no atomics and the totals no clearing).
 __global__ void __launch_bounds__(kFinishThreads) encode_group_kernel(const EncodeArgs a) {
+    // launched early (programmatic dependent launch): wait for the previous
+    // kernel of the call to complete and its writes to be visible, then let
+    // the next one be scheduled (it waits for this one in turn)
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     __shared__ uint32_t warp_sum[kFinishThreads / 32];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const uint64_t t = uint64_t(blockIdx.x) * kGroupTiles + tid;
@@ -396,6 +409,11 @@ __global__ void __launch_bounds__(kFinishThreads) encode_group_kernel(const Enco
 // chunk is a power of two <= 8): the first record index of every tile of the
 // group, the index entries of the group's chunks, and E from the last group.
 __global__ void __launch_bounds__(kFinishThreads) encode_index_kernel(const EncodeArgs a) {
+    // launched early (programmatic dependent launch): wait for the previous
+    // kernel of the call to complete and its writes to be visible, then let
+    // the next one be scheduled (it waits for this one in turn)
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     constexpr int kWarps = kFinishThreads / 32;
     __shared__ uint64_t warp_part[kWarps];
     __shared__ uint32_t warp_incl[kWarps];
@@ -458,6 +476,9 @@ constexpr int kRecordThreads = 256;
 static_assert(kRecordTiles * kEncodeWarps == 32, "one lane per (tile, consumer warp)");
 
 __global__ void __launch_bounds__(kRecordThreads) encode_records_kernel(const EncodeArgs a) {
+    // launched early (programmatic dependent launch): wait for the previous
+    // kernel of the call to complete and its writes to be visible
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int lane = threadIdx.x & 31;
     const uint64_t t0 = (uint64_t(blockIdx.x) * (kRecordThreads / 32) + (threadIdx.x >> 5)) * kRecordTiles;
     if (t0 >= a.n_tiles) return;
@@ -523,6 +544,23 @@ __global__ void __launch_bounds__(kRecordThreads) encode_records_kernel(const En
     }
 }
 
+// Launch with programmatic stream serialization: the kernel's CTAs may be
+// scheduled while the previous kernel in the stream drains; each waits for it
+// in griddepcontrol.wait before reading anything it wrote.
+template <typename Kernel>
+cudaError_t launch_dependent(Kernel kernel, unsigned grid, unsigned block, cudaStream_t s, const EncodeArgs& a) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(block);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, a);
+}
+
 }  // namespace
 
 cudaError_t launch_encode(const EncodeArgs& a, const EncodeLut& lut, const CUtensorMap& map, int grid,
@@ -535,14 +573,11 @@ cudaError_t launch_encode(const EncodeArgs& a, const EncodeLut& lut, const CUten
         encode_kernel<SPLITZIP_FP8_E5M2><<<grid, kBlock, kEncodeSmem<SPLITZIP_FP8_E5M2>, s>>>(a, map, lut);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess || a.n_groups == 0) return e;
-    encode_group_kernel<<<unsigned(a.n_groups), kFinishThreads, 0, s>>>(a);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    encode_index_kernel<<<unsigned(a.n_groups), kFinishThreads, 0, s>>>(a);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if ((e = launch_dependent(encode_group_kernel, unsigned(a.n_groups), kFinishThreads, s, a)) != cudaSuccess) return e;
+    if ((e = launch_dependent(encode_index_kernel, unsigned(a.n_groups), kFinishThreads, s, a)) != cudaSuccess) return e;
     const uint64_t warps = (a.n_tiles + kRecordTiles - 1) / kRecordTiles;
-    encode_records_kernel<<<unsigned((warps + kRecordThreads / 32 - 1) / (kRecordThreads / 32)), kRecordThreads, 0,
-                            s>>>(a);
-    return cudaGetLastError();
+    return launch_dependent(encode_records_kernel,
+                            unsigned((warps + kRecordThreads / 32 - 1) / (kRecordThreads / 32)), kRecordThreads, s, a);
 }
 
 cudaError_t occupancy_encode(int* blocks_per_sm, int dtype) {
