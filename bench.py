@@ -142,28 +142,28 @@ _ENC_SOURCES = ('encode.cu', 'encode_core.cuh', 'tma_pipeline.cuh', 'splitzip_in
 _DEC_SOURCES = ('decode.cu', 'decode_core.cuh', 'tma_pipeline.cuh', 'splitzip_internal.cuh')
 TRAFFIC = {
     ("kv_cache_32x2x32768x8x128_bf16", "encode"): {
-        "bytes": 8094332672, "sources": _ENC_SOURCES,
-        "sha256": "9217e4744acd0af809a8d324b8dd0ed304e46e1e71df9964714513941fb28543",
+        "bytes": 8094123264, "sources": _ENC_SOURCES,
+        "sha256": "e20cbcf7be70cf4493210d5db80401d531b9d6386a6b9755f517282decc2d489",
         "profile": "profiles/launches_kv_cache_32x2x32768x8x128_bf16.md"},
     ("kv_cache_32x2x32768x8x128_bf16", "decode"): {
-        "bytes": 7645132800, "sources": _DEC_SOURCES,
-        "sha256": "d8321a995cfc98490c2239d82f7b57ab5cb8b211cd6c7e46aab6f4ce0544df86",
+        "bytes": 7641231104, "sources": _DEC_SOURCES,
+        "sha256": "77df22b2c26f6787138c817c4963244aacac423b302050ebec756faf753e9646",
         "profile": "profiles/launches_kv_cache_32x2x32768x8x128_bf16.md"},
     ("kv_cache_32x2x65536x8x128_e5m2", "encode"): {
-        "bytes": 9081885952, "sources": _ENC_SOURCES,
-        "sha256": "9217e4744acd0af809a8d324b8dd0ed304e46e1e71df9964714513941fb28543",
+        "bytes": 9082352384, "sources": _ENC_SOURCES,
+        "sha256": "e20cbcf7be70cf4493210d5db80401d531b9d6386a6b9755f517282decc2d489",
         "profile": "profiles/launches_kv_cache_32x2x65536x8x128_e5m2.md"},
     ("kv_cache_32x2x65536x8x128_e5m2", "decode"): {
-        "bytes": 8306477568, "sources": _DEC_SOURCES,
-        "sha256": "d8321a995cfc98490c2239d82f7b57ab5cb8b211cd6c7e46aab6f4ce0544df86",
+        "bytes": 8305438976, "sources": _DEC_SOURCES,
+        "sha256": "77df22b2c26f6787138c817c4963244aacac423b302050ebec756faf753e9646",
         "profile": "profiles/launches_kv_cache_32x2x65536x8x128_e5m2.md"},
     ("kv_cache_32x2x32768x8x128_fp16", "encode"): {
-        "bytes": 8898562816, "sources": _ENC_SOURCES,
-        "sha256": "9217e4744acd0af809a8d324b8dd0ed304e46e1e71df9964714513941fb28543",
+        "bytes": 8899424000, "sources": _ENC_SOURCES,
+        "sha256": "e20cbcf7be70cf4493210d5db80401d531b9d6386a6b9755f517282decc2d489",
         "profile": "profiles/launches_kv_cache_32x2x32768x8x128_fp16.md"},
     ("kv_cache_32x2x32768x8x128_fp16", "decode"): {
-        "bytes": 8428215808, "sources": _DEC_SOURCES,
-        "sha256": "d8321a995cfc98490c2239d82f7b57ab5cb8b211cd6c7e46aab6f4ce0544df86",
+        "bytes": 8429386240, "sources": _DEC_SOURCES,
+        "sha256": "77df22b2c26f6787138c817c4963244aacac423b302050ebec756faf753e9646",
         "profile": "profiles/launches_kv_cache_32x2x32768x8x128_fp16.md"},
 }
 

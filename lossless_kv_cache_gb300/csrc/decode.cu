@@ -95,6 +95,25 @@ __device__ __forceinline__ void decode_subtile(const uint8_t* nb, const uint8_t*
     constexpr uint32_t UE = DT == SPLITZIP_FP8_E5M2 ? 16u : 8u;
     const uint32_t units = (cnt + UE - 1u) / UE;
     const uint32_t rounds = (units + kConsumers - 1u) / kConsumers;
+    // paged output: a sub-tile that lies in one page takes one page-table
+    // lookup for all its units (the same decision in every thread)
+    [[maybe_unused]] bool one_page = false, page_ok = true;
+    [[maybe_unused]] uint64_t page_off = 0;
+    if constexpr (PAGED) {
+        if (cnt > 0 && (g >> om.shift) == ((g + cnt - 1u) >> om.shift)) {
+            one_page = true;
+            page_ok = om.at(g, EB, page_off);
+        }
+    }
+    auto out_at = [&](uint32_t e, uint64_t& off) -> bool {
+        if constexpr (PAGED) {
+            if (one_page) {
+                off = page_off + uint64_t(e) * EB;
+                return page_ok;
+            }
+        }
+        return om.at(g + e, EB, off);
+    };
 #pragma unroll 2
     for (uint32_t k = 0; k < rounds; ++k) {
         const uint32_t u = k * kConsumers + uint32_t(tid);
@@ -119,7 +138,7 @@ __device__ __forceinline__ void decode_subtile(const uint8_t* nb, const uint8_t*
                 o = decode_unit_e5m2(nib, s3lo, s3hi, lut2);
             }
             uint64_t off;
-            if (om.at(g + e, EB, off)) __stcs(reinterpret_cast<uint4*>(om.base + off), o);
+            if (out_at(e, off)) __stcs(reinterpret_cast<uint4*>(om.base + off), o);
         } else if (e < cnt) {
             const uint32_t valid = cnt - e;
             uint4 o;
@@ -144,7 +163,7 @@ __device__ __forceinline__ void decode_subtile(const uint8_t* nb, const uint8_t*
                                      lut2);
             }
             uint64_t off;
-            if (om.at(g + e, EB, off)) {
+            if (out_at(e, off)) {
                 for (uint32_t b = 0; b < valid; ++b) {
                     const uint32_t q = EB == 2 ? b >> 1 : b >> 2;
                     const uint32_t w = q == 0 ? o.x : q == 1 ? o.y : q == 2 ? o.z : o.w;

@@ -119,42 +119,126 @@ __global__ void __launch_bounds__(kBlock, kMinBlocks<DT>)
 
     const uint8_t* in = static_cast<const uint8_t*>(a.in);
     const uint32_t tile_bytes = a.tile_elems * EB;
-    if (warp == kConsumerWarps) {
-        // ---- producer: stream the CTA's tiles (blockIdx.x + k * gridDim.x) ----
-        if (lane != 0) return;
-        // the pool tile that holds tile t (paged input; a page index outside
-        // the pool is reported and read as page 0, inside the pool)
-        auto source_tile = [&](uint64_t t) -> uint64_t {
-            if (!a.pages) return t;
-            int64_t p = a.pages[t >> a.page_tile_shift];
-            if (p < 0 || uint64_t(p) >= a.pool_pages) {
-                report(a.error, SPLITZIP_ERR_INVALID_ARG);
-                p = 0;
+    // ---- the producer warp ----
+    if constexpr (DT == SPLITZIP_BF16) {
+        // BF16, bound by HBM, is sensitive to its producer's pace: paged input
+        // gets the page indices loaded 32 tiles ahead by the whole warp (a
+        // one-tile lookahead whose check waited on the load cost paged BF16
+        // 9 %), and contiguous input a loop with no page lookup at all.  E5M2
+        // and FP16, whose consumers are bound by integer work, measured 0.5-1 %
+        // slower with the warp-wide lookup and keep the single-lane producer.
+        if (warp == kConsumerWarps && a.pages) {
+            // ---- producer warp, paged input: lane 0 streams the CTA's tiles
+            // (blockIdx.x + k * gridDim.x) from the pool; the whole warp loads the
+            // page indices of the CTA's tiles 32 to 63 tiles ahead, so lane 0
+            // never waits on a page-table load ----
+            const uint64_t G = gridDim.x;
+            auto raw_page = [&](uint64_t t) -> int32_t {  // checked where it is used
+                return t < a.n_tiles ? a.pages[t >> a.page_tile_shift] : 0;
+            };
+            // page of tile (batch + lane) of this and of the next batch of 32
+            int32_t pg_cur = raw_page(blockIdx.x + uint64_t(lane) * G);
+            int32_t pg_next = raw_page(blockIdx.x + uint64_t(32 + lane) * G);
+            uint32_t it = 0;
+            for (uint64_t t = blockIdx.x; t < a.n_tiles; t += G, ++it) {
+                const uint32_t stage = it % kStages, use = it / kStages, j = it & 31u;
+                if (j == 0 && it > 0) {
+                    pg_cur = pg_next;
+                    pg_next = raw_page(t + uint64_t(32 + lane) * G);
+                }
+                // the pool tile that holds tile t; a page index outside the pool
+                // is reported and read as page 0, inside the pool
+                int64_t p = __shfl_sync(kFull, pg_cur, int(j));
+                if (p < 0 || uint64_t(p) >= a.pool_pages) {
+                    if (lane == 0) report(a.error, SPLITZIP_ERR_INVALID_ARG);
+                    p = 0;
+                }
+                const uint64_t src =
+                    (uint64_t(p) << a.page_tile_shift) | (t & ((uint64_t(1) << a.page_tile_shift) - 1u));
+                if (use > 0 && !mbar_wait(&empty_bar[stage], (use - 1) & 1u) && lane == 0)
+                    report(a.error, SPLITZIP_ERR_TIMEOUT);
+                if (lane == 0) {
+                    const uint64_t tb = src * tile_bytes;
+                    if (tb < a.tensor_bytes) {
+                        mbar_arrive_expect_tx(&full_bar[stage], a.box_bytes);
+                        tensor_load_2d(ring + stage * kStageBytes, &map, int32_t((tb & 127u) / EB), int32_t(tb >> 7),
+                                       &full_bar[stage]);
+                    } else {
+                        mbar_arrive(&full_bar[stage]);  // the consumers read this tile from global memory
+                    }
+                }
+                __syncwarp();
             }
-            return (uint64_t(p) << a.page_tile_shift) | (t & ((uint64_t(1) << a.page_tile_shift) - 1u));
-        };
-        uint32_t it = 0;
-        uint64_t src_next = blockIdx.x < a.n_tiles ? source_tile(blockIdx.x) : 0;
-        for (uint64_t t = blockIdx.x; t < a.n_tiles; t += gridDim.x, ++it) {
-            const uint32_t stage = it % kStages, use = it / kStages;
-            const uint64_t src = src_next;
-            // the next tile's page lookup is issued before this stage's wait
-            if (t + gridDim.x < a.n_tiles) src_next = source_tile(t + gridDim.x);
-            if (use > 0 && !mbar_wait(&empty_bar[stage], (use - 1) & 1u)) report(a.error, SPLITZIP_ERR_TIMEOUT);
-            const uint64_t tb = src * tile_bytes;
-            if (tb < a.tensor_bytes) {
-                mbar_arrive_expect_tx(&full_bar[stage], a.box_bytes);
-                tensor_load_2d(ring + stage * kStageBytes, &map, int32_t((tb & 127u) / EB), int32_t(tb >> 7),
-                               &full_bar[stage]);
-            } else {
-                mbar_arrive(&full_bar[stage]);  // the consumers read this tile from global memory
+            if (lane == 0) {
+                // every copy of this CTA is issued: the call's next kernel may be
+                // scheduled (it waits for this grid to complete before it reads)
+                asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+                if (!drain_stages(full_bar, kStages, it)) report(a.error, SPLITZIP_ERR_TIMEOUT);
             }
+            return;
         }
-        // every copy of this CTA is issued: the call's next kernel may be
-        // scheduled (it waits for this grid to complete before it reads)
-        asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-        if (!drain_stages(full_bar, kStages, it)) report(a.error, SPLITZIP_ERR_TIMEOUT);
-        return;
+
+        if (warp == kConsumerWarps) {
+            // ---- producer, contiguous input: stream the CTA's tiles
+            // (blockIdx.x + k * gridDim.x) ----
+            if (lane != 0) return;
+            uint32_t it = 0;
+            for (uint64_t t = blockIdx.x; t < a.n_tiles; t += gridDim.x, ++it) {
+                const uint32_t stage = it % kStages, use = it / kStages;
+                if (use > 0 && !mbar_wait(&empty_bar[stage], (use - 1) & 1u)) report(a.error, SPLITZIP_ERR_TIMEOUT);
+                const uint64_t tb = t * tile_bytes;
+                if (tb < a.tensor_bytes) {
+                    mbar_arrive_expect_tx(&full_bar[stage], a.box_bytes);
+                    tensor_load_2d(ring + stage * kStageBytes, &map, int32_t((tb & 127u) / EB), int32_t(tb >> 7),
+                                   &full_bar[stage]);
+                } else {
+                    mbar_arrive(&full_bar[stage]);  // the consumers read this tile from global memory
+                }
+            }
+            // every copy of this CTA is issued: the call's next kernel may be
+            // scheduled (it waits for this grid to complete before it reads)
+            asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+            if (!drain_stages(full_bar, kStages, it)) report(a.error, SPLITZIP_ERR_TIMEOUT);
+            return;
+        }
+    } else {
+        if (warp == kConsumerWarps) {
+            // ---- producer: stream the CTA's tiles (blockIdx.x + k * gridDim.x) ----
+            if (lane != 0) return;
+            // the pool tile that holds tile t (paged input; a page index outside
+            // the pool is reported and read as page 0, inside the pool)
+            auto source_tile = [&](uint64_t t) -> uint64_t {
+                if (!a.pages) return t;
+                int64_t p = a.pages[t >> a.page_tile_shift];
+                if (p < 0 || uint64_t(p) >= a.pool_pages) {
+                    report(a.error, SPLITZIP_ERR_INVALID_ARG);
+                    p = 0;
+                }
+                return (uint64_t(p) << a.page_tile_shift) | (t & ((uint64_t(1) << a.page_tile_shift) - 1u));
+            };
+            uint32_t it = 0;
+            uint64_t src_next = blockIdx.x < a.n_tiles ? source_tile(blockIdx.x) : 0;
+            for (uint64_t t = blockIdx.x; t < a.n_tiles; t += gridDim.x, ++it) {
+                const uint32_t stage = it % kStages, use = it / kStages;
+                const uint64_t src = src_next;
+                // the next tile's page lookup is issued before this stage's wait
+                if (t + gridDim.x < a.n_tiles) src_next = source_tile(t + gridDim.x);
+                if (use > 0 && !mbar_wait(&empty_bar[stage], (use - 1) & 1u)) report(a.error, SPLITZIP_ERR_TIMEOUT);
+                const uint64_t tb = src * tile_bytes;
+                if (tb < a.tensor_bytes) {
+                    mbar_arrive_expect_tx(&full_bar[stage], a.box_bytes);
+                    tensor_load_2d(ring + stage * kStageBytes, &map, int32_t((tb & 127u) / EB), int32_t(tb >> 7),
+                                   &full_bar[stage]);
+                } else {
+                    mbar_arrive(&full_bar[stage]);  // the consumers read this tile from global memory
+                }
+            }
+            // every copy of this CTA is issued: the call's next kernel may be
+            // scheduled (it waits for this grid to complete before it reads)
+            asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+            if (!drain_stages(full_bar, kStages, it)) report(a.error, SPLITZIP_ERR_TIMEOUT);
+            return;
+        }
     }
 
     // ---- consumers: thread `tid` owns bytes [64 tid, 64 tid + 64) of a tile ----
