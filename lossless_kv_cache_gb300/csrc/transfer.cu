@@ -10,6 +10,8 @@
 // decoded into the destination.  Four internal streams (encode, D2H, H2D,
 // decode) and per-slot events let the four stages of different pieces run at
 // the same time; kRing slots of device and host buffers are reused in turn.
+// The streams and events come from a per-device pool and are reused by later
+// calls.
 // Slots start on 2 MiB boundaries (64 KiB for slots under 2 MiB): with slots
 // at the 16-byte-aligned stride of a container's maximum size, the link copies
 // of every other slot ran ~30 % slower (BF16 cache, one-layer pieces: 23.2-27.5
@@ -22,6 +24,7 @@
 // the previous piece's link copy, so the size would arrive only after that
 // copy drained and the link would idle while the host enqueued the next.)
 #include <cstring>
+#include <mutex>
 #include <vector>
 
 #include "splitzip.h"
@@ -98,9 +101,11 @@ struct Streams {
     cudaStream_t s[4] = {nullptr, nullptr, nullptr, nullptr};  // encode, D2H, H2D, decode
     cudaEvent_t info[kRing], d2h[kRing], h2d[kRing], dec[kRing];
     cudaEvent_t t0 = nullptr, t1 = nullptr, entry = nullptr;
+    cudaEvent_t join[4] = {nullptr, nullptr, nullptr, nullptr};  // each stream's last work, at the end
     bool ok = true;
     Streams() {
         for (auto& x : s) ok &= cudaStreamCreateWithFlags(&x, cudaStreamNonBlocking) == cudaSuccess;
+        for (auto& e : join) ok &= cudaEventCreateWithFlags(&e, cudaEventDisableTiming) == cudaSuccess;
         for (int k = 0; k < kRing; ++k) {
             info[k] = d2h[k] = h2d[k] = dec[k] = nullptr;
             ok &= cudaEventCreateWithFlags(&info[k], cudaEventDisableTiming) == cudaSuccess;
@@ -119,9 +124,56 @@ struct Streams {
             for (cudaEvent_t e : {info[k], d2h[k], h2d[k], dec[k]})
                 if (e) cudaEventDestroy(e);
         }
-        for (cudaEvent_t e : {t0, t1, entry})
+        for (cudaEvent_t e : {t0, t1, entry, join[0], join[1], join[2], join[3]})
             if (e) cudaEventDestroy(e);
     }
+};
+
+// Stream sets are pooled per device: a call leases one (creating it only when
+// every set is in use) and returns it, so repeated transfers (a request's
+// layers one after another) create no streams or events, and concurrent calls
+// each hold their own set.  Every wait a call issues is on an event that the
+// same call recorded first, so a set carries nothing from one call to the
+// next.  The sets live as long as the process: a static destructor could run
+// after the CUDA runtime has shut down.
+constexpr int kPoolDevices = 64;
+std::mutex g_pool_mutex;
+std::vector<Streams*> g_pool[kPoolDevices];
+
+class StreamsLease {
+  public:
+    StreamsLease() {
+        if (cudaGetDevice(&dev_) != cudaSuccess || dev_ < 0 || dev_ >= kPoolDevices) {
+            dev_ = -1;
+            return;
+        }
+        {
+            std::lock_guard<std::mutex> lock(g_pool_mutex);
+            if (!g_pool[dev_].empty()) {
+                s_ = g_pool[dev_].back();
+                g_pool[dev_].pop_back();
+            }
+        }
+        if (!s_) {
+            s_ = new Streams();
+            if (!s_->ok) {
+                delete s_;
+                s_ = nullptr;
+            }
+        }
+    }
+    ~StreamsLease() {
+        if (!s_) return;
+        std::lock_guard<std::mutex> lock(g_pool_mutex);
+        g_pool[dev_].push_back(s_);
+    }
+    StreamsLease(const StreamsLease&) = delete;
+    StreamsLease& operator=(const StreamsLease&) = delete;
+    Streams* get() const { return s_; }
+
+  private:
+    int dev_ = -1;
+    Streams* s_ = nullptr;
 };
 
 // Page-locked host memory; *mapped = its address in the device's address
@@ -170,11 +222,12 @@ extern "C" int splitzip_transfer(const void* d_src, void* d_dst, uint64_t n, int
     void* h_stage_mapped = nullptr;  // the link copies need page-locked memory
     if (!is_pinned_host(h_stage, &h_stage_mapped)) return SPLITZIP_ERR_INVALID_ARG;
 
-    Streams S;
-    if (!S.ok) {
+    const StreamsLease lease;
+    if (!lease.get()) {
         cudaGetLastError();
         return SPLITZIP_ERR_CUDA;
     }
+    Streams& S = *lease.get();
     const uint64_t eb = elem_bytes(dtype);
     const uint8_t* src = static_cast<const uint8_t*>(d_src);
     uint8_t* dst = static_cast<uint8_t*>(d_dst);
@@ -268,15 +321,9 @@ extern "C" int splitzip_transfer(const void* d_src, void* d_dst, uint64_t n, int
     }
 
     // join: the last operations of every stream before the end event
-    for (auto x : S.s) {
-        cudaEvent_t e;
-        if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) {
-            cuda_ok = false;
-            continue;
-        }
-        ok(cudaEventRecord(e, x));
-        ok(cudaStreamWaitEvent(s_dec, e, 0));
-        cudaEventDestroy(e);
+    for (int q = 0; q < 4; ++q) {
+        ok(cudaEventRecord(S.join[q], S.s[q]));
+        ok(cudaStreamWaitEvent(s_dec, S.join[q], 0));
     }
     ok(cudaEventRecord(S.t1, s_dec));
     ok(cudaStreamWaitEvent(stream, S.t1, 0));
