@@ -168,6 +168,7 @@ TRAFFIC = {
 }
 
 E2E_BLOCKS = 7  # timed blocks of the end-to-end leg (the median one is reported)
+TRANSFER_RUNS = 5  # runs of each kind in the transfer leg (medians reported)
 
 
 def sources_sha256(names):
@@ -788,22 +789,30 @@ def run_ours(args, world, rank, local):
             tpieces = int(max(1, min(32, raw_bytes // (64 << 20))))
         tpiece = -(-(-(-n // tpieces)) // CHUNK) * CHUNK
         y = torch.empty_like(x)
-        res = {}
-        for compress in (True, False):
-            tb = sz.TransferBuffers(n, dtype, tpiece, compress, CHUNK, device=device)
-            sz.transfer(x, y, cb, tb)  # warm-up
-            runs = [sz.transfer(x, y, cb, tb) for _ in range(3)]
-            torch.cuda.synchronize()
-            res[compress] = (statistics.median(r[0] for r in runs), runs[0][1], bool(torch.equal(y, x)))
-            del tb
-        z_ms, z_link, z_ok = res[True]
-        r_ms, r_link, r_ok = res[False]
+        # compressed and raw transfers alternate, so that both meet the same
+        # state of the host link (shared with the machine's other GPUs)
+        tbs = {c: sz.TransferBuffers(n, dtype, tpiece, c, CHUNK, device=device) for c in (True, False)}
+        for c in (True, False):
+            sz.transfer(x, y, cb, tbs[c])  # warm-up
+        runs = {True: [], False: []}
+        ok_all = True
+        for _ in range(TRANSFER_RUNS):
+            for c in (True, False):
+                y.zero_()
+                runs[c].append(sz.transfer(x, y, cb, tbs[c]))
+                torch.cuda.synchronize()
+                ok_all &= bool(torch.equal(y, x))
+        del tbs
+        z_ms, z_link = statistics.median(r[0] for r in runs[True]), runs[True][0][1]
+        r_ms, r_link = statistics.median(r[0] for r in runs[False]), runs[False][0][1]
         transfer = {"pieces": -(-n // tpiece), "piece_elems": tpiece, "splitzip_ms": round(z_ms, 3),
                     "raw_ms": round(r_ms, 3), "speedup": round(r_ms / z_ms, 4),
                     "link_bytes_each_way": {"splitzip": z_link, "raw": r_link},
-                    "raw_link_GBps_each_way": round(r_link / (r_ms * 1e-3) / 1e9, 1), "verified": z_ok and r_ok,
+                    "raw_link_GBps_each_way": round(r_link / (r_ms * 1e-3) / 1e9, 1), "verified": ok_all,
+                    "runs_ms": {"splitzip": [round(r[0], 3) for r in runs[True]],
+                                "raw": [round(r[0], 3) for r in runs[False]]},
                     "path": "device -> pinned host -> device copies (cudaMemcpyAsync), encode / D2H / H2D / decode "
-                            "on four streams, median of 3"}
+                            "on four streams; compressed and raw runs alternate, median of %d each" % TRANSFER_RUNS}
         del y
 
     # ---- online calibration: histogram + Top-16 on the device, then the
